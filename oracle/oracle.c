@@ -1,0 +1,291 @@
+/*
+ * fp64 CPU oracle for the TND FlashAttention forward and score-gradient.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * CPU-baseline leg of the benchmark load this library.  It shares no code,
+ * header, table or helper with the CUDA library and is never on its path.
+ *
+ * Sources (Ascend CANN operator pages):
+ *   [UnpadGrad]   "aclnnFlashAttentionUnpaddingScoreGrad"   (zh, 8.3.RC1alpha002)
+ *   [UnpadGradV5] "aclnnFlashAttentionUnpaddingScoreGradV5" (en)
+ *   [ScoreV2]     "aclnnFlashAttentionScoreV2"              (zh, news repost)
+ *
+ * What is computed, per sequence b, query head h (kv head g = h / (Nq/Nkv)),
+ * query row i and key row j of that sequence:
+ *   s_ij  = scale * <Q_i, K_j>                                [UnpadGrad, function
+ *           description: S = Mask((QK^T + pse)/sqrt(d)); scaleValue stands for
+ *           1/sqrt(d), parameters section]
+ *   kept_ij from sparseMode / preTokens / nextTokens          [UnpadGrad, parameters:
+ *           sparseMode]
+ *   m_i   = max over kept s_ij (and the sink logit if given)  [UnpadGradV5, function
+ *           description: m = max(sink, max(S))]
+ *   l_i   = sum over kept exp(s_ij - m_i) (+ exp(sink - m_i)) [UnpadGradV5, the
+ *           Attention formula's denominator]
+ *   p_ij  = exp(s_ij - m_i) / l_i  (0 if not kept or l_i = 0)
+ *   z_ij  = keep-bit / keepProb    (1 without dropout)        [UnpadGrad, function
+ *           description: P = Dropout(Softmax(S), keep_prob); parameters:
+ *           dropMaskOptional size (sum_b sum_n Sq*Skv)/8, keepProb = share of 1s]
+ *   O_i   = sum_j p_ij z_ij V_j                                [UnpadGrad: Y = P V]
+ * and the gradient:
+ *   dP_ij = <dY_i, V_j>,   D_i = <dY_i, O_i>
+ *   dS_ij = p_ij (z_ij dP_ij - D_i)
+ *   dV_j  = sum_{h in g} sum_i p_ij z_ij dY_i                  [UnpadGrad: dV = P^T dY]
+ *   dQ_i  = scale * sum_j dS_ij K_j                            [UnpadGrad: dQ = dS K / sqrt(d)]
+ *   dK_j  = scale * sum_{h in g} sum_i dS_ij Q_i               [UnpadGrad: dK = dS^T Q / sqrt(d)]
+ *   dSink_h = - sum_b sum_i (exp(sink_h - m_i) / l_i) D_i      [UnpadGradV5: dSink =
+ *           reduce(-P * dP * SimpleSoftmax(sink, x_max, x_sum)), with
+ *           sum_j P_ij dP_ij read as D_i]
+ *
+ * Readings taken where the pages are silent (all listed in the design notes):
+ *   - dS is the derivative of the stated forward: with P the pre-dropout softmax
+ *     and dropout applied as P*z, d(sum dY*O)/ds_ij = p_ij (z_ij dP_ij - D_i).
+ *   - sparseMode 3 keeps j <= i + (Skv - Sq) (lower triangle anchored at the
+ *     bottom-right vertex); mode 2 keeps j <= i (top-left vertex); mode 4 keeps
+ *     -preTokens <= j - i <= nextTokens; mode 0 (no attention-mask tensor) keeps
+ *     everything and ignores preTokens/nextTokens.
+ *   - keep-bit of (b, h, i, j) sits at flat index
+ *     base_b + (h*Sq_b + i)*Skv_b + j, base_b = sum_{b'<b} Nq*Sq_b'*Skv_b',
+ *     byte = index >> 3, bit = index & 7 (least significant bit first).
+ *   - a row with no kept key and no sink has m = -inf, l = 0, O = 0 and
+ *     contributes nothing to the gradient.
+ *
+ * Everything is plain fp64 loops over rows; the selection fields of
+ * ora_problem (head range, first row per sequence) only narrow loop bounds so
+ * that tests can evaluate part of a large problem.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct ora_problem {
+    int64_t B;
+    const int64_t *cu_q;    /* B+1 cumulative query offsets, cu_q[0] = 0        */
+    const int64_t *cu_kv;   /* B+1 cumulative key/value offsets                 */
+    int64_t Nq, Nkv, D;
+    double scale;           /* scaleValue                                       */
+    double keep_prob;       /* keepProb in (0, 1]                               */
+    int64_t pre_tokens, next_tokens, sparse_mode;
+    const uint8_t *drop_mask; /* packed keep-bits, NULL = no dropout            */
+    const double *sink;       /* [Nq] sink logits, NULL = no sink               */
+    /* selection: heads [h_lo, h_hi) and rows i >= row_lo[b] (NULL = all rows) */
+    int64_t h_lo, h_hi;
+    const int64_t *row_lo;
+} ora_problem;
+
+/* sparseMode predicate; [UnpadGrad, parameters: sparseMode]. */
+int ora_keep(int64_t mode, int64_t pre, int64_t next, int64_t sq, int64_t skv,
+             int64_t i, int64_t j)
+{
+    switch (mode) {
+    case 0: return 1;                                  /* no attenMask: keep all */
+    case 2: return j <= i;                             /* leftUpCausal           */
+    case 3: return j <= i + (skv - sq);                /* rightDownCausal        */
+    case 4: return (j - i >= -pre) && (j - i <= next); /* band                   */
+    default: return 0;
+    }
+}
+
+/* first flat keep-bit index of sequence b */
+int64_t ora_mask_base(const ora_problem *p, int64_t b)
+{
+    int64_t base = 0;
+    for (int64_t bb = 0; bb < b; ++bb) {
+        base += p->Nq * (p->cu_q[bb + 1] - p->cu_q[bb]) * (p->cu_kv[bb + 1] - p->cu_kv[bb]);
+    }
+    return base;
+}
+
+int ora_keep_bit(const uint8_t *mask, int64_t index)
+{
+    return (mask[index >> 3] >> (index & 7)) & 1;
+}
+
+/* z_ij: dropout multiplier of one (b, h, i, j) */
+static double drop_z(const ora_problem *p, int64_t base, int64_t h, int64_t i, int64_t j,
+                     int64_t sq, int64_t skv)
+{
+    if (p->drop_mask == NULL || p->keep_prob >= 1.0) return 1.0;
+    int64_t index = base + (h * sq + i) * skv + j;
+    return ora_keep_bit(p->drop_mask, index) ? 1.0 / p->keep_prob : 0.0;
+}
+
+static double dot(const double *a, const double *b, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t d = 0; d < n; ++d) acc += a[d] * b[d];
+    return acc;
+}
+
+static int row_selected(const ora_problem *p, int64_t b, int64_t i)
+{
+    return p->row_lo == NULL || i >= p->row_lo[b];
+}
+
+/* scores s_ij of row (b, h, i) into s[0..skv), kept flags into kept[] */
+static void row_scores(const ora_problem *p, const double *q, const double *k,
+                       int64_t b, int64_t h, int64_t i, double *s, unsigned char *kept)
+{
+    const int64_t G = p->Nq / p->Nkv, g = h / G, D = p->D;
+    const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
+    const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
+    const double *qi = q + ((tq + i) * p->Nq + h) * D;
+    for (int64_t j = 0; j < skv; ++j) {
+        kept[j] = (unsigned char)ora_keep(p->sparse_mode, p->pre_tokens, p->next_tokens, sq, skv, i, j);
+        s[j] = kept[j] ? p->scale * dot(qi, k + ((tk + j) * p->Nkv + g) * D, D) : 0.0;
+    }
+}
+
+/* m_i and l_i of one row from its scores; [UnpadGradV5] sink formulas */
+static void row_max_sum(const ora_problem *p, int64_t h, const double *s, const unsigned char *kept,
+                        int64_t skv, double *m_out, double *l_out)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < skv; ++j)
+        if (kept[j] && s[j] > m) m = s[j];
+    if (p->sink && p->sink[h] > m) m = p->sink[h];
+    double l = 0.0;
+    if (m > -INFINITY) {
+        for (int64_t j = 0; j < skv; ++j)
+            if (kept[j]) l += exp(s[j] - m);
+        if (p->sink) l += exp(p->sink[h] - m);
+    }
+    *m_out = m;
+    *l_out = l;
+}
+
+static int64_t max_skv(const ora_problem *p)
+{
+    int64_t mx = 1;
+    for (int64_t b = 0; b < p->B; ++b) {
+        int64_t s = p->cu_kv[b + 1] - p->cu_kv[b];
+        if (s > mx) mx = s;
+    }
+    return mx;
+}
+
+/*
+ * Forward: out [Tq][Nq][D], smax / ssum [Tq][Nq] (natural-log units).
+ * [UnpadGrad] Y = Dropout(Softmax(Mask(scale QK^T)), keep_prob) V, with the
+ * forward's max and sum as described for softmaxMax / softmaxSum [ScoreV2].
+ */
+int ora_fwd(const ora_problem *p, const double *q, const double *k, const double *v,
+            double *out, double *smax, double *ssum)
+{
+    const int64_t D = p->D, G = p->Nq / p->Nkv;
+    const int64_t nunits = p->B * p->Nq, skvmax = max_skv(p);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < nunits; ++u) {
+        const int64_t b = u / p->Nq, h = u % p->Nq, g = h / G;
+        if (h < p->h_lo || h >= p->h_hi) continue;
+        const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
+        const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
+        const int64_t base = ora_mask_base(p, b);
+        double *s = (double *)malloc(sizeof(double) * skvmax);
+        unsigned char *kept = (unsigned char *)malloc(skvmax);
+        if (!s || !kept) { err = 1; free(s); free(kept); continue; }
+        for (int64_t i = 0; i < sq; ++i) {
+            if (!row_selected(p, b, i)) continue;
+            double m, l;
+            row_scores(p, q, k, b, h, i, s, kept);
+            row_max_sum(p, h, s, kept, skv, &m, &l);
+            double *o = out + ((tq + i) * p->Nq + h) * D;
+            for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+            if (l > 0.0) {
+                for (int64_t j = 0; j < skv; ++j) {
+                    if (!kept[j]) continue;
+                    double w = exp(s[j] - m) / l * drop_z(p, base, h, i, j, sq, skv);
+                    const double *vj = v + ((tk + j) * p->Nkv + g) * D;
+                    for (int64_t d = 0; d < D; ++d) o[d] += w * vj[d];
+                }
+            }
+            smax[(tq + i) * p->Nq + h] = m;
+            ssum[(tq + i) * p->Nq + h] = l;
+        }
+        free(s);
+        free(kept);
+    }
+    return err;
+}
+
+/*
+ * Gradient from the forward's out / smax / ssum (as the grad operator consumes
+ * attentionIn, softmaxMax and softmaxSum [UnpadGrad, parameters]).
+ * dq like q; dk, dv like k; dsink [Nq] (may be NULL without a sink).
+ * ds_dense (may be NULL): dS at the flat keep-bit index of every (b,h,i,j).
+ * Only selected heads / rows are written; dk / dv of every kv row of every
+ * selected kv group are overwritten (they sum over the selected rows only).
+ */
+int ora_grad(const ora_problem *p, const double *q, const double *k, const double *v,
+             const double *dy, const double *out, const double *smax, const double *ssum,
+             double *dq, double *dk, double *dv, double *dsink, double *ds_dense)
+{
+    const int64_t D = p->D, G = p->Nq / p->Nkv;
+    const int64_t nunits = p->B * p->Nkv, skvmax = max_skv(p);
+    double *sink_part = (double *)calloc((size_t)(nunits * G), sizeof(double));
+    if (!sink_part) return 1;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < nunits; ++u) {
+        const int64_t b = u / p->Nkv, g = u % p->Nkv;
+        if ((g + 1) * G <= p->h_lo || g * G >= p->h_hi) continue;
+        const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
+        const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
+        const int64_t base = ora_mask_base(p, b);
+        double *s = (double *)malloc(sizeof(double) * skvmax);
+        unsigned char *kept = (unsigned char *)malloc(skvmax);
+        if (!s || !kept) { err = 1; free(s); free(kept); continue; }
+        for (int64_t j = 0; j < skv; ++j) {
+            double *dkj = dk + ((tk + j) * p->Nkv + g) * D, *dvj = dv + ((tk + j) * p->Nkv + g) * D;
+            for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+        }
+        for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+            if (h < p->h_lo || h >= p->h_hi) continue;
+            for (int64_t i = 0; i < sq; ++i) {
+                if (!row_selected(p, b, i)) continue;
+                const int64_t r = (tq + i) * p->Nq + h;
+                const double *qi = q + r * D, *dyi = dy + r * D, *oi = out + r * D;
+                double *dqi = dq + r * D;
+                const double m = smax[r], l = ssum[r];
+                const double Di = dot(dyi, oi, D);
+                for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
+                row_scores(p, q, k, b, h, i, s, kept);
+                for (int64_t j = 0; j < skv; ++j) {
+                    if (!kept[j] || !(l > 0.0)) continue;
+                    const double *kj = k + ((tk + j) * p->Nkv + g) * D;
+                    const double *vj = v + ((tk + j) * p->Nkv + g) * D;
+                    double *dkj = dk + ((tk + j) * p->Nkv + g) * D;
+                    double *dvj = dv + ((tk + j) * p->Nkv + g) * D;
+                    const double pij = exp(s[j] - m) / l;
+                    const double z = drop_z(p, base, h, i, j, sq, skv);
+                    const double dP = dot(dyi, vj, D);
+                    const double dS = pij * (z * dP - Di);
+                    for (int64_t d = 0; d < D; ++d) {
+                        dqi[d] += p->scale * dS * kj[d];
+                        dkj[d] += p->scale * dS * qi[d];
+                        dvj[d] += pij * z * dyi[d];
+                    }
+                    if (ds_dense) ds_dense[base + (h * sq + i) * skv + j] = dS;
+                }
+                if (p->sink && l > 0.0) sink_part[u * G + (h - g * G)] -= exp(p->sink[h] - m) / l * Di;
+            }
+        }
+        free(s);
+        free(kept);
+    }
+    if (dsink) {
+        for (int64_t h = p->h_lo; h < p->h_hi; ++h) dsink[h] = 0.0;
+        if (p->sink) {
+            for (int64_t u = 0; u < nunits; ++u) {       /* fixed order over (b, g) */
+                const int64_t g = u % p->Nkv;
+                for (int64_t hh = 0; hh < G; ++hh) {
+                    const int64_t h = g * G + hh;
+                    if (h >= p->h_lo && h < p->h_hi) dsink[h] += sink_part[u * G + hh];
+                }
+            }
+        }
+    }
+    free(sink_part);
+    return err;
+}

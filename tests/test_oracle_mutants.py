@@ -1,0 +1,72 @@
+"""The oracle pins must catch plausible mistakes.
+
+Each case copies the oracle source, plants one mistake (a dropped term, a
+wrong sign, index or anchor, a transposed layout), compiles the copy on the
+CPU and checks that the pins of test_oracle_pins reject it.
+"""
+
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "ds_without_rowsum_term": ("pij * (z * dP - Di)", "pij * (z * dP)"),
+    "dk_without_scale": ("dkj[d] += p->scale * dS * qi[d]", "dkj[d] += dS * qi[d]"),
+    "dv_without_dropout": ("dvj[d] += pij * z * dyi[d]", "dvj[d] += pij * dyi[d]"),
+    "causal_top_left_anchor": ("case 3: return j <= i + (skv - sq);", "case 3: return j <= i;"),
+    "bit_index_row_major_heads": ("int64_t index = base + (h * sq + i) * skv + j;",
+                                  "int64_t index = base + (i * p->Nq + h) * skv + j;"),
+    "sink_missing_from_sum": ("if (p->sink) l += exp(p->sink[h] - m);", ""),
+    "dsink_wrong_sign": ("sink_part[u * G + (h - g * G)] -= ", "sink_part[u * G + (h - g * G)] += "),
+    "gqa_interleaved_heads": ("const int64_t G = p->Nq / p->Nkv, g = h / G, D = p->D;",
+                              "const int64_t G = p->Nq / p->Nkv, g = h % p->Nkv, D = p->D;"),
+    "band_exclusive_edge": ("(j - i >= -pre) && (j - i <= next)", "(j - i > -pre) && (j - i <= next)"),
+}
+
+
+def _pin_suite(ora):
+    """Run the pins that exercise every term; True if all pass."""
+    try:
+        for ci in range(len(pins.CASES)):
+            pins.test_forward_and_grad_match_autograd(ora, ci)
+        for mode, pre, nxt in [(3, pins.INF, pins.INF), (4, 3, 0), (4, 2, 3)]:
+            for sq, skv in [(5, 9), (7, 7)]:
+                pins.test_mask_predicate_matches_explicit_matrix(ora, mode, pre, nxt, sq, skv)
+        pins.test_dropout_bit_layout_bruteforce(ora)
+        pins.test_ds_row_sums(ora, True)
+        pins.test_gqa_equals_repeated_mha(ora)
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_planted_mistake(name):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, name
+    with tempfile.TemporaryDirectory() as tmp:
+        src = os.path.join(tmp, "mutant.c")
+        so = os.path.join(tmp, "libmutant.so")
+        open(src, "w").write(text.replace(old, new))
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", src, "-o", so, "-lm"])
+        oracle.build()
+        prev = oracle.use_library(oracle.bind(so))
+        try:
+            assert not _pin_suite(oracle), f"pins accepted the planted mistake {name}"
+        finally:
+            oracle.use_library(prev)
+
+
+def test_unmutated_source_passes_suite():
+    oracle.build()
+    oracle.use_library(None)
+    assert _pin_suite(oracle)

@@ -1,0 +1,362 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against something fixed independently: the
+closed form of the all-ones sample program on the aclnnFlashAttentionScoreV2
+page (example section), torch autograd of the textbook attention forward,
+central finite differences, closed forms (Q = 0, causal / band pair counts),
+brute-force mask matrices and bit layouts, and exact identities (row sums of
+dS, bilinear identities, GQA = repeated MHA, varlen = concatenation).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from tests.oracle_pins_helpers import (autograd_reference, mask_matrix, random_bits,
+                                       random_problem, scale_for)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+INF = 2147483647
+
+
+def _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, **kw):
+    return ora.Problem(cu_q, cu_kv, nq, nkv, d, scale, **kw)
+
+
+# --------------------------------------------------------------------------
+# worked example of the forward page
+# --------------------------------------------------------------------------
+
+def test_allones_sample_forward_and_grad(ora):
+    fx = json.load(open(os.path.join(GOLDEN, "scorev2_allones_sample.json")))
+    inp, exp_ = fx["inputs"], fx["expected"]
+    T, N, D = inp["tnd_relayout"]["T"], inp["tnd_relayout"]["N"], inp["tnd_relayout"]["D"]
+    q = np.full((T, N, D), inp["q_value"])
+    k = np.full((T, N, D), inp["k_value"])
+    v = np.full((T, N, D), inp["v_value"])
+    p = _problem(ora, inp["tnd_relayout"]["cu_seqlens"], inp["tnd_relayout"]["cu_seqlens"], N, N, D,
+                 inp["scaleValue"], keep_prob=inp["keepProb"], pre_tokens=inp["preTokens"],
+                 next_tokens=inp["nextTokens"], sparse_mode=inp["sparseMode"])
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    np.testing.assert_allclose(smax, exp_["softmax_max"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ssum, exp_["softmax_sum"], rtol=0, atol=1e-9)
+    np.testing.assert_allclose(out, exp_["attention_out"], rtol=0, atol=1e-12)
+    dy = np.random.default_rng(5).standard_normal((T, N, D))
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    assert np.abs(dq).max() <= 1e-9 and np.abs(dk).max() <= 1e-9
+    np.testing.assert_allclose(dv, np.broadcast_to(dy.mean(axis=0), dv.shape), rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# masks
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode,pre,nxt", [(0, INF, INF), (2, INF, INF), (3, INF, INF), (4, 3, 0),
+                                          (4, 0, 2), (4, 5, 4), (4, 2, -1), (4, -1, 3)])
+@pytest.mark.parametrize("sq,skv", [(7, 7), (5, 9), (9, 5), (1, 13), (13, 1), (8, 8)])
+def test_mask_predicate_matches_explicit_matrix(ora, mode, pre, nxt, sq, skv):
+    ref = mask_matrix(mode, pre, nxt, sq, skv)
+    got = np.array([[ora.keep(mode, pre, nxt, sq, skv, i, j) for j in range(skv)] for i in range(sq)],
+                   dtype=bool).reshape(sq, skv)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_mask_pair_counts_closed_forms(ora):
+    # causal: S(S+1)/2 kept pairs per (sequence, head)
+    for s in (1, 2, 37, 64, 130):
+        n = sum(ora.keep(3, INF, INF, s, s, i, j) for i in range(s) for j in range(s))
+        assert n == s * (s + 1) // 2
+    # band preTokens=W, nextTokens=0 over S rows: sum_i (min(i, W) + 1)
+    S, W = 200, 17
+    n = sum(ora.keep(4, W, 0, S, S, i, j) for i in range(S) for j in range(S))
+    assert n == W * (W + 1) // 2 + (S - W) * (W + 1)
+    # the sliding-window workload: 8192 rows, window 1024 back -> 7,872,000 pairs
+    S, W = 8192, 1024
+    assert W * (W + 1) // 2 + (S - W) * (W + 1) == 7_872_000
+    kept_rows = np.array([sum(ora.keep(4, W, 0, S, S, i, j) for j in range(max(0, i - W - 2), i + 3))
+                          for i in (0, 1, 500, 1023, 1024, 1025, 5000, 8191)])
+    np.testing.assert_array_equal(kept_rows, [1, 2, 501, 1024, 1025, 1025, 1025, 1025])
+
+
+def test_mask_mode_equivalences(ora):
+    for s in (1, 6, 11):
+        for i in range(s):
+            for j in range(s):
+                c3 = ora.keep(3, INF, INF, s, s, i, j)
+                assert c3 == ora.keep(2, INF, INF, s, s, i, j) == ora.keep(4, INF, 0, s, s, i, j)
+                assert ora.keep(4, s, s, s, s, i, j) == ora.keep(0, INF, INF, s, s, i, j) == 1
+
+
+# --------------------------------------------------------------------------
+# dropout keep-bit layout
+# --------------------------------------------------------------------------
+
+def test_dropout_bit_layout_bruteforce(ora):
+    rng = np.random.default_rng(11)
+    seq_q, seq_kv, nq = [3, 0, 5, 9], [7, 4, 0, 13], 3
+    shapes = [(nq, a, b) for a, b in zip(seq_q, seq_kv)]
+    tensors, packed = random_bits(rng, shapes, 0.5)
+    cu_q = np.concatenate([[0], np.cumsum(seq_q)])
+    cu_kv = np.concatenate([[0], np.cumsum(seq_kv)])
+    p = _problem(ora, cu_q, cu_kv, nq, 1, 4, 1.0, keep_prob=0.5, drop_mask=packed)
+    assert p.mask_bits() == sum(int(np.prod(s)) for s in shapes)
+    assert packed.size == (p.mask_bits() + 7) // 8
+    for b, t in enumerate(tensors):
+        base = p.mask_base(b)
+        for h in range(nq):
+            for i in range(seq_q[b]):
+                for j in range(seq_kv[b]):
+                    assert ora.keep_bit(packed, base + (h * seq_q[b] + i) * seq_kv[b] + j) == int(t[h, i, j])
+
+
+def test_all_ones_dropout_mask_scales_by_inverse_keep_prob(ora):
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(3, [5, 7], [6, 7], 2, 1, 8)
+    base = _problem(ora, cu_q, cu_kv, 2, 1, 8, 0.3, sparse_mode=3)
+    nbits = base.mask_bits()
+    ones = np.packbits(np.ones(nbits, bool), bitorder="little")
+    kp = 0.8
+    drop = _problem(ora, cu_q, cu_kv, 2, 1, 8, 0.3, sparse_mode=3, keep_prob=kp, drop_mask=ones)
+    same = _problem(ora, cu_q, cu_kv, 2, 1, 8, 0.3, sparse_mode=3, keep_prob=1.0, drop_mask=ones)
+    o0, m0, l0 = ora.fwd(base, q, k, v)
+    o1, m1, l1 = ora.fwd(drop, q, k, v)
+    o2, _, _ = ora.fwd(same, q, k, v)
+    np.testing.assert_allclose(o1, o0 / kp, rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(o2, o0)
+    np.testing.assert_array_equal(m1, m0)
+    np.testing.assert_array_equal(l1, l0)
+
+
+# --------------------------------------------------------------------------
+# forward and gradient against torch autograd of the textbook formula
+# --------------------------------------------------------------------------
+
+CASES = [
+    # seqlens_q, seqlens_kv, nq, nkv, d, mode, pre, nxt, dropout, sink
+    ([5, 9], [5, 9], 2, 2, 8, 0, INF, INF, False, False),
+    ([5, 9], [5, 9], 2, 2, 8, 3, INF, INF, False, False),
+    ([6, 3], [9, 3], 4, 2, 8, 3, INF, INF, False, False),   # Sq < Skv, GQA
+    ([9, 4], [6, 4], 2, 1, 8, 3, INF, INF, False, False),   # Sq > Skv: fully masked rows
+    ([7, 0, 5], [7, 3, 5], 2, 2, 4, 2, INF, INF, False, False),
+    ([8, 11], [8, 11], 4, 1, 8, 4, 3, 0, False, False),
+    ([8, 11], [8, 11], 2, 2, 8, 4, 2, 3, True, False),
+    ([6, 5], [6, 5], 2, 2, 8, 3, INF, INF, True, True),
+    ([6, 0, 9], [6, 2, 9], 3, 1, 4, 0, INF, INF, False, True),
+    ([4, 7], [0, 7], 2, 1, 4, 3, INF, INF, True, True),      # a sequence with no keys
+]
+
+
+def _case(ora, case, seed=0):
+    sq, skv, nq, nkv, d, mode, pre, nxt, drop, sink = case
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(100 + seed, sq, skv, nq, nkv, d)
+    scale = scale_for(d) * 1.7
+    bits, packed, kp = None, None, 1.0
+    if drop:
+        bits, packed = random_bits(rng, [(nq, a, b) for a, b in zip(sq, skv)], 0.75)
+        kp = 0.75
+    snk = rng.standard_normal(nq) if sink else None
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, keep_prob=kp, pre_tokens=pre, next_tokens=nxt,
+                 sparse_mode=mode, drop_mask=packed, sink=snk)
+    ref = autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, mode=mode, pre=pre, nxt=nxt,
+                             bits=bits, keep_prob=kp, sink=snk)
+    return p, (q, k, v, dy), ref
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_forward_and_grad_match_autograd(ora, ci):
+    p, (q, k, v, dy), ref = _case(ora, CASES[ci], ci)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-12)
+    fin = np.isfinite(ref["smax"])
+    np.testing.assert_array_equal(np.isfinite(smax), fin)
+    np.testing.assert_allclose(smax[fin], ref["smax"][fin], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(ssum[~np.isnan(ref["ssum"])], ref["ssum"][~np.isnan(ref["ssum"])],
+                               rtol=1e-12, atol=1e-13)
+    dq, dk, dv, dsink = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    np.testing.assert_allclose(dq, ref["dq"], rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dk, ref["dk"], rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dv, ref["dv"], rtol=1e-10, atol=1e-11)
+    if ref["dsink"] is not None:
+        np.testing.assert_allclose(dsink, ref["dsink"], rtol=1e-10, atol=1e-11)
+    else:
+        assert np.all(dsink == 0)
+
+
+# --------------------------------------------------------------------------
+# finite differences of L = sum(dY * O) through the oracle's own forward
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ci", [1, 2, 5, 6, 7, 9])
+def test_grad_matches_central_differences(ora, ci):
+    p, (q, k, v, dy), _ = _case(ora, CASES[ci], ci)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, dv, dsink = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    h = 1e-6
+    rng = np.random.default_rng(ci)
+
+    def loss(qq, kk, vv):
+        o, _, _ = ora.fwd(p, qq, kk, vv)
+        return float(np.sum(o * dy))
+
+    for name, arr, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(12):
+            idx = tuple(rng.integers(0, n) for n in arr.shape)
+            a1, a2 = arr.copy(), arr.copy()
+            a1[idx] += h
+            a2[idx] -= h
+            args1 = {"q": q, "k": k, "v": v}
+            args2 = dict(args1)
+            args1[name], args2[name] = a1, a2
+            fd = (loss(args1["q"], args1["k"], args1["v"]) - loss(args2["q"], args2["k"], args2["v"])) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+    if p.sink is not None:
+        for hh in range(p.nq):
+            s1, s2 = p.sink.copy(), p.sink.copy()
+            s1[hh] += h
+            s2[hh] -= h
+            p1 = ora.Problem(p.cu_q, p.cu_kv, p.nq, p.nkv, p.d, p._c.scale, p._c.keep_prob,
+                             p._c.pre_tokens, p._c.next_tokens, p._c.sparse_mode, p.drop_mask, s1)
+            p2 = ora.Problem(p.cu_q, p.cu_kv, p.nq, p.nkv, p.d, p._c.scale, p._c.keep_prob,
+                             p._c.pre_tokens, p._c.next_tokens, p._c.sparse_mode, p.drop_mask, s2)
+            fd = (np.sum(ora.fwd(p1, q, k, v)[0] * dy) - np.sum(ora.fwd(p2, q, k, v)[0] * dy)) / (2 * h)
+            assert abs(fd - dsink[hh]) <= 1e-6 * max(1.0, abs(dsink[hh])), (hh, fd, dsink[hh])
+
+
+# --------------------------------------------------------------------------
+# closed forms and exact identities
+# --------------------------------------------------------------------------
+
+def test_q_zero_closed_form(ora):
+    """Q = 0, no mask, no dropout: every probability is 1/Skv, so
+    dV_j = (1/Skv) sum_i dY_i (summed over the group's heads) and dK = 0."""
+    seq = [6, 10]
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(7, seq, seq, 4, 2, 8)
+    q[:] = 0.0
+    p = _problem(ora, cu_q, cu_kv, 4, 2, 8, 0.5)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    assert np.all(dk == 0.0)
+    for b in range(2):
+        t0, t1 = cu_q[b], cu_q[b + 1]
+        for g in range(2):
+            expect = dy[t0:t1, 2 * g:2 * g + 2, :].sum(axis=(0, 1)) / seq[b]
+            np.testing.assert_allclose(dv[t0:t1, g, :], np.broadcast_to(expect, (seq[b], 8)),
+                                       rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(out[t0:t1], np.broadcast_to(
+            np.repeat(v[t0:t1].mean(axis=0), 2, axis=0), out[t0:t1].shape), rtol=1e-13, atol=1e-14)
+
+
+def test_identical_value_rows_give_zero_ds(ora):
+    """All V rows equal: dP_ij = D_i, so dS = 0 and dQ = dK = 0 (any mask)."""
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(8, [7, 5], [7, 5], 2, 2, 8)
+    v[:] = rng.standard_normal(8)
+    p = _problem(ora, cu_q, cu_kv, 2, 2, 8, 0.4, sparse_mode=3)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+
+
+@pytest.mark.parametrize("sink", [False, True])
+def test_ds_row_sums(ora, sink):
+    """Without sink every row of dS sums to 0; with a sink the sum of dS over a
+    head plus that head's dSink is 0."""
+    seq_q, seq_kv, nq = [6, 9], [8, 9], 2
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(9, seq_q, seq_kv, nq, 1, 8)
+    bits, packed = random_bits(rng, [(nq, a, b) for a, b in zip(seq_q, seq_kv)], 0.6)
+    snk = rng.standard_normal(nq) if sink else None
+    p = _problem(ora, cu_q, cu_kv, nq, 1, 8, 0.35, sparse_mode=3, keep_prob=0.6, drop_mask=packed, sink=snk)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, dv, dsink, ds = ora.grad(p, q, k, v, dy, out, smax, ssum, want_ds=True)
+    per_head = np.zeros(nq)
+    for b in range(2):
+        base = p.mask_base(b)
+        blk = ds[base: base + nq * seq_q[b] * seq_kv[b]].reshape(nq, seq_q[b], seq_kv[b])
+        if not sink:
+            np.testing.assert_allclose(blk.sum(axis=2), 0.0, atol=1e-13)
+        per_head += blk.sum(axis=(1, 2))
+    if sink:
+        np.testing.assert_allclose(per_head + dsink, 0.0, atol=1e-12)
+        assert np.abs(dsink).max() > 1e-3
+
+
+def test_bilinear_identities(ora):
+    """<dQ,Q> = <dK,K> (per kv group) and <dV,V> = <dY,O>."""
+    p, (q, k, v, dy), _ = _case(ora, CASES[6], 6)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    G = p.nq // p.nkv
+    for g in range(p.nkv):
+        lhs = np.sum(dq[:, g * G:(g + 1) * G] * q[:, g * G:(g + 1) * G])
+        rhs = np.sum(dk[:, g] * k[:, g])
+        assert abs(lhs - rhs) < 1e-10 * max(1, abs(lhs))
+    assert abs(np.sum(dv * v) - np.sum(dy * out)) < 1e-10 * max(1, abs(np.sum(dy * out)))
+
+
+def test_gqa_equals_repeated_mha(ora):
+    seq = [7, 12]
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(12, seq, seq, 6, 2, 8)
+    pg = _problem(ora, cu_q, cu_kv, 6, 2, 8, 0.3, sparse_mode=3)
+    pm = _problem(ora, cu_q, cu_kv, 6, 6, 8, 0.3, sparse_mode=3)
+    kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+    og, mg, lg, dqg, dkg, dvg, _ = ora.fwd_grad(pg, q, k, v, dy)
+    om, mm, lm, dqm, dkm, dvm, _ = ora.fwd_grad(pm, q, kr, vr, dy)
+    np.testing.assert_allclose(og, om, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dqg, dqm, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dkg, dkm.reshape(-1, 2, 3, 8).sum(axis=2), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dvg, dvm.reshape(-1, 2, 3, 8).sum(axis=2), rtol=1e-12, atol=1e-13)
+
+
+def test_varlen_equals_concatenated_runs(ora):
+    seq_q, seq_kv = [5, 0, 11, 3], [6, 4, 11, 3]
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(13, seq_q, seq_kv, 2, 1, 8)
+    snk = rng.standard_normal(2)
+    p = _problem(ora, cu_q, cu_kv, 2, 1, 8, 0.3, sparse_mode=3, sink=snk)
+    full = ora.fwd_grad(p, q, k, v, dy)
+    dsink_total = np.zeros(2)
+    for b in range(4):
+        a0, a1, c0, c1 = cu_q[b], cu_q[b + 1], cu_kv[b], cu_kv[b + 1]
+        pb = _problem(ora, [0, a1 - a0], [0, c1 - c0], 2, 1, 8, 0.3, sparse_mode=3, sink=snk)
+        part = ora.fwd_grad(pb, q[a0:a1], k[c0:c1], v[c0:c1], dy[a0:a1])
+        np.testing.assert_allclose(full[0][a0:a1], part[0], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(full[3][a0:a1], part[3], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(full[4][c0:c1], part[4], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(full[5][c0:c1], part[5], rtol=1e-13, atol=1e-14)
+        dsink_total += part[6]
+    np.testing.assert_allclose(full[6], dsink_total, rtol=1e-12, atol=1e-14)
+
+
+def test_very_negative_sink_equals_no_sink(ora):
+    seq = [9, 6]
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(14, seq, seq, 2, 2, 8)
+    p0 = _problem(ora, cu_q, cu_kv, 2, 2, 8, 0.3, sparse_mode=3)
+    p1 = _problem(ora, cu_q, cu_kv, 2, 2, 8, 0.3, sparse_mode=3, sink=np.array([-1e4, -1e4]))
+    r0, r1 = ora.fwd_grad(p0, q, k, v, dy), ora.fwd_grad(p1, q, k, v, dy)
+    for a, b in zip(r0[:6], r1[:6]):
+        np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+    assert np.all(r1[6] == 0.0) or np.abs(r1[6]).max() < 1e-300
+
+
+def test_forward_matches_library_softmax(ora):
+    from scipy.special import softmax
+    seq = [10]
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(15, seq, seq, 1, 1, 16)
+    p = _problem(ora, cu_q, cu_kv, 1, 1, 16, 0.25)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    ref = softmax(0.25 * q[:, 0] @ k[:, 0].T, axis=1) @ v[:, 0]
+    np.testing.assert_allclose(out[:, 0], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_selection_narrows_without_changing_values(ora):
+    p, (q, k, v, dy), _ = _case(ora, CASES[2], 2)
+    full = ora.fwd_grad(p, q, k, v, dy)
+    sel = ora.Problem(p.cu_q, p.cu_kv, p.nq, p.nkv, p.d, p._c.scale, sparse_mode=3,
+                      heads=(2, 4), row_lo=[3, 1])
+    out, smax, ssum = ora.fwd(sel, q, k, v)
+    dq, dk, dv, _ = ora.grad(sel, q, k, v, dy, full[0], full[1], full[2])
+    for b in range(2):
+        lo, hi = p.cu_q[b] + [3, 1][b], p.cu_q[b + 1]
+        np.testing.assert_array_equal(out[lo:hi, 2:4], full[0][lo:hi, 2:4])
+        np.testing.assert_array_equal(dq[lo:hi, 2:4], full[3][lo:hi, 2:4])
+    assert np.all(out[:, :2] == 0)
