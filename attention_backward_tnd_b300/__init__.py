@@ -1,0 +1,249 @@
+"""Python binding of the TND attention library (``libtndattn.so``).
+
+Argument marshalling only: every step of the forward and the gradient runs in
+the library's CUDA kernels.  The ``tnd_*`` functions mirror the C entry points
+of ``include/tnd_attn.h`` one to one (integers for device pointers and the
+stream); ``fwd`` and ``grad`` take torch CUDA tensors, allocate outputs and the
+workspace with torch, and call those entry points on the current stream.
+There is no fallback: without the built library every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtndattn.so")
+
+TND_OK, TND_ERR_NULLPTR, TND_ERR_INVALID, TND_ERR_UNSUPPORTED = 0, 1, 2, 3
+TND_ERR_WORKSPACE, TND_ERR_CUDA, TND_ERR_DEVICE_TIMEOUT, TND_ERR_DEVICE_CHECK = 4, 5, 6, 7
+TND_F16, TND_BF16, TND_F32 = 0, 1, 2
+TND_OPT_GRAD_PATH, TND_OPT_WAIT_LIMIT_MS, TND_OPT_PROFILE = 0, 1, 2
+
+# exported symbols, in header order
+SYMBOLS = ["tnd_attn_fwd_workspace_size", "tnd_attn_fwd", "tnd_attn_grad_workspace_size", "tnd_attn_grad",
+           "tnd_attn_device_status", "tnd_status_string", "tnd_attn_set_option", "tnd_attn_profile_read",
+           "tnd_attn_grad_plan"]
+
+
+class TndError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({status_text(status)})")
+        self.status = status
+
+
+_lib = None
+_i64, _u64, _f64, _vp, _int = ctypes.c_int64, ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} is missing; build it with "
+                               "attention_backward_tnd_b300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        ws_args = [_int, _i64, _i64p, _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _int, _int,
+                   ctypes.POINTER(ctypes.c_uint64)]
+        L.tnd_attn_fwd_workspace_size.argtypes = ws_args
+        L.tnd_attn_grad_workspace_size.argtypes = ws_args
+        L.tnd_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64, _i64, _i64, _f64,
+                                   _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64, _vp]
+        L.tnd_attn_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64,
+                                    _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _u64, _vp]
+        L.tnd_attn_device_status.argtypes = [_vp, _u64, _vp]
+        L.tnd_status_string.argtypes = [_int]
+        L.tnd_status_string.restype = ctypes.c_char_p
+        L.tnd_attn_set_option.argtypes = [_int, _i64]
+        L.tnd_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                                            _i64p, _int, ctypes.POINTER(ctypes.c_int), _int]
+        L.tnd_attn_grad_plan.argtypes = [_i64, _i64p, _i64p, _i64, _i64, _i64, _i64, _i64, _i64p, _i64, _i64p,
+                                         _i64p]
+        for name in SYMBOLS:
+            if name != "tnd_status_string":
+                getattr(L, name).restype = _int
+        _lib = L
+    return _lib
+
+
+def status_text(status: int) -> str:
+    try:
+        return lib().tnd_status_string(status).decode()
+    except Exception:  # pragma: no cover - library missing
+        return "?"
+
+
+def _cu(arr) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(arr, dtype=np.int64))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_i64p)
+
+
+# --- one-to-one wrappers of the C entry points --------------------------------------------
+
+def tnd_attn_fwd_workspace_size(dtype, batch, cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value,
+                                keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_sink):
+    cq, ck, out = _cu(cu_q), _cu(cu_kv), ctypes.c_uint64(0)
+    st = lib().tnd_attn_fwd_workspace_size(dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim,
+                                           scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                           int(has_drop_mask), int(has_sink), ctypes.byref(out))
+    return st, out.value
+
+
+def tnd_attn_grad_workspace_size(dtype, batch, cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value,
+                                 keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_sink):
+    cq, ck, out = _cu(cu_q), _cu(cu_kv), ctypes.c_uint64(0)
+    st = lib().tnd_attn_grad_workspace_size(dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim,
+                                            scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                            int(has_drop_mask), int(has_sink), ctypes.byref(out))
+    return st, out.value
+
+
+def tnd_attn_fwd(query, key, value, drop_mask, sink, dtype, batch, cu_q, cu_kv, head_num, kv_head_num, head_dim,
+                 scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, attention_out, softmax_max,
+                 softmax_sum, workspace, workspace_size, stream):
+    cq, ck = _cu(cu_q), _cu(cu_kv)
+    return lib().tnd_attn_fwd(query, key, value, drop_mask, sink, dtype, batch, _p(cq), _p(ck), head_num,
+                              kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                              attention_out, softmax_max, softmax_sum, workspace, workspace_size, stream)
+
+
+def tnd_attn_grad(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink, dtype, batch,
+                  cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens,
+                  sparse_mode, dq, dk, dv, dsink, workspace, workspace_size, stream):
+    cq, ck = _cu(cu_q), _cu(cu_kv)
+    return lib().tnd_attn_grad(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink,
+                               dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim, scale_value,
+                               keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv, dsink, workspace,
+                               workspace_size, stream)
+
+
+def tnd_attn_device_status(workspace, workspace_size, stream):
+    return lib().tnd_attn_device_status(workspace, workspace_size, stream)
+
+
+def tnd_status_string(status: int) -> str:
+    return lib().tnd_status_string(status).decode()
+
+
+def tnd_attn_set_option(option: int, value: int) -> int:
+    return lib().tnd_attn_set_option(option, value)
+
+
+def tnd_attn_profile_read(reset: bool = False):
+    """{kernel name: (total ms, launches)} recorded since the last reset."""
+    cap = 32
+    names = (ctypes.c_char_p * cap)()
+    ms = (ctypes.c_double * cap)()
+    n = (ctypes.c_int64 * cap)()
+    count = ctypes.c_int(0)
+    st = lib().tnd_attn_profile_read(names, ms, n, cap, ctypes.byref(count), int(reset))
+    if st != TND_OK:
+        raise TndError(st, "tnd_attn_profile_read")
+    return {names[i].decode(): (ms[i], n[i]) for i in range(count.value)}
+
+
+def tnd_attn_grad_plan(batch, cu_q, cu_kv, head_num, kv_head_num, pre_tokens, next_tokens, sparse_mode):
+    """(status, units int64 [n,5] = (b, g, j, first q block, end q block), kept pairs)."""
+    cq, ck = _cu(cu_q), _cu(cu_kv)
+    n, kept = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = lib().tnd_attn_grad_plan(batch, _p(cq), _p(ck), head_num, kv_head_num, pre_tokens, next_tokens,
+                                  sparse_mode, None, 0, ctypes.byref(n), ctypes.byref(kept))
+    if st != TND_OK:
+        return st, None, None
+    units = np.zeros((n.value, 5), dtype=np.int64)
+    st = lib().tnd_attn_grad_plan(batch, _p(cq), _p(ck), head_num, kv_head_num, pre_tokens, next_tokens,
+                                  sparse_mode, _p(units), n.value, ctypes.byref(n), ctypes.byref(kept))
+    return st, units, kept.value
+
+
+# --- torch-tensor helpers -----------------------------------------------------------------
+
+def dtype_code(t) -> int:
+    import torch
+    return {torch.float16: TND_F16, torch.bfloat16: TND_BF16, torch.float32: TND_F32}[t.dtype]
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_prob: float = 1.0,
+        pre_tokens: int = 2147483647, next_tokens: int = 2147483647, sparse_mode: int = 0, drop_mask=None,
+        sink=None, workspace=None):
+    """Forward on torch CUDA tensors: returns (out, softmax_max, softmax_sum) ([T,N,8] fp32 stats)."""
+    import torch
+    tq, nq, d = q.shape
+    nkv = k.shape[1]
+    batch = len(cu_q) - 1
+    dt = dtype_code(q)
+    st, ws_bytes = tnd_attn_fwd_workspace_size(dt, batch, cu_q, cu_kv, nq, nkv, d, scale, keep_prob, pre_tokens,
+                                               next_tokens, sparse_mode, drop_mask is not None, sink is not None)
+    if st != TND_OK:
+        raise TndError(st, "tnd_attn_fwd_workspace_size")
+    out = torch.empty_like(q)
+    smax = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
+    ssum = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(drop_mask), _ptr(sink), dt, batch, cu_q,
+                      cu_kv, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens, sparse_mode, out.data_ptr(),
+                      smax.data_ptr(), ssum.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
+    if st != TND_OK:
+        raise TndError(st, "tnd_attn_fwd")
+    return out, smax, ssum
+
+
+def grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob=1.0, pre_tokens=2147483647,
+                         next_tokens=2147483647, sparse_mode=0, has_drop=False, has_sink=False) -> int:
+    st, n = tnd_attn_grad_workspace_size(dtype_code(q), len(cu_q) - 1, cu_q, cu_kv, q.shape[1], k.shape[1],
+                                         q.shape[2], scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                         has_drop, has_sink)
+    if st != TND_OK:
+        raise TndError(st, "tnd_attn_grad_workspace_size")
+    return n
+
+
+def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_prob=1.0,
+         pre_tokens=2147483647, next_tokens=2147483647, sparse_mode=0, drop_mask=None, sink=None,
+         workspace=None, outputs=None):
+    """Gradient on torch CUDA tensors: returns (dq, dk, dv, dsink or None)."""
+    import torch
+    tq, nq, d = q.shape
+    nkv = k.shape[1]
+    batch = len(cu_q) - 1
+    dt = dtype_code(q)
+    if workspace is None:
+        n = grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                 drop_mask is not None, sink is not None)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    if outputs is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dsink = torch.empty(nq, dtype=torch.float32, device=q.device) if sink is not None else None
+    else:
+        dq, dk, dv, dsink = outputs
+    st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(drop_mask),
+                       softmax_max.data_ptr(), softmax_sum.data_ptr(), out.data_ptr(), _ptr(sink), dt, batch, cu_q,
+                       cu_kv, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens, sparse_mode, dq.data_ptr(),
+                       dk.data_ptr(), dv.data_ptr(), _ptr(dsink), workspace.data_ptr(), workspace.numel(),
+                       _stream())
+    if st != TND_OK:
+        raise TndError(st, "tnd_attn_grad")
+    return dq, dk, dv, dsink
+
+
+def device_status(workspace) -> int:
+    return tnd_attn_device_status(workspace.data_ptr(), workspace.numel(), _stream())

@@ -1,0 +1,435 @@
+// CUDA-core kernels of the TND attention library: the forward, the gradient
+// prepass (rowsum(dY o O), log2-sum-exp, sink terms), a dK/dV kernel, a dQ
+// kernel and the dSink reduction.  They serve every dtype (fp32 included)
+// and every head dim up to 256; the tensor-core gradient replaces the dK/dV
+// and dQ kernels for bf16/fp16 at D = 128.
+//
+// Formulas: "aclnnFlashAttentionUnpaddingScoreGrad", function description
+// (forward Y = Dropout(Softmax(Mask(scale Q K^T)), keep_prob) V; backward
+// dV = P^T dY, dQ = dS K * scale, dK = dS^T Q * scale) and
+// "aclnnFlashAttentionUnpaddingScoreGradV5", function description (sink:
+// m = max(sink, max S), denominator adds exp(sink - m); dSink).
+//
+// Thread layout of the row kernels: 128 threads = 32 rows x 4 lanes; lane c4
+// of a row owns columns c4, c4+4, c4+8, ...; a dot product of two rows is four
+// partial sums combined with two shuffles.  Exponentials are base 2 on
+// logits pre-multiplied by scale*log2(e).
+#include "tnd_device.cuh"
+
+#include <cmath>
+
+namespace tnd {
+namespace {
+
+constexpr int R = kSimtRows;  // rows per block
+constexpr int kThreads = 128;
+
+// Union [ulo, uhi] of the kept key ranges of the rows held by the block
+// (empty: ulo > uhi).  Every thread passes its row's range.
+__device__ __forceinline__ void block_union(int64_t lo, int64_t hi, int64_t &ulo, int64_t &uhi)
+{
+    __shared__ long long s_lo[kThreads / 32], s_hi[kThreads / 32];
+    long long a = (lo <= hi) ? lo : LLONG_MAX, b = (lo <= hi) ? hi : LLONG_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        s_lo[w] = a;
+        s_hi[w] = b;
+    }
+    __syncthreads();
+    a = s_lo[0];
+    b = s_hi[0];
+#pragma unroll
+    for (int i = 1; i < kThreads / 32; ++i) {
+        a = min(a, s_lo[i]);
+        b = max(b, s_hi[i]);
+    }
+    __syncthreads();
+    ulo = a;
+    uhi = b;
+}
+
+__device__ __forceinline__ float quad_sum(float x)
+{
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    return x;
+}
+
+// Cooperative load of rows [r0, r0+R) of a [rows, nheads, D] tensor (head hh)
+// into smem as fp32 [R][DMAX]; rows at or past `limit` read as 0.
+template <typename T, int DMAX>
+__device__ __forceinline__ void load_tile(float *dst, const T *src, int64_t row_base, int64_t r0,
+                                          int64_t limit, int nheads, int hh, int D, float mul)
+{
+    for (int e = threadIdx.x; e < R * D; e += kThreads) {
+        const int rr = e / D, cc = e - rr * D;
+        const int64_t row = r0 + rr;
+        float x = 0.0f;
+        if (row < limit) x = Elem<T>::load(src + ((row_base + row) * nheads + hh) * (int64_t)D + cc) * mul;
+        dst[rr * DMAX + cc] = x;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward: one block per (32 query rows, query head)
+// ---------------------------------------------------------------------------
+template <typename T, int DMAX>
+__global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
+{
+    constexpr int DP = DMAX / 4;
+    extern __shared__ float smem[];
+    float *Ks = smem, *Vs = smem + R * DMAX;
+    const int2 it = a.q_items[blockIdx.x];
+    const SeqDesc sd = a.seqs[it.x];
+    const int h = blockIdx.y, g = h / a.group, D = a.d;
+    const int r = threadIdx.x >> 2, c4 = threadIdx.x & 3;
+    const int64_t i = (int64_t)it.y + r;
+    const bool row_ok = i < sd.sq;
+    const T *Q = (const T *)a.q, *K = (const T *)a.k, *V = (const T *)a.v;
+    const float C = a.scale * kLog2e;
+
+    float qreg[DP], acc[DP];
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+        const int col = c4 + 4 * k;
+        qreg[k] = (row_ok && col < D) ? Elem<T>::load(Q + ((sd.tq + i) * a.nq + h) * (int64_t)D + col) * C : 0.0f;
+        acc[k] = 0.0f;
+    }
+    float m = -INFINITY, l = 0.0f;
+    if (a.has_sink) {
+        m = a.sink[h] * kLog2e;
+        l = 1.0f;
+    }
+    int64_t lo = 1, hi = 0;
+    if (row_ok) key_range(a.mask, sd.sq, sd.skv, i, lo, hi);
+    int64_t ulo, uhi;
+    block_union(lo, hi, ulo, uhi);
+
+    for (int64_t kt = (ulo <= uhi) ? (ulo / R) * R : 1; kt <= uhi; kt += R) {
+        __syncthreads();
+        load_tile<T, DMAX>(Ks, K, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
+        load_tile<T, DMAX>(Vs, V, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
+        __syncthreads();
+        for (int c = 0; c < R; ++c) {
+            const int64_t j = kt + c;
+            float s = 0.0f;
+#pragma unroll
+            for (int k = 0; k < DP; ++k) s += qreg[k] * Ks[c * DMAX + c4 + 4 * k];
+            s = quad_sum(s);
+            if (j >= lo && j <= hi) {
+                const float mn = fmaxf(m, s);
+                const float corr = ex2(m - mn);
+                const float p = ex2(s - mn);
+                const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
+                const float pz = p * z;
+                l = l * corr + p;
+#pragma unroll
+                for (int k = 0; k < DP; ++k) acc[k] = acc[k] * corr + pz * Vs[c * DMAX + c4 + 4 * k];
+                m = mn;
+            }
+        }
+    }
+    if (!row_ok) return;
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    T *O = (T *)a.o;
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+        const int col = c4 + 4 * k;
+        if (col < D) Elem<T>::store(O + ((sd.tq + i) * a.nq + h) * (int64_t)D + col, acc[k] * inv);
+    }
+    const float mnat = (m == -INFINITY) ? -INFINITY : m * kLn2;
+    const int64_t rbase = ((sd.tq + i) * a.nq + h) * 8;
+    for (int e = c4; e < 8; e += 4) {
+        a.smax[rbase + e] = mnat;
+        a.ssum[rbase + e] = l;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gradient prepass: one warp per (token, query head)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) prepass_kernel(GradArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nrows = a.tq * a.nq;
+    const T *dY = (const T *)a.dy, *O = (const T *)a.o;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < nrows; r += (int64_t)gridDim.x * 8) {
+        const int64_t t = r / a.nq;
+        const int h = (int)(r - t * a.nq);
+        float dot = 0.0f;
+        for (int c = lane; c < a.d; c += 32) dot += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
+        dot = warp_sum(dot);
+        if (lane == 0) {
+            const float m = a.smax[r * 8], l = a.ssum[r * 8];
+            const bool live = l > 0.0f;
+            a.drow[(int64_t)h * a.tq + t] = dot;
+            a.lse2[(int64_t)h * a.tq + t] = live ? m * kLog2e + lg2(l) : INFINITY;
+            if (a.has_sink) {
+                a.sinkrow[(int64_t)h * a.tq + t] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * dot : 0.0f;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one block per (32 kv rows, kv head)
+// ---------------------------------------------------------------------------
+template <typename T, int DMAX>
+__global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
+{
+    constexpr int DP = DMAX / 4;
+    extern __shared__ float smem[];
+    float *Qs = smem, *dYs = smem + R * DMAX;
+    float *lses = dYs + R * DMAX, *Ds = lses + R;
+    const int2 it = a.kv_items[blockIdx.x];
+    const SeqDesc sd = a.seqs[it.x];
+    const int g = blockIdx.y, D = a.d;
+    const int r = threadIdx.x >> 2, c4 = threadIdx.x & 3;
+    const int64_t j = (int64_t)it.y + r;
+    const bool row_ok = j < sd.skv;
+    const T *Q = (const T *)a.q, *K = (const T *)a.k, *V = (const T *)a.v, *dY = (const T *)a.dy;
+    const float C = a.scale * kLog2e;
+
+    float kreg[DP], vreg[DP], adk[DP], adv[DP];
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+        const int col = c4 + 4 * k;
+        const bool ok = row_ok && col < D;
+        const int64_t off = ((sd.tk + j) * a.nkv + g) * (int64_t)D + col;
+        kreg[k] = ok ? Elem<T>::load(K + off) * C : 0.0f;
+        vreg[k] = ok ? Elem<T>::load(V + off) : 0.0f;
+        adk[k] = 0.0f;
+        adv[k] = 0.0f;
+    }
+    const int64_t j0 = it.y, j1 = min((int64_t)it.y + R, (int64_t)sd.skv) - 1;
+    const int lane = threadIdx.x & 31;
+
+    for (int h = g * a.group; h < (g + 1) * a.group; ++h) {
+        for (int64_t qt = 0; qt < sd.sq; qt += R) {
+            // does any row of this q tile keep a key of [j0, j1]?
+            int64_t lo = 1, hi = 0;
+            if (qt + lane < sd.sq) key_range(a.mask, sd.sq, sd.skv, qt + lane, lo, hi);
+            const bool hit = (lo <= hi) && (hi >= j0) && (lo <= j1);
+            if (!__syncthreads_or(hit)) continue;
+            load_tile<T, DMAX>(Qs, Q, sd.tq, qt, sd.sq, a.nq, h, D, 1.0f);
+            load_tile<T, DMAX>(dYs, dY, sd.tq, qt, sd.sq, a.nq, h, D, 1.0f);
+            if (threadIdx.x < R) {
+                const int64_t i = qt + threadIdx.x;
+                const bool ok = i < sd.sq;
+                lses[threadIdx.x] = ok ? a.lse2[(int64_t)h * a.tq + sd.tq + i] : INFINITY;
+                Ds[threadIdx.x] = ok ? a.drow[(int64_t)h * a.tq + sd.tq + i] : 0.0f;
+            }
+            __syncthreads();
+            for (int rr = 0; rr < R; ++rr) {
+                const int64_t i = qt + rr;
+                float s = 0.0f, dp = 0.0f;
+#pragma unroll
+                for (int k = 0; k < DP; ++k) {
+                    s += Qs[rr * DMAX + c4 + 4 * k] * kreg[k];
+                    dp += dYs[rr * DMAX + c4 + 4 * k] * vreg[k];
+                }
+                s = quad_sum(s);
+                dp = quad_sum(dp);
+                int64_t rlo = 1, rhi = 0;
+                if (i < sd.sq) key_range(a.mask, sd.sq, sd.skv, i, rlo, rhi);
+                if (row_ok && j >= rlo && j <= rhi) {
+                    const float p = ex2(s - lses[rr]);
+                    const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
+                    const float pz = p * z;
+                    const float ds = p * (z * dp - Ds[rr]);
+#pragma unroll
+                    for (int k = 0; k < DP; ++k) {
+                        adv[k] += pz * dYs[rr * DMAX + c4 + 4 * k];
+                        adk[k] += ds * Qs[rr * DMAX + c4 + 4 * k];
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (!row_ok) return;
+    T *dK = (T *)a.dk, *dV = (T *)a.dv;
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+        const int col = c4 + 4 * k;
+        if (col < D) {
+            const int64_t off = ((sd.tk + j) * a.nkv + g) * (int64_t)D + col;
+            Elem<T>::store(dK + off, adk[k] * a.scale);
+            Elem<T>::store(dV + off, adv[k]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one block per (32 query rows, query head)
+// ---------------------------------------------------------------------------
+template <typename T, int DMAX>
+__global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
+{
+    constexpr int DP = DMAX / 4;
+    extern __shared__ float smem[];
+    float *Ks = smem, *Vs = smem + R * DMAX;
+    const int2 it = a.q_items[blockIdx.x];
+    const SeqDesc sd = a.seqs[it.x];
+    const int h = blockIdx.y, g = h / a.group, D = a.d;
+    const int r = threadIdx.x >> 2, c4 = threadIdx.x & 3;
+    const int64_t i = (int64_t)it.y + r;
+    const bool row_ok = i < sd.sq;
+    const T *Q = (const T *)a.q, *K = (const T *)a.k, *V = (const T *)a.v, *dY = (const T *)a.dy;
+    const float C = a.scale * kLog2e;
+
+    float qreg[DP], dyreg[DP], acc[DP];
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+        const int col = c4 + 4 * k;
+        const bool ok = row_ok && col < D;
+        const int64_t off = ((sd.tq + i) * a.nq + h) * (int64_t)D + col;
+        qreg[k] = ok ? Elem<T>::load(Q + off) * C : 0.0f;
+        dyreg[k] = ok ? Elem<T>::load(dY + off) : 0.0f;
+        acc[k] = 0.0f;
+    }
+    const float lse = row_ok ? a.lse2[(int64_t)h * a.tq + sd.tq + i] : INFINITY;
+    const float Di = row_ok ? a.drow[(int64_t)h * a.tq + sd.tq + i] : 0.0f;
+    int64_t lo = 1, hi = 0;
+    if (row_ok) key_range(a.mask, sd.sq, sd.skv, i, lo, hi);
+    int64_t ulo, uhi;
+    block_union(lo, hi, ulo, uhi);
+
+    for (int64_t kt = (ulo <= uhi) ? (ulo / R) * R : 1; kt <= uhi; kt += R) {
+        __syncthreads();
+        load_tile<T, DMAX>(Ks, K, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
+        load_tile<T, DMAX>(Vs, V, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
+        __syncthreads();
+        for (int c = 0; c < R; ++c) {
+            const int64_t j = kt + c;
+            float s = 0.0f, dp = 0.0f;
+#pragma unroll
+            for (int k = 0; k < DP; ++k) {
+                s += qreg[k] * Ks[c * DMAX + c4 + 4 * k];
+                dp += dyreg[k] * Vs[c * DMAX + c4 + 4 * k];
+            }
+            s = quad_sum(s);
+            dp = quad_sum(dp);
+            if (j >= lo && j <= hi) {
+                const float p = ex2(s - lse);
+                const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
+                const float ds = p * (z * dp - Di);
+#pragma unroll
+                for (int k = 0; k < DP; ++k) acc[k] += ds * Ks[c * DMAX + c4 + 4 * k];
+            }
+        }
+    }
+    if (!row_ok) return;
+    T *dQ = (T *)a.dq;
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+        const int col = c4 + 4 * k;
+        if (col < D) Elem<T>::store(dQ + ((sd.tq + i) * a.nq + h) * (int64_t)D + col, acc[k] * a.scale);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dSink_h = sum over all query rows of the head of -p_sink * D (fixed order)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) sink_reduce_kernel(GradArgs a)
+{
+    __shared__ float part[256];
+    const int h = blockIdx.x;
+    float acc = 0.0f;
+    for (int64_t t = threadIdx.x; t < a.tq; t += 256) acc += a.sinkrow[(int64_t)h * a.tq + t];
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) a.dsink[h] = part[0];
+}
+
+template <template <typename, int> class Launch, typename... Args>
+cudaError_t dispatch(int dtype, int d, Args &&...args)
+{
+    if (dtype == TND_BF16) {
+        if (d <= 64) return Launch<__nv_bfloat16, 64>::run(args...);
+        if (d <= 128) return Launch<__nv_bfloat16, 128>::run(args...);
+        return Launch<__nv_bfloat16, 256>::run(args...);
+    }
+    if (dtype == TND_F16) {
+        if (d <= 64) return Launch<__half, 64>::run(args...);
+        if (d <= 128) return Launch<__half, 128>::run(args...);
+        return Launch<__half, 256>::run(args...);
+    }
+    if (d <= 64) return Launch<float, 64>::run(args...);
+    if (d <= 128) return Launch<float, 128>::run(args...);
+    return Launch<float, 256>::run(args...);
+}
+
+template <typename T, int DMAX> struct FwdLaunch {
+    static cudaError_t run(const FwdArgs &a, cudaStream_t s)
+    {
+        if (a.n_q_items == 0) return cudaSuccess;
+        const size_t smem = 2 * R * DMAX * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(fwd_simt_kernel<T, DMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        fwd_simt_kernel<T, DMAX><<<dim3(a.n_q_items, a.nq), kThreads, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+};
+
+template <typename T, int DMAX> struct DkdvLaunch {
+    static cudaError_t run(const GradArgs &a, cudaStream_t s)
+    {
+        if (a.n_kv_items == 0) return cudaSuccess;
+        const size_t smem = (2 * R * DMAX + 2 * R) * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(grad_dkdv_simt_kernel<T, DMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        grad_dkdv_simt_kernel<T, DMAX><<<dim3(a.n_kv_items, a.nkv), kThreads, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+};
+
+template <typename T, int DMAX> struct DqLaunch {
+    static cudaError_t run(const GradArgs &a, cudaStream_t s)
+    {
+        if (a.n_q_items == 0) return cudaSuccess;
+        const size_t smem = 2 * R * DMAX * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(grad_dq_simt_kernel<T, DMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        grad_dq_simt_kernel<T, DMAX><<<dim3(a.n_q_items, a.nq), kThreads, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+};
+
+template <typename T, int DMAX> struct PrepassLaunch {
+    static cudaError_t run(const GradArgs &a, cudaStream_t s)
+    {
+        const int64_t rows = a.tq * a.nq;
+        if (rows == 0) return cudaSuccess;
+        const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 148 * 16);
+        prepass_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+};
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s) { return dispatch<FwdLaunch>(a.dtype, a.d, a, s); }
+cudaError_t launch_grad_dkdv_simt(const GradArgs &a, cudaStream_t s) { return dispatch<DkdvLaunch>(a.dtype, a.d, a, s); }
+cudaError_t launch_grad_dq_simt(const GradArgs &a, cudaStream_t s) { return dispatch<DqLaunch>(a.dtype, a.d, a, s); }
+
+cudaError_t launch_prepass(const GradArgs &a, bool, cudaStream_t s) { return dispatch<PrepassLaunch>(a.dtype, a.d, a, s); }
+
+cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s)
+{
+    if (!a.has_sink || a.nq == 0) return cudaSuccess;
+    sink_reduce_kernel<<<a.nq, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace tnd

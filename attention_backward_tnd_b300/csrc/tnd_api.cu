@@ -1,0 +1,589 @@
+// Host side of the C ABI declared in include/tnd_attn.h: argument checks
+// (the first phase of the pages' two-phase interface, "function prototype"
+// and "constraints" sections of aclnnFlashAttentionUnpaddingScoreGrad /
+// ...GradV5), the per-call plan (sequence table, work lists, tensor-core
+// units), the workspace layout and the kernel launches.
+#include "tnd_internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+namespace tnd {
+namespace {
+
+// ---------------------------------------------------------------------------
+// process-wide options and the kernel-time record
+// ---------------------------------------------------------------------------
+struct Options {
+    int grad_path = 0;
+    int64_t wait_limit_ms = 2000;
+    int profile = 0;
+};
+Options g_opt;
+std::mutex g_mu;
+
+struct ProfEntry {
+    int kind;
+    cudaEvent_t start, stop;
+};
+const char *kKindNames[] = {"fwd_simt", "grad_prepass", "grad_dkdv_simt", "grad_dq_simt",
+                            "grad_sink_reduce", "grad_tc_main", "grad_zero_dq"};
+constexpr int kNumKinds = sizeof(kKindNames) / sizeof(kKindNames[0]);
+enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_ZERO };
+std::vector<ProfEntry> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+constexpr size_t kProfCap = 4096;
+
+cudaEvent_t take_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Runs `launch` on stream s, bracketed by events when profiling is on.
+template <typename F>
+cudaError_t timed(int kind, cudaStream_t s, F &&launch)
+{
+    if (!g_opt.profile) return launch();
+    std::lock_guard<std::mutex> lk(g_mu);
+    cudaEvent_t a = take_event(), b = take_event();
+    if (!a || !b) return launch();
+    cudaEventRecord(a, s);
+    cudaError_t e = launch();
+    cudaEventRecord(b, s);
+    if (g_prof.size() >= kProfCap) {
+        cudaEventSynchronize(g_prof.front().stop);
+        g_event_pool.push_back(g_prof.front().start);
+        g_event_pool.push_back(g_prof.front().stop);
+        g_prof.erase(g_prof.begin());
+    }
+    g_prof.push_back({kind, a, b});
+    return e;
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+struct Problem {
+    int dtype = 0;
+    int64_t batch = 0;
+    const int64_t *cuq = nullptr, *cukv = nullptr;
+    int64_t nq = 0, nkv = 0, d = 0;
+    double scale = 0, keep = 1;
+    int64_t pre = 0, next = 0, mode = 0;
+    bool has_drop = false, has_sink = false;
+    int64_t tq = 0, tkv = 0;
+};
+
+constexpr int64_t kMaxTokens = int64_t(1) << 20;  // T in [1, 1M]
+constexpr int64_t kMaxHeads = 256;                // N in [1, 256]
+constexpr int64_t kMaxHeadDim = 768;              // D in [1, 768] (V5 page)
+constexpr int64_t kMaxBatch = 20000;              // B in [1, 20000] (V5 page)
+constexpr int64_t kSimtMaxHeadDim = 256;          // this build's CUDA-core kernels
+
+tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq,
+                    int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next,
+                    int64_t mode, bool has_drop, bool has_sink, Problem &p)
+{
+    if (!cuq || !cukv) return TND_ERR_NULLPTR;
+    if (keep < 1.0 && !has_drop) return TND_ERR_NULLPTR;  // dropMask needed when keepProb < 1
+    if (dtype != TND_F16 && dtype != TND_BF16 && dtype != TND_F32) return TND_ERR_INVALID;
+    if (batch < 1 || batch > kMaxBatch) return TND_ERR_INVALID;
+    if (cuq[0] != 0 || cukv[0] != 0) return TND_ERR_INVALID;
+    for (int64_t b = 0; b < batch; ++b) {
+        if (cuq[b + 1] < cuq[b] || cukv[b + 1] < cukv[b]) return TND_ERR_INVALID;
+    }
+    p.tq = cuq[batch];
+    p.tkv = cukv[batch];
+    if (p.tq < 1 || p.tq > kMaxTokens || p.tkv < 1 || p.tkv > kMaxTokens) return TND_ERR_INVALID;
+    if (nq < 1 || nq > kMaxHeads || nkv < 1 || nkv > kMaxHeads || nq % nkv != 0) return TND_ERR_INVALID;
+    if (d < 1 || d > kMaxHeadDim) return TND_ERR_INVALID;
+    if (!(keep > 0.0 && keep <= 1.0)) return TND_ERR_INVALID;
+    if (!std::isfinite(scale)) return TND_ERR_INVALID;
+    if (mode < 0 || mode > 8) return TND_ERR_INVALID;
+    if (mode == 4 && pre + next < 0) return TND_ERR_INVALID;  // band needs an intersection
+    if (mode == 1 || mode >= 5) return TND_ERR_UNSUPPORTED;
+    if (mode == 4) {
+        for (int64_t b = 0; b < batch; ++b) {
+            if (cuq[b + 1] - cuq[b] != cukv[b + 1] - cukv[b]) return TND_ERR_UNSUPPORTED;
+        }
+    }
+    if (d > kSimtMaxHeadDim) return TND_ERR_UNSUPPORTED;
+    p.dtype = dtype;
+    p.batch = batch;
+    p.cuq = cuq;
+    p.cukv = cukv;
+    p.nq = nq;
+    p.nkv = nkv;
+    p.d = d;
+    p.scale = scale;
+    p.keep = keep;
+    p.pre = pre;
+    p.next = next;
+    p.mode = mode;
+    p.has_drop = has_drop && keep < 1.0;
+    p.has_sink = has_sink;
+    return TND_OK;
+}
+
+MaskSpec mask_of(const Problem &p)
+{
+    MaskSpec m;
+    m.mode = (int32_t)p.mode;
+    m.pre = p.pre;
+    m.next = p.next;
+    return m;
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// plan: sequence table, CUDA-core work lists and tensor-core units
+// ---------------------------------------------------------------------------
+struct Plan {
+    std::vector<SeqDesc> seqs;
+    std::vector<int2> q_items, kv_items;
+    std::vector<GradUnit> units;
+    std::vector<QBlockInfo> qblk;
+    std::vector<int2> uncovered;  // (b, first row) of 64-row q blocks nothing contributes to
+    int64_t kept_pairs = 0;       // summed over sequences and query heads
+};
+
+// Union of the kept key ranges of query rows [r0, r1) (empty: lo > hi).
+void rows_union(const MaskSpec &m, int64_t sq, int64_t skv, int64_t r0, int64_t r1, int64_t &ulo,
+                int64_t &uhi)
+{
+    ulo = INT64_MAX;
+    uhi = INT64_MIN;
+    for (int64_t i = r0; i < r1; ++i) {
+        int64_t lo, hi;
+        key_range(m, sq, skv, i, lo, hi);
+        if (lo > hi) continue;
+        ulo = std::min(ulo, lo);
+        uhi = std::max(uhi, hi);
+    }
+}
+
+void build_plan(const Problem &p, bool with_units, Plan &pl)
+{
+    const MaskSpec m = mask_of(p);
+    const int64_t G = p.nq / p.nkv;
+    pl.seqs.resize(p.batch);
+    int64_t base = 0, qblk0 = 0;
+    struct GroupWork {
+        int64_t work;
+        int32_t b;
+    };
+    std::vector<GroupWork> gw;
+    std::vector<std::vector<GradUnit>> seq_units(p.batch);
+    for (int64_t b = 0; b < p.batch; ++b) {
+        const int64_t sq = p.cuq[b + 1] - p.cuq[b], skv = p.cukv[b + 1] - p.cukv[b];
+        SeqDesc &sd = pl.seqs[b];
+        sd.tq = p.cuq[b];
+        sd.tk = p.cukv[b];
+        sd.sq = (int32_t)sq;
+        sd.skv = (int32_t)skv;
+        sd.mask_base = base;
+        sd.qblk0 = (int32_t)qblk0;
+        sd.nqblk = (int32_t)((sq + kQBlock - 1) / kQBlock);
+        base += p.nq * sq * skv;
+        qblk0 += sd.nqblk;
+        for (int64_t r = 0; r < sq; r += kSimtRows) pl.q_items.push_back(make_int2((int)b, (int)r));
+        for (int64_t r = 0; r < skv; r += kSimtRows) pl.kv_items.push_back(make_int2((int)b, (int)r));
+        for (int64_t i = 0; i < sq; ++i) {
+            int64_t lo, hi;
+            key_range(m, sq, skv, i, lo, hi);
+            if (hi >= lo) pl.kept_pairs += (hi - lo + 1) * p.nq;
+        }
+        if (!with_units) continue;
+        const int64_t nkb = (skv + kKvBlock - 1) / kKvBlock;
+        std::vector<int32_t> ilo(nkb, INT32_MAX), ihi(nkb, -1);
+        for (int64_t qb = 0; qb < sd.nqblk; ++qb) {
+            int64_t ulo, uhi;
+            rows_union(m, sq, skv, qb * kQBlock, std::min<int64_t>(sq, (qb + 1) * kQBlock), ulo, uhi);
+            QBlockInfo qi;
+            if (ulo > uhi) {
+                qi.jlo = qi.jhi = -1;
+                pl.uncovered.push_back(make_int2((int)b, (int)(qb * kQBlock)));
+            } else {
+                qi.jlo = (int32_t)(ulo / kKvBlock);
+                qi.jhi = (int32_t)(uhi / kKvBlock);
+                for (int64_t j = qi.jlo; j <= qi.jhi; ++j) {
+                    ilo[j] = std::min<int32_t>(ilo[j], (int32_t)qb);
+                    ihi[j] = std::max<int32_t>(ihi[j], (int32_t)qb);
+                }
+            }
+            pl.qblk.push_back(qi);
+        }
+        int64_t work = 0;
+        // kv blocks in descending order: the dQ chain of a q block runs from
+        // its highest contributing kv block down to its lowest.
+        for (int64_t j = nkb - 1; j >= 0; --j) {
+            GradUnit u{};
+            u.b = (int32_t)b;
+            u.j = (int32_t)j;
+            u.qb_lo = ihi[j] < 0 ? 0 : ilo[j];
+            u.qb_hi = ihi[j] < 0 ? 0 : ihi[j] + 1;
+            work += u.qb_hi - u.qb_lo + 1;
+            seq_units[b].push_back(u);
+        }
+        gw.push_back({work, (int32_t)b});
+    }
+    if (!with_units) return;
+    // Sequences with the most work first; every kv head of a sequence in turn.
+    std::stable_sort(gw.begin(), gw.end(), [](const GroupWork &x, const GroupWork &y) { return x.work > y.work; });
+    for (const GroupWork &w : gw) {
+        for (int64_t g = 0; g < p.nkv; ++g) {
+            for (GradUnit u : seq_units[w.b]) {
+                u.g = (int32_t)g;
+                pl.units.push_back(u);
+            }
+        }
+    }
+    (void)G;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct Layout {
+    size_t seqs = 0, q_items = 0, kv_items = 0, units = 0, qblk = 0, uncovered = 0;  // offsets of the
+    size_t plan_end = 0;                                                                // copied plan
+    size_t flags = 0, lse2 = 0, drow = 0, sinkrow = 0, dqacc = 0, total = 0;
+};
+
+Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
+{
+    Layout L;
+    size_t off = kStatusBytes;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = round_up(off + bytes, 256);
+        return o;
+    };
+    L.seqs = take(pl.seqs.size() * sizeof(SeqDesc));
+    L.q_items = take(pl.q_items.size() * sizeof(int2));
+    L.kv_items = take(pl.kv_items.size() * sizeof(int2));
+    L.units = take(pl.units.size() * sizeof(GradUnit));
+    L.qblk = take(pl.qblk.size() * sizeof(QBlockInfo));
+    L.uncovered = take(pl.uncovered.size() * sizeof(int2));
+    L.plan_end = off;
+    if (grad) {
+        const size_t rows = (size_t)p.tq * (size_t)p.nq;
+        L.flags = take(tc ? pl.qblk.size() * (size_t)p.nq * sizeof(int32_t) : 0);
+        L.lse2 = take(rows * sizeof(float));
+        L.drow = take(rows * sizeof(float));
+        L.sinkrow = take(p.has_sink ? rows * sizeof(float) : 0);
+        L.dqacc = take(tc ? rows * (size_t)p.d * sizeof(float) : 0);
+    }
+    L.total = off;
+    return L;
+}
+
+bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
+
+// Copies the plan into the workspace and clears the status words (and the
+// dQ chain flags of the tensor-core path).
+tnd_status upload_plan(const Plan &pl, const Layout &L, void *ws, bool clear_flags, const Problem &p,
+                       cudaStream_t s)
+{
+    std::vector<unsigned char> host(L.plan_end, 0);
+    auto put = [&](size_t off, const void *src, size_t bytes) {
+        if (bytes) std::memcpy(host.data() + off, src, bytes);
+    };
+    put(L.seqs, pl.seqs.data(), pl.seqs.size() * sizeof(SeqDesc));
+    put(L.q_items, pl.q_items.data(), pl.q_items.size() * sizeof(int2));
+    put(L.kv_items, pl.kv_items.data(), pl.kv_items.size() * sizeof(int2));
+    put(L.units, pl.units.data(), pl.units.size() * sizeof(GradUnit));
+    put(L.qblk, pl.qblk.data(), pl.qblk.size() * sizeof(QBlockInfo));
+    put(L.uncovered, pl.uncovered.data(), pl.uncovered.size() * sizeof(int2));
+    // status words start at zero (host buffer is zero-filled there)
+    if (cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return TND_ERR_CUDA;
+    if (clear_flags) {
+        const size_t bytes = pl.qblk.size() * (size_t)p.nq * sizeof(int32_t);
+        if (bytes && cudaMemsetAsync((char *)ws + L.flags, 0, bytes, s) != cudaSuccess) return TND_ERR_CUDA;
+    }
+    return TND_OK;
+}
+
+template <typename A>
+void fill_common(A &a, const Problem &p, const Plan &pl, const Layout &L, void *ws)
+{
+    char *w = (char *)ws;
+    a.dtype = p.dtype;
+    a.batch = (int32_t)p.batch;
+    a.nq = (int32_t)p.nq;
+    a.nkv = (int32_t)p.nkv;
+    a.d = (int32_t)p.d;
+    a.group = (int32_t)(p.nq / p.nkv);
+    a.tq = p.tq;
+    a.tkv = p.tkv;
+    a.scale = (float)p.scale;
+    a.keep_prob = (float)p.keep;
+    a.inv_keep = (float)(1.0 / p.keep);
+    a.mask = mask_of(p);
+    a.has_drop = p.has_drop;
+    a.has_sink = p.has_sink;
+    a.status = (uint32_t *)w;
+    a.seqs = (const SeqDesc *)(w + L.seqs);
+    a.q_items = (const int2 *)(w + L.q_items);
+    a.n_q_items = (int32_t)pl.q_items.size();
+}
+
+}  // namespace
+}  // namespace tnd
+
+using namespace tnd;
+
+extern "C" {
+
+const char *tnd_status_string(tnd_status s)
+{
+    switch (s) {
+    case TND_OK: return "ok";
+    case TND_ERR_NULLPTR: return "a required pointer argument is NULL";
+    case TND_ERR_INVALID: return "an argument is outside the supported dtype, shape, scalar or alignment limits";
+    case TND_ERR_UNSUPPORTED: return "the argument combination is valid but not implemented by this library";
+    case TND_ERR_WORKSPACE: return "the workspace is NULL, misaligned or smaller than required";
+    case TND_ERR_CUDA: return "a CUDA runtime call failed";
+    case TND_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired; outputs of that call are invalid";
+    case TND_ERR_DEVICE_CHECK: return "a device-side consistency check failed";
+    }
+    return "unknown status";
+}
+
+tnd_status tnd_attn_set_option(tnd_option option, int64_t value)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    switch (option) {
+    case TND_OPT_GRAD_PATH:
+        if (value != 0 && value != 1) return TND_ERR_INVALID;
+        g_opt.grad_path = (int)value;
+        return TND_OK;
+    case TND_OPT_WAIT_LIMIT_MS:
+        if (value < 1 || value > 600000) return TND_ERR_INVALID;
+        g_opt.wait_limit_ms = value;
+        return TND_OK;
+    case TND_OPT_PROFILE:
+        if (value != 0 && value != 1) return TND_ERR_INVALID;
+        g_opt.profile = (int)value;
+        return TND_OK;
+    }
+    return TND_ERR_INVALID;
+}
+
+tnd_status tnd_attn_profile_read(const char **names, double *total_ms, int64_t *launches, int capacity,
+                                 int *count, int reset)
+{
+    if (!count) return TND_ERR_NULLPTR;
+    std::lock_guard<std::mutex> lk(g_mu);
+    double ms[kNumKinds] = {0};
+    int64_t n[kNumKinds] = {0};
+    for (const ProfEntry &e : g_prof) {
+        if (cudaEventSynchronize(e.stop) != cudaSuccess) return TND_ERR_CUDA;
+        float t = 0.0f;
+        if (cudaEventElapsedTime(&t, e.start, e.stop) != cudaSuccess) return TND_ERR_CUDA;
+        ms[e.kind] += t;
+        n[e.kind] += 1;
+    }
+    for (int k = 0; k < kNumKinds && k < capacity; ++k) {
+        if (names) names[k] = kKindNames[k];
+        if (total_ms) total_ms[k] = ms[k];
+        if (launches) launches[k] = n[k];
+    }
+    *count = kNumKinds;
+    if (reset) {
+        for (const ProfEntry &e : g_prof) {
+            g_event_pool.push_back(e.start);
+            g_event_pool.push_back(e.stop);
+        }
+        g_prof.clear();
+    }
+    return TND_OK;
+}
+
+tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
+                                       int64_t nq, int64_t nkv, int64_t d, double scale, double keep, int64_t pre,
+                                       int64_t next, int64_t mode, int has_drop, int has_sink, uint64_t *ws_size)
+{
+    if (!ws_size) return TND_ERR_NULLPTR;
+    Problem p;
+    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode, has_drop != 0,
+                             has_sink != 0, p);
+    if (st != TND_OK) return st;
+    Plan pl;
+    build_plan(p, false, pl);
+    *ws_size = layout_for(p, pl, false, false).total;
+    return TND_OK;
+}
+
+tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask, const float *sink,
+                        tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq,
+                        int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode,
+                        void *out, float *smax, float *ssum, void *ws, uint64_t ws_size, void *stream)
+{
+    if (!q || !k || !v || !out || !smax || !ssum) return TND_ERR_NULLPTR;
+    Problem p;
+    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode,
+                             drop_mask != nullptr, sink != nullptr, p);
+    if (st != TND_OK) return st;
+    for (const void *ptr : {q, k, v, (const void *)out, (const void *)smax, (const void *)ssum})
+        if (!aligned16(ptr)) return TND_ERR_INVALID;
+    Plan pl;
+    build_plan(p, false, pl);
+    const Layout L = layout_for(p, pl, false, false);
+    if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = upload_plan(pl, L, ws, false, p, s);
+    if (st != TND_OK) return st;
+    FwdArgs a{};
+    fill_common(a, p, pl, L, ws);
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.drop_mask = p.has_drop ? drop_mask : nullptr;
+    a.sink = sink;
+    a.o = out;
+    a.smax = smax;
+    a.ssum = ssum;
+    if (timed(K_FWD, s, [&] { return launch_fwd_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    return TND_OK;
+}
+
+tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
+                                        int64_t nq, int64_t nkv, int64_t d, double scale, double keep, int64_t pre,
+                                        int64_t next, int64_t mode, int has_drop, int has_sink, uint64_t *ws_size)
+{
+    if (!ws_size) return TND_ERR_NULLPTR;
+    Problem p;
+    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode, has_drop != 0,
+                             has_sink != 0, p);
+    if (st != TND_OK) return st;
+    const bool tc = grad_tc_supported(p.dtype, (int)p.d);
+    Plan pl;
+    build_plan(p, tc, pl);
+    *ws_size = layout_for(p, pl, true, tc).total;
+    return TND_OK;
+}
+
+tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
+                         const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
+                         int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv,
+                         int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq,
+                         void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream)
+{
+    if (!q || !k || !v || !dy || !smax || !ssum || !o || !dq || !dk || !dv) return TND_ERR_NULLPTR;
+    if (sink && !dsink) return TND_ERR_NULLPTR;
+    Problem p;
+    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode,
+                             drop_mask != nullptr, sink != nullptr, p);
+    if (st != TND_OK) return st;
+    for (const void *ptr : {q, k, v, dy, (const void *)smax, (const void *)ssum, o, (const void *)dq,
+                            (const void *)dk, (const void *)dv})
+        if (!aligned16(ptr)) return TND_ERR_INVALID;
+    const bool tc_layout = grad_tc_supported(p.dtype, (int)p.d);
+    const bool tc = use_tc(p);
+    Plan pl;
+    build_plan(p, tc_layout, pl);
+    const Layout L = layout_for(p, pl, true, tc_layout);
+    if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = upload_plan(pl, L, ws, tc, p, s);
+    if (st != TND_OK) return st;
+    GradArgs a{};
+    fill_common(a, p, pl, L, ws);
+    char *w = (char *)ws;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dy = dy;
+    a.o = o;
+    a.drop_mask = p.has_drop ? drop_mask : nullptr;
+    a.smax = smax;
+    a.ssum = ssum;
+    a.sink = sink;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dsink = dsink;
+    a.kv_items = (const int2 *)(w + L.kv_items);
+    a.n_kv_items = (int32_t)pl.kv_items.size();
+    a.lse2 = (float *)(w + L.lse2);
+    a.drow = (float *)(w + L.drow);
+    a.sinkrow = p.has_sink ? (float *)(w + L.sinkrow) : nullptr;
+    a.units = (const GradUnit *)(w + L.units);
+    a.n_units = (int32_t)pl.units.size();
+    a.qblk = (const QBlockInfo *)(w + L.qblk);
+    a.n_qblk = (int32_t)pl.qblk.size();
+    a.flags = (int32_t *)(w + L.flags);
+    a.dqacc = tc_layout ? (float *)(w + L.dqacc) : nullptr;
+    {
+        int dev = 0, khz = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+        if (khz <= 0) khz = 2000000;
+        a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)khz;
+    }
+    if (timed(K_PREPASS, s, [&] { return launch_prepass(a, tc, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    if (tc) {
+        if (timed(K_TC, s, [&] { return launch_grad_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    } else {
+        if (timed(K_DKDV, s, [&] { return launch_grad_dkdv_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+        if (timed(K_DQ, s, [&] { return launch_grad_dq_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    }
+    if (p.has_sink) {
+        if (timed(K_SINK, s, [&] { return launch_sink_reduce(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    }
+    return TND_OK;
+}
+
+tnd_status tnd_attn_device_status(const void *ws, uint64_t ws_size, void *stream)
+{
+    if (!ws) return TND_ERR_NULLPTR;
+    if (ws_size < kStatusBytes) return TND_ERR_WORKSPACE;
+    uint32_t words[4] = {0, 0, 0, 0};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(words, ws, sizeof(words), cudaMemcpyDeviceToHost, s) != cudaSuccess) return TND_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TND_ERR_CUDA;
+    if (words[kStatusWord] == 0) return TND_OK;
+    if (words[kStatusWord] == (uint32_t)TND_ERR_DEVICE_TIMEOUT) return TND_ERR_DEVICE_TIMEOUT;
+    return TND_ERR_DEVICE_CHECK;
+}
+
+tnd_status tnd_attn_grad_plan(int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv,
+                              int64_t pre, int64_t next, int64_t mode, int64_t *units, int64_t capacity,
+                              int64_t *n_units, int64_t *kept_pairs)
+{
+    if (!n_units || !kept_pairs) return TND_ERR_NULLPTR;
+    Problem p;
+    tnd_status st = validate(TND_BF16, batch, cuq, cukv, nq, nkv, 128, 1.0, 1.0, pre, next, mode, false, false, p);
+    if (st != TND_OK) return st;
+    Plan pl;
+    build_plan(p, true, pl);
+    *n_units = (int64_t)pl.units.size();
+    *kept_pairs = pl.kept_pairs;
+    if (units) {
+        for (int64_t u = 0; u < (int64_t)pl.units.size() && u < capacity; ++u) {
+            const GradUnit &g = pl.units[u];
+            units[5 * u + 0] = g.b;
+            units[5 * u + 1] = g.g;
+            units[5 * u + 2] = g.j;
+            units[5 * u + 3] = g.qb_lo;
+            units[5 * u + 4] = g.qb_hi;
+        }
+    }
+    return TND_OK;
+}
+
+}  // extern "C"

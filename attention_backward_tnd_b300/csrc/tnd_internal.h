@@ -1,0 +1,135 @@
+// Internal declarations shared by the host API and the kernels of the TND
+// attention library.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tnd_attn.h"
+
+namespace tnd {
+
+// Rows per block of the tensor-core gradient: kv block (UMMA M) and q block.
+constexpr int kKvBlock = 128;
+constexpr int kQBlock = 64;
+// Rows per block of the CUDA-core kernels.
+constexpr int kSimtRows = 32;
+
+// Offsets into the status area at the start of every workspace.
+constexpr int kStatusWord = 0;     // first device error code (0 = none)
+constexpr int kStatusDetail = 1;   // where it happened (kernel-specific)
+constexpr int kWorkCounter = 2;    // next unit of the persistent kernel
+constexpr size_t kStatusBytes = 256;
+
+// One sequence of the packed batch, as the kernels see it.
+struct SeqDesc {
+    int64_t tq;         // first query row (token index) of the sequence
+    int64_t tk;         // first key/value row
+    int32_t sq;         // query rows
+    int32_t skv;        // key/value rows
+    int64_t mask_base;  // flat keep-bit index of (h=0, i=0, j=0)
+    int32_t qblk0;      // global index of its first 64-row q block
+    int32_t nqblk;      // number of 64-row q blocks
+};
+
+// Mask description (sparseMode 0/2/3/4 computed from indices).
+struct MaskSpec {
+    int32_t mode;
+    int64_t pre;
+    int64_t next;
+};
+
+// Key range [lo, hi] kept for query row i (empty when lo > hi).  Rows of
+// every supported mode keep one contiguous range whose ends never decrease
+// with i, which the schedules rely on.
+__host__ __device__ inline void key_range(const MaskSpec &m, int64_t sq, int64_t skv, int64_t i,
+                                          int64_t &lo, int64_t &hi)
+{
+    lo = 0;
+    hi = skv - 1;
+    if (m.mode == 2) {
+        hi = hi < i ? hi : i;
+    } else if (m.mode == 3) {
+        const int64_t e = i + skv - sq;
+        hi = hi < e ? hi : e;
+    } else if (m.mode == 4) {
+        const int64_t a = i - m.pre, e = i + m.next;
+        lo = lo > a ? lo : a;
+        hi = hi < e ? hi : e;
+    }
+}
+
+// Work unit of the tensor-core gradient: kv block j of kv head g of
+// sequence b, visiting q blocks [qb_lo, qb_hi) for each of the group's heads.
+struct GradUnit {
+    int32_t b, g, j, qb_lo, qb_hi, pad0, pad1, pad2;
+};
+
+// Contributors of one global q block: kv blocks [jlo, jhi] (jlo = -1: none).
+struct QBlockInfo {
+    int32_t jlo, jhi;
+};
+
+// Everything a gradient launch needs to know (device pointers into the
+// caller's buffers and the workspace).
+struct GradArgs {
+    const void *q, *k, *v, *dy, *o;
+    const uint8_t *drop_mask;
+    const float *smax, *ssum, *sink;
+    void *dq, *dk, *dv;
+    float *dsink;
+    int dtype;
+    int32_t batch, nq, nkv, d, group;
+    int64_t tq, tkv;
+    float scale, keep_prob, inv_keep;
+    MaskSpec mask;
+    int has_drop, has_sink;
+    // workspace regions
+    uint32_t *status;
+    const SeqDesc *seqs;
+    const int2 *q_items;      // (b, first row) per 32-row q block
+    int32_t n_q_items;
+    const int2 *kv_items;     // (b, first row) per 32-row kv block
+    int32_t n_kv_items;
+    float *lse2;              // [Nq][Tq]  m*log2(e) + log2(l)  (+inf if l == 0)
+    float *drow;              // [Nq][Tq]  rowsum(dY o O)
+    float *sinkrow;           // [Nq][Tq]  -p_sink * D  (sink only)
+    // tensor-core path
+    const GradUnit *units;
+    int32_t n_units;
+    const QBlockInfo *qblk;
+    int32_t n_qblk;
+    int32_t *flags;           // [n_qblk][Nq] contributions added so far
+    float *dqacc;             // [Tq][Nq][D] fp32 partial sums
+    int64_t wait_limit_cycles;
+};
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    const uint8_t *drop_mask;
+    const float *sink;
+    void *o;
+    float *smax, *ssum;
+    int dtype;
+    int32_t batch, nq, nkv, d, group;
+    int64_t tq, tkv;
+    float scale, keep_prob, inv_keep;
+    MaskSpec mask;
+    int has_drop, has_sink;
+    uint32_t *status;
+    const SeqDesc *seqs;
+    const int2 *q_items;
+    int32_t n_q_items;
+};
+
+// Kernel launchers (each returns the CUDA error of its launch).
+cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_prepass(const GradArgs &a, bool zero_tc_state, cudaStream_t s);
+cudaError_t launch_grad_dkdv_simt(const GradArgs &a, cudaStream_t s);
+cudaError_t launch_grad_dq_simt(const GradArgs &a, cudaStream_t s);
+cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s);
+// Tensor-core gradient (bf16/fp16, D = 128); false if this build lacks it.
+bool grad_tc_supported(int dtype, int d);
+cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s);
+
+}  // namespace tnd

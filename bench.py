@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the TND attention score-gradient on B300.
+
+One step = one tnd_attn_grad call (prepass, main gradient kernel, dSink
+reduction when a sink is present) over one batch of the synthetic workload,
+inputs already resident in HBM.  Metric: mask-adjusted attention-grad TFLOP/s,
+FLOP = sum over sequences and query heads of 10 * D * (kept (q, kv) pairs)
+(five GEMMs of 2*D FLOP per kept pair: S, dP, dV, dK, dQ; dropout does not
+reduce the count), and its fraction of the measured dense BF16 peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With N > 1 the script runs under torchrun: every rank processes its own copy
+of the workload (independent replicas, no collective on the data path), the
+timed region is bracketed by barriers and rank 0 reports the maximum over
+ranks.  --impl reference times the fp64 CPU oracle on the host cores on a
+bounded sample of the same workload (the reference arm of this project).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention-grad TFLOP/s (mask-adjusted) & % of B300 dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "causal_varlen_bf16"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def kept_pairs(wl) -> int:
+    """Kept (q-row, kv-row) pairs summed over sequences and query heads,
+    counted row by row from the sparseMode definitions."""
+    total = 0
+    for sq, skv in zip(wl.seqlens_q, wl.seqlens_kv):
+        i = np.arange(sq, dtype=np.int64)
+        lo = np.zeros(sq, dtype=np.int64)
+        hi = np.full(sq, skv - 1, dtype=np.int64)
+        if wl.sparse_mode == 2:
+            hi = np.minimum(hi, i)
+        elif wl.sparse_mode == 3:
+            hi = np.minimum(hi, i + skv - sq)
+        elif wl.sparse_mode == 4:
+            lo = np.maximum(lo, i - wl.pre_tokens)
+            hi = np.minimum(hi, i + wl.next_tokens)
+        total += int(np.maximum(hi - lo + 1, 0).sum())
+    return total * wl.nq
+
+
+def grad_flop(wl) -> float:
+    return 10.0 * wl.d * kept_pairs(wl)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, if it
+    was taken on the current kernel source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    rec = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ": " in line:
+            k, v = line[2:].split(": ", 1)
+            rec[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "attention_backward_tnd_b300", "csrc", rec.get("source", ""))
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if sha != rec.get("source_sha256_16") or rec.get("workload") is None:
+        return None
+    try:
+        return {"bytes_per_launch": float(rec["dram_bytes_per_launch"]), "workload": rec["workload"]}
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.idx)], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, flags in rows for k, fl in enumerate(flags) if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def workload_config(wl, l2_note=True):
+    cfg = {"workload": wl.name, "dtype": wl.dtype, "B": wl.batch, "T": wl.tq, "Nq": wl.nq, "Nkv": wl.nkv,
+           "D": wl.d, "sparse_mode": wl.sparse_mode, "pre_tokens": wl.pre_tokens, "next_tokens": wl.next_tokens,
+           "keep_prob": wl.keep_prob, "sink": wl.has_sink, "seed": wl.seed,
+           "seqlens": wl.seqlens_q if wl.batch <= 16 else f"{wl.batch} sequences",
+           "kept_pairs": kept_pairs(wl)}
+    if l2_note:
+        cfg["l2"] = "flushed between timed steps (256 MiB write, outside the per-step events)"
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, inp, target_s: float, max_s: float):
+    """Times the fp64 oracle (forward + gradient) on whole sequences taken in
+    order until about target_s of work; returns (TFLOP/s, seconds, sample text,
+    threads used)."""
+    import oracle
+    oracle.build()
+    chosen, est = [], 0.0
+    rate = 1.0e9 * max(1, os.cpu_count() or 1)       # rough fp64 flop/s for sizing only
+    for b in range(wl.batch):
+        sub = workloads.custom(wl.name, wl.dtype, [wl.seqlens_q[b]], [wl.seqlens_kv[b]], wl.nq, wl.nkv, wl.d,
+                               scale=wl.scale, keep_prob=wl.keep_prob, pre_tokens=wl.pre_tokens,
+                               next_tokens=wl.next_tokens, sparse_mode=wl.sparse_mode, has_sink=wl.has_sink)
+        cost = kept_pairs(sub) * wl.d * 14.0 / rate
+        if chosen and est + cost > target_s:
+            break
+        chosen.append(b)
+        est += cost
+        if est >= target_s:
+            break
+    heads = wl.nq
+    # shrink to fewer kv groups if even one sequence is far too large
+    while est > max_s and heads > wl.nq // wl.nkv:
+        heads //= 2
+        est /= 2
+    hs = (0, max(heads - heads % (wl.nq // wl.nkv), wl.nq // wl.nkv))
+    b0 = chosen[0]
+    row_lo = None
+    if est > max_s:  # keep a suffix of query rows (exact for dQ of those rows)
+        keep_frac = max_s / est
+        row_lo = [int(wl.seqlens_q[b] * (1 - keep_frac)) if b in chosen else wl.seqlens_q[b] for b in range(wl.batch)]
+    p = oracle.problem_from_workload(wl, drop_mask=inp.mask, sink=inp.sink, heads=hs, row_lo=(
+        row_lo if row_lo is not None else [0 if b in chosen else wl.seqlens_q[b] for b in range(wl.batch)]))
+    t0 = time.perf_counter()
+    oracle.fwd_grad(p, inp.q64, inp.k64, inp.v64, inp.dy64)
+    dt = time.perf_counter() - t0
+    # mask-adjusted pairs actually covered by the sample
+    pairs = 0
+    for b in chosen:
+        sq, skv = wl.seqlens_q[b], wl.seqlens_kv[b]
+        sub = workloads.custom(wl.name, wl.dtype, [sq], [skv], 1, 1, wl.d, keep_prob=wl.keep_prob,
+                               pre_tokens=wl.pre_tokens, next_tokens=wl.next_tokens, sparse_mode=wl.sparse_mode)
+        rows = kept_rows(sub)
+        lo = 0 if row_lo is None else row_lo[b]
+        pairs += int(rows[lo:].sum()) * (hs[1] - hs[0])
+    units = len(chosen) * max(1, (hs[1] - hs[0]) // (wl.nq // wl.nkv))
+    threads = min(os.cpu_count() or 1, units)
+    text = (f"sequences {chosen} (lengths {[wl.seqlens_q[b] for b in chosen]}), query heads [{hs[0]}, {hs[1]})"
+            + ("" if row_lo is None else ", query-row suffix") + f": {pairs} kept pairs, forward + gradient in fp64")
+    return 10.0 * wl.d * pairs / dt / 1e12, dt, text, threads
+
+
+def kept_rows(wl):
+    sq, skv = wl.seqlens_q[0], wl.seqlens_kv[0]
+    i = np.arange(sq, dtype=np.int64)
+    lo = np.zeros(sq, dtype=np.int64)
+    hi = np.full(sq, skv - 1, dtype=np.int64)
+    if wl.sparse_mode == 2:
+        hi = np.minimum(hi, i)
+    elif wl.sparse_mode == 3:
+        hi = np.minimum(hi, i + skv - sq)
+    elif wl.sparse_mode == 4:
+        lo = np.maximum(lo, i - wl.pre_tokens)
+        hi = np.minimum(hi, i + wl.next_tokens)
+    return np.maximum(hi - lo + 1, 0)
+
+
+def run_reference(args, wl, rank):
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(wl)
+    for _ in range(args.warmup):
+        oracle_sample(wl, inp, target_s=1.0, max_s=3.0)
+    vals, secs, text, threads = [], [], "", 1
+    for _ in range(args.steps):
+        v, dt, text, threads = oracle_sample(wl, inp, target_s=1.0, max_s=3.0)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, l2_note=False),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": text},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the library on the GPU
+# ---------------------------------------------------------------------------
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import attention_backward_tnd_b300 as tnd
+    from attention_backward_tnd_b300 import build as tbuild
+
+    tbuild.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = workloads.make_inputs(wl, with_fp64=(rank == 0 and world == 1))
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[wl.dtype]
+
+    def to_dev(a):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    q, k, v, dy = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.dy))
+    sink = None if inp.sink is None else torch.from_numpy(inp.sink).to(dev)
+    mask = None if inp.mask is None else torch.from_numpy(inp.mask).to(dev)
+    cu_q, cu_kv = wl.cu_q, wl.cu_kv
+    out, smax, ssum = tnd.fwd(q, k, v, cu_q, cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens, wl.next_tokens,
+                              wl.sparse_mode, mask, sink)
+    nbytes = tnd.grad_workspace_bytes(q, k, cu_q, cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens, wl.next_tokens,
+                                      wl.sparse_mode, mask is not None, sink is not None)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+            torch.empty(wl.nq, dtype=torch.float32, device=dev) if sink is not None else None)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        tnd.grad(q, k, v, dy, out, smax, ssum, cu_q, cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens,
+                 wl.next_tokens, wl.sparse_mode, mask, sink, workspace=ws, outputs=outs)
+
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_PROFILE, 1) == tnd.TND_OK
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = tnd.device_status(ws)
+    if st != tnd.TND_OK:
+        raise SystemExit(f"device status after warm-up: {tnd.tnd_status_string(st)}")
+    tnd.tnd_attn_profile_read(reset=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    st = tnd.device_status(ws)
+    if st != tnd.TND_OK:
+        raise SystemExit(f"device status after timed steps: {tnd.tnd_status_string(st)}")
+    prof = tnd.tnd_attn_profile_read(reset=True)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flop = grad_flop(wl)
+    value = world * flop / (ms_per_step * 1e-3) / 1e12
+    launches = int(sum(n for _, n in prof.values()))
+    kernels = {name: {"ms_per_launch": ms / n, "launches": n} for name, (ms, n) in prof.items() if n}
+    main = max(kernels, key=lambda kname: kernels[kname]["ms_per_launch"] * kernels[kname]["launches"])
+    main_ms = kernels[main]["ms_per_launch"]
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flop / (main_ms * 1e-3) / 1e12
+    traffic = traffic_record(main)
+
+    # end to end: pinned host inputs -> device, gradient, device -> pinned host outputs
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, dy, out, smax, ssum)]
+    dev_in = [q, k, v, dy, out, smax, ssum]
+    if sink is not None:
+        host_in.append(sink.cpu().pin_memory())
+        dev_in.append(sink)
+    if mask is not None:
+        host_in.append(mask.cpu().pin_memory())
+        dev_in.append(mask)
+    host_out = [t.cpu().pin_memory() for t in outs if t is not None]
+    dev_out = [t for t in outs if t is not None]
+    h2d = int(sum(t.numel() * t.element_size() for t in host_in))
+    d2h = int(sum(t.numel() * t.element_size() for t in host_out))
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for hsrc, d in zip(host_in, dev_in):
+            d.copy_(hsrc, non_blocking=True)
+        step()
+        for d, hdst in zip(dev_out, host_out):
+            hdst.copy_(d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) inputs; forward O/max/sum "
+            "from this library's forward)",
+            "config": dict(workload_config(wl), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "pct_of_bf16_peak": 100.0 * (value / world) / peak, "peak_source": peak_src,
+            "roofline": {"bound": "tensor", "kernel": main, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": None if traffic is None else traffic["bytes_per_launch"],
+                         "peak_kind": f"bf16 dense, burst ({peak_src})"},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "clocks": clk.summary(),
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v_cpu, dt, text, threads = oracle_sample(wl, inp, target_s=12.0, max_s=30.0)
+            line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                    "sample": text, "seconds": dt}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workloads.workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+    else:
+        run_ours(args, wl, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

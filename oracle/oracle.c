@@ -164,49 +164,86 @@ static int64_t max_skv(const ora_problem *p)
     return mx;
 }
 
+/* (b, h, i) of flat query-row index r over all sequences and heads; -1 if none */
+static int row_of(const ora_problem *p, int64_t r, int64_t *b_out, int64_t *h_out, int64_t *i_out)
+{
+    const int64_t t = r / p->Nq, h = r % p->Nq;
+    for (int64_t b = 0; b < p->B; ++b) {
+        if (t >= p->cu_q[b] && t < p->cu_q[b + 1]) {
+            *b_out = b;
+            *h_out = h;
+            *i_out = t - p->cu_q[b];
+            return 0;
+        }
+    }
+    return -1;
+}
+
 /*
  * Forward: out [Tq][Nq][D], smax / ssum [Tq][Nq] (natural-log units).
  * [UnpadGrad] Y = Dropout(Softmax(Mask(scale QK^T)), keep_prob) V, with the
  * forward's max and sum as described for softmaxMax / softmaxSum [ScoreV2].
+ * Every query row is independent; rows run in parallel.
  */
 int ora_fwd(const ora_problem *p, const double *q, const double *k, const double *v,
             double *out, double *smax, double *ssum)
 {
     const int64_t D = p->D, G = p->Nq / p->Nkv;
-    const int64_t nunits = p->B * p->Nq, skvmax = max_skv(p);
+    const int64_t nrows = p->cu_q[p->B] * p->Nq, skvmax = max_skv(p);
     int err = 0;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t u = 0; u < nunits; ++u) {
-        const int64_t b = u / p->Nq, h = u % p->Nq, g = h / G;
-        if (h < p->h_lo || h >= p->h_hi) continue;
-        const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
-        const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
-        const int64_t base = ora_mask_base(p, b);
+#pragma omp parallel
+    {
         double *s = (double *)malloc(sizeof(double) * skvmax);
         unsigned char *kept = (unsigned char *)malloc(skvmax);
-        if (!s || !kept) { err = 1; free(s); free(kept); continue; }
-        for (int64_t i = 0; i < sq; ++i) {
-            if (!row_selected(p, b, i)) continue;
+        if (!s || !kept) err = 1;
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int64_t b, h, i;
+            if (!s || !kept || row_of(p, r, &b, &h, &i)) continue;
+            if (h < p->h_lo || h >= p->h_hi || !row_selected(p, b, i)) continue;
+            const int64_t g = h / G, tq = p->cu_q[b], tk = p->cu_kv[b];
+            const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
+            const int64_t base = ora_mask_base(p, b);
             double m, l;
             row_scores(p, q, k, b, h, i, s, kept);
             row_max_sum(p, h, s, kept, skv, &m, &l);
-            double *o = out + ((tq + i) * p->Nq + h) * D;
+            double *o = out + r * D;
             for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
             if (l > 0.0) {
                 for (int64_t j = 0; j < skv; ++j) {
                     if (!kept[j]) continue;
-                    double w = exp(s[j] - m) / l * drop_z(p, base, h, i, j, sq, skv);
+                    const double w = exp(s[j] - m) / l * drop_z(p, base, h, i, j, sq, skv);
                     const double *vj = v + ((tk + j) * p->Nkv + g) * D;
                     for (int64_t d = 0; d < D; ++d) o[d] += w * vj[d];
                 }
             }
-            smax[(tq + i) * p->Nq + h] = m;
-            ssum[(tq + i) * p->Nq + h] = l;
+            smax[r] = m;
+            ssum[r] = l;
         }
         free(s);
         free(kept);
     }
     return err;
+}
+
+/* dS_ij of one (b, h, i, j) from the row's statistics; 0 if not kept */
+static double grad_ds(const ora_problem *p, const double *q, const double *k, const double *v,
+                      const double *dy, double m, double l, double Di, int64_t b, int64_t base,
+                      int64_t h, int64_t i, int64_t j, double *pz_out)
+{
+    const int64_t G = p->Nq / p->Nkv, g = h / G, D = p->D;
+    const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
+    const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
+    *pz_out = 0.0;
+    if (!ora_keep(p->sparse_mode, p->pre_tokens, p->next_tokens, sq, skv, i, j) || !(l > 0.0)) return 0.0;
+    const int64_t r = (tq + i) * p->Nq + h;
+    const double *kj = k + ((tk + j) * p->Nkv + g) * D, *vj = v + ((tk + j) * p->Nkv + g) * D;
+    const double s = p->scale * dot(q + r * D, kj, D);
+    const double pij = exp(s - m) / l;
+    const double z = drop_z(p, base, h, i, j, sq, skv);
+    const double dP = dot(dy + r * D, vj, D);
+    *pz_out = pij * z;
+    return pij * (z * dP - Di);
 }
 
 /*
@@ -216,76 +253,79 @@ int ora_fwd(const ora_problem *p, const double *q, const double *k, const double
  * ds_dense (may be NULL): dS at the flat keep-bit index of every (b,h,i,j).
  * Only selected heads / rows are written; dk / dv of every kv row of every
  * selected kv group are overwritten (they sum over the selected rows only).
+ * Three passes, each over independent outputs: D_i per query row, dQ per
+ * query row, dK / dV per key row.
  */
 int ora_grad(const ora_problem *p, const double *q, const double *k, const double *v,
              const double *dy, const double *out, const double *smax, const double *ssum,
              double *dq, double *dk, double *dv, double *dsink, double *ds_dense)
 {
     const int64_t D = p->D, G = p->Nq / p->Nkv;
-    const int64_t nunits = p->B * p->Nkv, skvmax = max_skv(p);
-    double *sink_part = (double *)calloc((size_t)(nunits * G), sizeof(double));
-    if (!sink_part) return 1;
-    int err = 0;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t u = 0; u < nunits; ++u) {
-        const int64_t b = u / p->Nkv, g = u % p->Nkv;
-        if ((g + 1) * G <= p->h_lo || g * G >= p->h_hi) continue;
-        const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
-        const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
+    const int64_t nrows = p->cu_q[p->B] * p->Nq, nkvrows = p->cu_kv[p->B] * p->Nkv;
+    double *Drow = (double *)calloc((size_t)(nrows > 0 ? nrows : 1), sizeof(double));
+    if (!Drow) return 1;
+    /* D_i = <dY_i, O_i> */
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; ++r) Drow[r] = dot(dy + r * D, out + r * D, D);
+    /* dQ_i = scale * sum_j dS_ij K_j */
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t b, h, i;
+        if (row_of(p, r, &b, &h, &i)) continue;
+        if (h < p->h_lo || h >= p->h_hi || !row_selected(p, b, i)) continue;
+        const int64_t g = h / G, tk = p->cu_kv[b], skv = p->cu_kv[b + 1] - tk;
+        const int64_t sq = p->cu_q[b + 1] - p->cu_q[b];
         const int64_t base = ora_mask_base(p, b);
-        double *s = (double *)malloc(sizeof(double) * skvmax);
-        unsigned char *kept = (unsigned char *)malloc(skvmax);
-        if (!s || !kept) { err = 1; free(s); free(kept); continue; }
+        double *dqi = dq + r * D;
+        for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
         for (int64_t j = 0; j < skv; ++j) {
-            double *dkj = dk + ((tk + j) * p->Nkv + g) * D, *dvj = dv + ((tk + j) * p->Nkv + g) * D;
-            for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+            double pz;
+            const double dS = grad_ds(p, q, k, v, dy, smax[r], ssum[r], Drow[r], b, base, h, i, j, &pz);
+            if (dS == 0.0) continue;
+            const double *kj = k + ((tk + j) * p->Nkv + g) * D;
+            for (int64_t d = 0; d < D; ++d) dqi[d] += p->scale * dS * kj[d];
+            if (ds_dense) ds_dense[base + (h * sq + i) * skv + j] = dS;
         }
+    }
+    /* dK_j = scale * sum_{h in g} sum_i dS_ij Q_i,  dV_j = sum_{h in g} sum_i p_ij z_ij dY_i */
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t kr = 0; kr < nkvrows; ++kr) {
+        const int64_t t = kr / p->Nkv, g = kr % p->Nkv;
+        if ((g + 1) * G <= p->h_lo || g * G >= p->h_hi) continue;
+        int64_t b = 0;
+        while (b < p->B && !(t >= p->cu_kv[b] && t < p->cu_kv[b + 1])) ++b;
+        if (b >= p->B) continue;
+        const int64_t j = t - p->cu_kv[b], tq = p->cu_q[b], sq = p->cu_q[b + 1] - tq;
+        const int64_t base = ora_mask_base(p, b);
+        double *dkj = dk + kr * D, *dvj = dv + kr * D;
+        for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
         for (int64_t h = g * G; h < (g + 1) * G; ++h) {
             if (h < p->h_lo || h >= p->h_hi) continue;
             for (int64_t i = 0; i < sq; ++i) {
                 if (!row_selected(p, b, i)) continue;
                 const int64_t r = (tq + i) * p->Nq + h;
-                const double *qi = q + r * D, *dyi = dy + r * D, *oi = out + r * D;
-                double *dqi = dq + r * D;
-                const double m = smax[r], l = ssum[r];
-                const double Di = dot(dyi, oi, D);
-                for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
-                row_scores(p, q, k, b, h, i, s, kept);
-                for (int64_t j = 0; j < skv; ++j) {
-                    if (!kept[j] || !(l > 0.0)) continue;
-                    const double *kj = k + ((tk + j) * p->Nkv + g) * D;
-                    const double *vj = v + ((tk + j) * p->Nkv + g) * D;
-                    double *dkj = dk + ((tk + j) * p->Nkv + g) * D;
-                    double *dvj = dv + ((tk + j) * p->Nkv + g) * D;
-                    const double pij = exp(s[j] - m) / l;
-                    const double z = drop_z(p, base, h, i, j, sq, skv);
-                    const double dP = dot(dyi, vj, D);
-                    const double dS = pij * (z * dP - Di);
-                    for (int64_t d = 0; d < D; ++d) {
-                        dqi[d] += p->scale * dS * kj[d];
-                        dkj[d] += p->scale * dS * qi[d];
-                        dvj[d] += pij * z * dyi[d];
-                    }
-                    if (ds_dense) ds_dense[base + (h * sq + i) * skv + j] = dS;
+                double pz;
+                const double dS = grad_ds(p, q, k, v, dy, smax[r], ssum[r], Drow[r], b, base, h, i, j, &pz);
+                const double *qi = q + r * D, *dyi = dy + r * D;
+                for (int64_t d = 0; d < D; ++d) {
+                    dkj[d] += p->scale * dS * qi[d];
+                    dvj[d] += pz * dyi[d];
                 }
-                if (p->sink && l > 0.0) sink_part[u * G + (h - g * G)] -= exp(p->sink[h] - m) / l * Di;
             }
         }
-        free(s);
-        free(kept);
     }
+    /* dSink_h = -sum_i exp(sink_h - m_i) / l_i * D_i, summed in row order */
     if (dsink) {
         for (int64_t h = p->h_lo; h < p->h_hi; ++h) dsink[h] = 0.0;
         if (p->sink) {
-            for (int64_t u = 0; u < nunits; ++u) {       /* fixed order over (b, g) */
-                const int64_t g = u % p->Nkv;
-                for (int64_t hh = 0; hh < G; ++hh) {
-                    const int64_t h = g * G + hh;
-                    if (h >= p->h_lo && h < p->h_hi) dsink[h] += sink_part[u * G + hh];
-                }
+            for (int64_t r = 0; r < nrows; ++r) {
+                int64_t b, h, i;
+                if (row_of(p, r, &b, &h, &i)) continue;
+                if (h < p->h_lo || h >= p->h_hi || !row_selected(p, b, i)) continue;
+                if (ssum[r] > 0.0) dsink[h] -= exp(p->sink[h] - smax[r]) / ssum[r] * Drow[r];
             }
         }
     }
-    free(sink_part);
-    return err;
+    free(Drow);
+    return 0;
 }

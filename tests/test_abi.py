@@ -1,0 +1,197 @@
+"""C ABI checks that need no GPU: the library loads and exports every entry
+point the header declares, argument errors are reported before any device
+work, and the host-side gradient plan covers every kept tile exactly once in
+an order the dQ chain can follow."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import attention_backward_tnd_b300 as tnd
+from attention_backward_tnd_b300 import build as tbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INF = 2147483647
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tbuild.build()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "tnd_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tnd_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_entry_point():
+    names = header_functions()
+    assert "tnd_attn_grad" in names and "tnd_attn_fwd" in names
+    L = tnd.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(tnd.SYMBOLS) == names
+
+
+def test_status_strings():
+    for s in range(8):
+        assert tnd.tnd_status_string(s)
+    assert tnd.tnd_status_string(99) == "unknown status"
+
+
+def ws(dtype=tnd.TND_BF16, batch=2, cu_q=(0, 5, 9), cu_kv=(0, 5, 9), nq=4, nkv=2, d=128, scale=0.1, keep=1.0,
+       pre=INF, nxt=INF, mode=3, drop=False, sink=False):
+    return tnd.tnd_attn_grad_workspace_size(dtype, batch, list(cu_q), list(cu_kv), nq, nkv, d, scale, keep, pre,
+                                            nxt, mode, drop, sink)
+
+
+def test_workspace_size_accepts_valid_problems():
+    st, n = ws()
+    assert st == tnd.TND_OK and n > 0
+    st2, n2 = ws(cu_q=(0, 500, 900), cu_kv=(0, 500, 900))
+    assert st2 == tnd.TND_OK and n2 > n
+    assert tnd.tnd_attn_fwd_workspace_size(tnd.TND_F32, 2, [0, 5, 9], [0, 5, 9], 4, 2, 64, 0.1, 1.0, INF, INF, 0,
+                                           False, False)[0] == tnd.TND_OK
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=7), tnd.TND_ERR_INVALID),
+    (dict(batch=0, cu_q=(0,), cu_kv=(0,)), tnd.TND_ERR_INVALID),
+    (dict(cu_q=(1, 5, 9)), tnd.TND_ERR_INVALID),
+    (dict(cu_q=(0, 6, 5)), tnd.TND_ERR_INVALID),
+    (dict(cu_q=(0, 0, 0)), tnd.TND_ERR_INVALID),                  # T = 0
+    (dict(cu_q=(0, 1 << 20, (1 << 20) + 1)), tnd.TND_ERR_INVALID),  # T > 1M
+    (dict(nq=3, nkv=2), tnd.TND_ERR_INVALID),                     # Nq % Nkv != 0
+    (dict(nq=512, nkv=2), tnd.TND_ERR_INVALID),                   # N > 256
+    (dict(nq=0), tnd.TND_ERR_INVALID),
+    (dict(d=0), tnd.TND_ERR_INVALID),
+    (dict(d=1024), tnd.TND_ERR_INVALID),                          # D > 768
+    (dict(keep=0.0, drop=True), tnd.TND_ERR_INVALID),
+    (dict(keep=1.5), tnd.TND_ERR_INVALID),
+    (dict(keep=0.5, drop=False), tnd.TND_ERR_NULLPTR),            # dropMask needed
+    (dict(scale=float("nan")), tnd.TND_ERR_INVALID),
+    (dict(mode=9), tnd.TND_ERR_INVALID),
+    (dict(mode=4, pre=-3, nxt=1), tnd.TND_ERR_INVALID),           # empty band
+    (dict(mode=1), tnd.TND_ERR_UNSUPPORTED),
+    (dict(mode=5), tnd.TND_ERR_UNSUPPORTED),
+    (dict(mode=6), tnd.TND_ERR_UNSUPPORTED),
+    (dict(mode=7), tnd.TND_ERR_UNSUPPORTED),
+    (dict(mode=8), tnd.TND_ERR_UNSUPPORTED),
+    (dict(mode=4, pre=3, nxt=0, cu_kv=(0, 6, 9)), tnd.TND_ERR_UNSUPPORTED),  # band with Sq != Skv
+    (dict(d=512), tnd.TND_ERR_UNSUPPORTED),
+])
+def test_workspace_size_rejects(kw, expect):
+    assert ws(**kw)[0] == expect
+
+
+def test_null_workspace_size_pointer_and_seqlens():
+    L = tnd.lib()
+    assert L.tnd_attn_grad_workspace_size(1, 1, None, None, 1, 1, 128, 0.1, 1.0, 0, 0, 0, 0, 0, None) == \
+        tnd.TND_ERR_NULLPTR
+
+
+def _grad_call(**over):
+    """tnd_attn_grad with fake aligned device addresses; only arguments that
+    fail validation are used, so nothing is ever dereferenced."""
+    args = dict(query=4096, key=4096, value=4096, dy=4096, drop_mask=None, softmax_max=4096, softmax_sum=4096,
+                attention_in=4096, sink=None, dtype=tnd.TND_BF16, batch=1, cu_q=[0, 8], cu_kv=[0, 8], head_num=2,
+                kv_head_num=1, head_dim=128, scale_value=0.1, keep_prob=1.0, pre_tokens=INF, next_tokens=INF,
+                sparse_mode=3, dq=4096, dk=4096, dv=4096, dsink=None, workspace=None, workspace_size=0, stream=None)
+    args.update(over)
+    return tnd.tnd_attn_grad(*args.values())
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(query=None), tnd.TND_ERR_NULLPTR),
+    (dict(dy=None), tnd.TND_ERR_NULLPTR),
+    (dict(attention_in=None), tnd.TND_ERR_NULLPTR),
+    (dict(dv=None), tnd.TND_ERR_NULLPTR),
+    (dict(sink=4096, dsink=None), tnd.TND_ERR_NULLPTR),
+    (dict(keep_prob=0.9), tnd.TND_ERR_NULLPTR),
+    (dict(head_num=3, kv_head_num=2), tnd.TND_ERR_INVALID),
+    (dict(query=4098), tnd.TND_ERR_INVALID),                     # misaligned
+    (dict(workspace=None, workspace_size=0), tnd.TND_ERR_WORKSPACE),
+    (dict(workspace=4096, workspace_size=16), tnd.TND_ERR_WORKSPACE),
+    (dict(workspace=4096 + 16, workspace_size=1 << 30), tnd.TND_ERR_WORKSPACE),  # not 256-aligned
+])
+def test_grad_rejects_before_device_work(over, expect):
+    assert _grad_call(**over) == expect
+
+
+def test_set_option_checks_values():
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, 5) == tnd.TND_ERR_INVALID
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_WAIT_LIMIT_MS, 0) == tnd.TND_ERR_INVALID
+    assert tnd.tnd_attn_set_option(99, 0) == tnd.TND_ERR_INVALID
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, 0) == tnd.TND_OK
+
+
+# ---------------------------------------------------------------------------
+# host-side gradient plan
+# ---------------------------------------------------------------------------
+
+def _keep(mode, pre, nxt, sq, skv, i, j):
+    if mode == 0:
+        return True
+    if mode == 2:
+        return j <= i
+    if mode == 3:
+        return j <= i + skv - sq
+    return -pre <= j - i <= nxt
+
+
+def _tiles(mode, pre, nxt, sq, skv):
+    """Brute force: set of (q block, kv block) with a kept pair, and kept pairs."""
+    tiles, kept = set(), 0
+    for i in range(sq):
+        for j in range(skv):
+            if _keep(mode, pre, nxt, sq, skv, i, j):
+                tiles.add((i // 64, j // 128))
+                kept += 1
+    return tiles, kept
+
+
+PLANS = [
+    ([300, 129, 1, 0, 700], [300, 129, 1, 5, 700], 4, 2, 3, INF, INF),
+    ([400, 50], [100, 600], 2, 2, 3, INF, INF),
+    ([700, 257], [700, 257], 2, 1, 4, 200, 0),
+    ([700, 257], [700, 257], 2, 1, 4, 30, 150),
+    ([130, 65], [500, 7], 2, 2, 0, INF, INF),
+    ([260, 90], [130, 300], 2, 1, 2, INF, INF),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PLANS)))
+def test_plan_covers_every_kept_tile_once_in_chain_order(case):
+    sq, skv, nq, nkv, mode, pre, nxt = PLANS[case]
+    cu_q = np.concatenate([[0], np.cumsum(sq)])
+    cu_kv = np.concatenate([[0], np.cumsum(skv)])
+    st, units, kept = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode)
+    assert st == tnd.TND_OK
+    seen = {}
+    order = {}
+    total_kept = 0
+    for b in range(len(sq)):
+        tiles, k = _tiles(mode, pre, nxt, sq[b], skv[b])
+        total_kept += k * nq
+        for g in range(nkv):
+            for (qb, j) in tiles:
+                seen[(b, g, qb, j)] = 0
+    for pos, (b, g, j, lo, hi) in enumerate(units):
+        for qb in range(lo, hi):
+            key = (b, g, qb, j)
+            assert key in seen, f"unit visits an empty tile {key}"
+            seen[key] += 1
+            order.setdefault((b, g, qb), []).append((pos, j))
+    assert all(v == 1 for v in seen.values()), "a kept tile is missed or visited twice"
+    assert kept == total_kept
+    # every kv block of every (sequence, kv head) is a unit (it writes dK/dV)
+    nunits = sum(nkv * ((s + 127) // 128) for s in skv)
+    assert len(units) == nunits
+    # the dQ chain of a q block runs from its highest kv block down: those
+    # units must be taken in that order
+    for (b, g, qb), lst in order.items():
+        js = [j for _, j in sorted(lst)]
+        assert js == sorted(js, reverse=True), (b, g, qb, js)

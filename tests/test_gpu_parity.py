@@ -1,0 +1,187 @@
+"""GPU parity: the library's forward and gradient against the fp64 oracle on
+the same seeded inputs, element by element.
+
+Small problems are compared in full (they span several 64/128-row blocks and
+ragged tails); the full-size workloads are compared on parts the oracle can
+finish in seconds (query-row suffixes, whose dQ and, for causal masks, dK/dV
+of the last key rows are exact; whole sequences of one kv group).
+Tolerance: bf16/fp16 |err| <= 1e-2 + 2e-2|ref| per element; fp32 1e-4
+relative (see gpu_helpers.tolerance).
+"""
+
+import numpy as np
+import pytest
+
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from tests import gpu_helpers as gh  # noqa: E402
+
+INF = 2147483647
+
+SMALL = {
+    # name: (dtype, seqlens_q, seqlens_kv, nq, nkv, d, mode, pre, next, keep, sink)
+    "causal_bf16_ragged": ("bf16", [37, 200, 129, 1, 300], None, 2, 2, 128, 3, INF, INF, 1.0, False),
+    "gqa_causal_bf16": ("bf16", [130, 257], None, 4, 1, 128, 3, INF, INF, 1.0, False),
+    "band_dropout_bf16": ("bf16", [300, 190], None, 4, 2, 128, 4, 64, 0, 0.9, False),
+    "band_two_sided_bf16": ("bf16", [257, 64], None, 2, 1, 128, 4, 40, 17, 1.0, False),
+    "sink_causal_bf16": ("bf16", [260, 70], None, 2, 1, 128, 3, INF, INF, 1.0, True),
+    "full_fp16_d64": ("f16", [1, 65, 130], None, 2, 2, 64, 0, INF, INF, 1.0, False),
+    "causal_fp16_d128_sink_dropout": ("f16", [150, 99], None, 2, 2, 128, 3, INF, INF, 0.8, True),
+    "causal_sq_ne_skv": ("bf16", [100, 20, 70], [40, 150, 70], 4, 2, 128, 3, INF, INF, 1.0, False),
+    "empty_sequences": ("bf16", [0, 50, 10, 77], [30, 0, 10, 77], 2, 1, 128, 3, INF, INF, 1.0, True),
+    "leftup_causal_bf16": ("bf16", [90, 40], [60, 80], 2, 2, 128, 2, INF, INF, 1.0, False),
+    "fp32_causal_d64": ("f32", [70, 33], None, 2, 1, 64, 3, INF, INF, 1.0, False),
+    "fp32_band_dropout_sink_d128": ("f32", [140, 65], None, 2, 2, 128, 4, 30, 5, 0.75, True),
+    "fp16_d96_full": ("f16", [45, 70], None, 3, 1, 96, 0, INF, INF, 1.0, False),
+    "single_token": ("bf16", [1], None, 1, 1, 128, 0, INF, INF, 1.0, False),
+}
+
+
+def _small(name, seed=777):
+    dt, sq, skv, nq, nkv, d, mode, pre, nxt, keep, sink = SMALL[name]
+    wl = workloads.custom(name, dt, sq, sq if skv is None else skv, nq, nkv, d, keep_prob=keep,
+                          pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, has_sink=sink, seed=seed)
+    return workloads.make_inputs(wl)
+
+
+@pytest.mark.parametrize("grad_path", [0, 1], ids=["auto", "cuda_core"])
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_cases_match_oracle(name, grad_path):
+    inp = _small(name)
+    got = gh.run_library(inp, grad_path=grad_path)
+    ref = gh.oracle_reference(inp)
+    gh.compare_all(inp, got, ref)
+
+
+@pytest.mark.parametrize("grad_path", [0, 1], ids=["auto", "cuda_core"])
+def test_tiny_varlen_fp16_workload(grad_path):
+    inp = workloads.make_inputs(workloads.workload("tiny_varlen_fp16"))
+    got = gh.run_library(inp, grad_path=grad_path)
+    gh.compare_all(inp, got, gh.oracle_reference(inp))
+
+
+def _suffix_rows(wl, count):
+    """Query-row mask of the last `count` rows of every sequence, and the
+    per-sequence first selected row."""
+    qm = np.zeros(wl.tq, bool)
+    row_lo = []
+    for b in range(wl.batch):
+        s = wl.seqlens_q[b]
+        lo = max(0, s - count)
+        qm[wl.cu_q[b] + lo: wl.cu_q[b + 1]] = True
+        row_lo.append(lo)
+    return qm, row_lo
+
+
+def _kv_suffix(wl, count):
+    km = np.zeros(wl.tkv, bool)
+    for b in range(wl.batch):
+        s = wl.seqlens_kv[b]
+        km[wl.cu_kv[b] + max(0, s - count): wl.cu_kv[b + 1]] = True
+    return km
+
+
+def _sequence_rows(wl, b, on_q=True):
+    cu = wl.cu_q if on_q else wl.cu_kv
+    m = np.zeros(cu[-1], bool)
+    m[cu[b]:cu[b + 1]] = True
+    return m
+
+
+def test_causal_varlen_bf16_workload_full():
+    inp = workloads.make_inputs(workloads.workload("causal_varlen_bf16"))
+    got = gh.run_library(inp)
+    wl = inp.wl
+    # kv group 3 in full (every sequence), plus query-row suffixes of all heads
+    ref = gh.oracle_reference(inp, heads=(3, 4))
+    gh.compare_all(inp, got, ref, heads=(3, 4))
+    qm, row_lo = _suffix_rows(wl, 64)
+    ref = gh.oracle_reference(inp, row_lo=row_lo)
+    gh.compare_all(inp, got, ref, q_rows=qm, kv_rows=_kv_suffix(wl, 64))
+
+
+def test_gqa_causal_bf16_workload_sampled():
+    inp = workloads.make_inputs(workloads.workload("gqa_causal_bf16"))
+    got = gh.run_library(inp)
+    wl = inp.wl
+    qm, row_lo = _suffix_rows(wl, 128)
+    for heads in ((0, 4), (28, 32)):
+        ref = gh.oracle_reference(inp, heads=heads, row_lo=row_lo)
+        gh.compare_all(inp, got, ref, q_rows=qm, kv_rows=_kv_suffix(wl, 128), heads=heads)
+    # the 4096-row sequence of kv group 5, in full
+    row_lo = [0] + [s for s in wl.seqlens_q[1:]]
+    ref = gh.oracle_reference(inp, heads=(20, 24), row_lo=row_lo)
+    gh.compare_all(inp, got, ref, q_rows=_sequence_rows(wl, 0), kv_rows=_sequence_rows(wl, 0, False),
+                   heads=(20, 24))
+
+
+def test_window_dropout_bf16_workload_sampled():
+    inp = workloads.make_inputs(workloads.workload("window_dropout_bf16"))
+    got = gh.run_library(inp)
+    wl = inp.wl
+    # sequence 5, kv group 2, in full (band keeps 1025 keys per row)
+    row_lo = [s if b != 5 else 0 for b, s in enumerate(wl.seqlens_q)]
+    ref = gh.oracle_reference(inp, heads=(8, 12), row_lo=row_lo)
+    gh.compare_all(inp, got, ref, q_rows=_sequence_rows(wl, 5), kv_rows=_sequence_rows(wl, 5, False),
+                   heads=(8, 12))
+
+
+def test_long_causal_sink_bf16_workload_sampled():
+    inp = workloads.make_inputs(workloads.workload("long_causal_sink_bf16"))
+    got = gh.run_library(inp)
+    wl = inp.wl
+    qm, row_lo = _suffix_rows(wl, 128)
+    ref = gh.oracle_reference(inp, heads=(5, 6), row_lo=row_lo)
+    hs = (5, 6)
+    res = gh.compare_all(inp, dict(got, dsink=None), ref, q_rows=qm, kv_rows=_kv_suffix(wl, 128), heads=hs)
+    # dSink = -sum_i p_sink,i D_i holds at any size: recompute it in fp64
+    # from the same forward statistics and outputs the gradient consumed
+    m = got["smax"][..., 0].double().cpu().numpy()
+    l = got["ssum"][..., 0].double().cpu().numpy()
+    o = gh.host64(got["out"])
+    dy = inp.dy64
+    D = np.einsum("tnd,tnd->tn", dy, o)
+    psink = np.exp(inp.sink.astype(np.float64)[None, :] - m) / l
+    expect = -(psink * D).sum(axis=0)
+    np.testing.assert_allclose(got["dsink"].cpu().numpy(), expect, rtol=1e-3, atol=1e-3)
+    assert res["dq"] >= 0
+
+
+def test_bilinear_identities_on_gpu_outputs():
+    """<dQ,Q> = <dK,K> per kv group and <dV,V> = <dY,O> hold exactly for the
+    true gradient; the bf16 outputs must satisfy them to rounding level."""
+    inp = workloads.make_inputs(workloads.workload("causal_varlen_bf16"))
+    got = gh.run_library(inp)
+    wl = inp.wl
+    dq, dk, dv, o = (gh.host64(got[n]) for n in ("dq", "dk", "dv", "out"))
+    g = wl.nq // wl.nkv
+    for kv in range(wl.nkv):
+        lhs = np.sum(dq[:, kv * g:(kv + 1) * g] * inp.q64[:, kv * g:(kv + 1) * g])
+        rhs = np.sum(dk[:, kv] * inp.k64[:, kv])
+        scale = np.sum(np.abs(dq[:, kv * g:(kv + 1) * g] * inp.q64[:, kv * g:(kv + 1) * g]))
+        assert abs(lhs - rhs) <= 2e-3 * scale, (kv, lhs, rhs, scale)
+    lhs, rhs = np.sum(dv * inp.v64), np.sum(inp.dy64 * o)
+    assert abs(lhs - rhs) <= 2e-3 * np.sum(np.abs(inp.dy64 * o))
+
+
+def test_gradient_is_bitwise_deterministic():
+    inp = _small("gqa_causal_bf16")
+    dev = gh.upload(inp)
+    a = gh.run_library(inp, dev)
+    b = gh.run_library(inp, dev)
+    for n in ("dq", "dk", "dv"):
+        assert torch.equal(a[n].view(torch.int16), b[n].view(torch.int16)), n
+
+
+def test_paths_agree_closely():
+    """The tensor-core and CUDA-core gradients agree to bf16 rounding."""
+    inp = _small("causal_bf16_ragged")
+    dev = gh.upload(inp)
+    a = gh.run_library(inp, dev, grad_path=0)
+    b = gh.run_library(inp, dev, grad_path=1)
+    for n in ("dq", "dk", "dv"):
+        x, y = gh.host64(a[n]), gh.host64(b[n])
+        assert np.all(np.abs(x - y) <= 1e-2 + 2e-2 * np.abs(y)), n
