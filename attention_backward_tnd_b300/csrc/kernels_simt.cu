@@ -61,17 +61,18 @@ __device__ __forceinline__ float quad_sum(float x)
 }
 
 // Cooperative load of rows [r0, r0+R) of a [rows, nheads, D] tensor (head hh)
-// into smem as fp32 [R][DMAX]; rows at or past `limit` read as 0.
+// into smem as fp32 [R][DMAX]; rows at or past `limit` and columns at or past
+// D read as 0 (the row kernels multiply whole DMAX-wide rows).
 template <typename T, int DMAX>
 __device__ __forceinline__ void load_tile(float *dst, const T *src, int64_t row_base, int64_t r0,
                                           int64_t limit, int nheads, int hh, int D, float mul)
 {
-    for (int e = threadIdx.x; e < R * D; e += kThreads) {
-        const int rr = e / D, cc = e - rr * D;
+    for (int e = threadIdx.x; e < R * DMAX; e += kThreads) {
+        const int rr = e / DMAX, cc = e - rr * DMAX;
         const int64_t row = r0 + rr;
         float x = 0.0f;
-        if (row < limit) x = Elem<T>::load(src + ((row_base + row) * nheads + hh) * (int64_t)D + cc) * mul;
-        dst[rr * DMAX + cc] = x;
+        if (row < limit && cc < D) x = Elem<T>::load(src + ((row_base + row) * nheads + hh) * (int64_t)D + cc) * mul;
+        dst[e] = x;
     }
 }
 

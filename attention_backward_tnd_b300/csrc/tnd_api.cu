@@ -144,6 +144,13 @@ MaskSpec mask_of(const Problem &p)
     return m;
 }
 
+int64_t mask_bits_total(const Problem &p)
+{
+    int64_t n = 0;
+    for (int64_t b = 0; b < p.batch; ++b) n += p.nq * (p.cuq[b + 1] - p.cuq[b]) * (p.cukv[b + 1] - p.cukv[b]);
+    return n;
+}
+
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -528,16 +535,23 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     a.n_qblk = (int32_t)pl.qblk.size();
     a.flags = (int32_t *)(w + L.flags);
     a.dqacc = tc_layout ? (float *)(w + L.dqacc) : nullptr;
+    a.uncovered = (const int2 *)(w + L.uncovered);
+    a.n_uncovered = (int32_t)pl.uncovered.size();
+    a.mask_bytes = (mask_bits_total(p) + 7) / 8;
     {
-        int dev = 0, khz = 0;
+        int dev = 0, khz = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (khz <= 0) khz = 2000000;
         a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)khz;
+        a.num_sms = sms > 0 ? sms : 148;
     }
     if (timed(K_PREPASS, s, [&] { return launch_prepass(a, tc, s); }) != cudaSuccess) return TND_ERR_CUDA;
     if (tc) {
         if (timed(K_TC, s, [&] { return launch_grad_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+        if (a.n_uncovered > 0 &&
+            timed(K_ZERO, s, [&] { return launch_zero_dq(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
     } else {
         if (timed(K_DKDV, s, [&] { return launch_grad_dkdv_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         if (timed(K_DQ, s, [&] { return launch_grad_dq_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;

@@ -75,6 +75,7 @@ struct QBlockInfo {
 struct GradArgs {
     const void *q, *k, *v, *dy, *o;
     const uint8_t *drop_mask;
+    int64_t mask_bytes;       // size of drop_mask in bytes
     const float *smax, *ssum, *sink;
     void *dq, *dk, *dv;
     float *dsink;
@@ -101,7 +102,10 @@ struct GradArgs {
     int32_t n_qblk;
     int32_t *flags;           // [n_qblk][Nq] contributions added so far
     float *dqacc;             // [Tq][Nq][D] fp32 partial sums
+    const int2 *uncovered;    // (b, first row) of q blocks no kv block reaches
+    int32_t n_uncovered;
     int64_t wait_limit_cycles;
+    int32_t num_sms;
 };
 
 struct FwdArgs {
@@ -131,5 +135,7 @@ cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s);
 // Tensor-core gradient (bf16/fp16, D = 128); false if this build lacks it.
 bool grad_tc_supported(int dtype, int d);
 cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s);
+// Zeroes dQ rows of q blocks that no kv block reaches (tensor-core path).
+cudaError_t launch_zero_dq(const GradArgs &a, cudaStream_t s);
 
 }  // namespace tnd

@@ -68,11 +68,13 @@ def oracle_reference(inp: workloads.Inputs, **kw):
 
 def tolerance(dtype: str, ref: np.ndarray):
     """Per-element bound: bf16/fp16 |err| <= 1e-2 + 2e-2|ref|; fp32 relative
-    1e-4, floored at 1e-6 of the tensor's RMS so exact zeros stay checkable."""
+    1e-4, with an absolute floor of 1e-5 x the tensor's RMS for elements whose
+    reference nearly cancels (fp32 sums of O(1) terms carry ~1e-7 absolute
+    error however small the result)."""
     if dtype in ("bf16", "f16"):
         return 1e-2 + 2e-2 * np.abs(ref)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
-    return 1e-4 * np.abs(ref) + 1e-6 * max(rms, 1e-30)
+    return 1e-4 * np.abs(ref) + 1e-5 * max(rms, 1e-30)
 
 
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str, mask=None):
@@ -86,11 +88,13 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str, mask=N
     err = np.abs(got - ref)
     tol = tolerance(dtype, ref)
     bad = ~(err <= tol)
-    worst = int(np.argmax(err))
-    maxnorm = float(err.reshape(-1)[worst])
-    assert not bad.any(), (f"{what}: {int(bad.sum())} of {got.size} elements out of tolerance; max |err| "
-                           f"{maxnorm:.3e} at flat {worst} (got {got.reshape(-1)[worst]:.6g}, "
-                           f"ref {ref.reshape(-1)[worst]:.6g})")
+    maxnorm = float(np.nanmax(err)) if not np.isnan(err).all() else float("nan")
+    if bad.any():
+        ratio = np.where(np.isnan(err), np.inf, err / tol).reshape(-1)
+        w = int(np.argmax(ratio))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} elements out of tolerance; max |err| "
+                             f"{maxnorm:.3e}; worst at flat {w}: got {got.reshape(-1)[w]:.6g}, ref "
+                             f"{ref.reshape(-1)[w]:.6g}, tol {tol.reshape(-1)[w]:.3e}")
     return maxnorm
 
 
