@@ -298,6 +298,7 @@ def run_ours(args, wl, rank, world, local_rank):
                  wl.next_tokens, wl.sparse_mode, mask, sink, workspace=ws, outputs=outs)
 
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_PROFILE, 1) == tnd.TND_OK
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, 1 if args.grad_path == "cuda_core" else 0) == tnd.TND_OK
     for _ in range(max(args.warmup, 0)):
         flush.fill_(1)
         step()
@@ -389,7 +390,8 @@ def run_ours(args, wl, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) inputs; forward O/max/sum "
             "from this library's forward)",
-            "config": dict(workload_config(wl), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "config": dict(workload_config(wl), grad_path=args.grad_path,
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "pct_of_bf16_peak": 100.0 * (value / world) / peak, "peak_source": peak_src,
             "roofline": {"bound": "tensor", "kernel": main, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
@@ -419,6 +421,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grad-path", default="auto", choices=["auto", "cuda_core"],
+                    help="auto: tensor-core kernel where it applies; cuda_core: the CUDA-core kernels")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
