@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -165,6 +166,7 @@ struct Plan {
     std::vector<QBlockInfo> qblk;
     std::vector<int2> uncovered;  // (b, first row) of 64-row q blocks nothing contributes to
     int64_t kept_pairs = 0;       // summed over sequences and query heads
+    std::vector<unsigned char> image;  // status words + plan arrays, as copied to the workspace
 };
 
 // Union of the kept key ranges of query rows [r0, r1) (empty: lo > hi).
@@ -270,10 +272,10 @@ struct Layout {
     size_t flags = 0, lse2 = 0, drow = 0, sinkrow = 0, dqacc = 0, total = 0;
 };
 
-Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
+// Offsets of the copied plan (status words first); the rest of the layout
+// follows plan_end.
+void plan_offsets(const Plan &pl, Layout &L, size_t &off)
 {
-    Layout L;
-    size_t off = kStatusBytes;
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off = round_up(off + bytes, 256);
@@ -286,6 +288,18 @@ Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
     L.qblk = take(pl.qblk.size() * sizeof(QBlockInfo));
     L.uncovered = take(pl.uncovered.size() * sizeof(int2));
     L.plan_end = off;
+}
+
+Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
+{
+    Layout L;
+    size_t off = kStatusBytes;
+    plan_offsets(pl, L, off);
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = round_up(off + bytes, 256);
+        return o;
+    };
     if (grad) {
         const size_t rows = (size_t)p.tq * (size_t)p.nq;
         L.flags = take(tc ? pl.qblk.size() * (size_t)p.nq * sizeof(int32_t) : 0);
@@ -298,16 +312,16 @@ Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
     return L;
 }
 
-bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
-
-// Copies the plan into the workspace and clears the status words (and the
-// dQ chain flags of the tensor-core path).
-tnd_status upload_plan(const Plan &pl, const Layout &L, void *ws, bool clear_flags, const Problem &p,
-                       cudaStream_t s)
+// Host image of the workspace's first plan_end bytes: zeroed status words,
+// then the plan arrays at their offsets.
+void build_image(Plan &pl)
 {
-    std::vector<unsigned char> host(L.plan_end, 0);
-    auto put = [&](size_t off, const void *src, size_t bytes) {
-        if (bytes) std::memcpy(host.data() + off, src, bytes);
+    Layout L;
+    size_t off = kStatusBytes;
+    plan_offsets(pl, L, off);
+    pl.image.assign(L.plan_end, 0);
+    auto put = [&](size_t o, const void *src, size_t bytes) {
+        if (bytes) std::memcpy(pl.image.data() + o, src, bytes);
     };
     put(L.seqs, pl.seqs.data(), pl.seqs.size() * sizeof(SeqDesc));
     put(L.q_items, pl.q_items.data(), pl.q_items.size() * sizeof(int2));
@@ -315,8 +329,58 @@ tnd_status upload_plan(const Plan &pl, const Layout &L, void *ws, bool clear_fla
     put(L.units, pl.units.data(), pl.units.size() * sizeof(GradUnit));
     put(L.qblk, pl.qblk.data(), pl.qblk.size() * sizeof(QBlockInfo));
     put(L.uncovered, pl.uncovered.data(), pl.uncovered.size() * sizeof(int2));
-    // status words start at zero (host buffer is zero-filled there)
-    if (cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, s) != cudaSuccess) return TND_ERR_CUDA;
+}
+
+// Plans depend only on the sequence table, head counts and the mask; calls
+// that repeat a problem (every training step of a fixed batch) reuse the
+// plan instead of rebuilding it.  Small LRU, shared by all threads.
+struct PlanKey {
+    int64_t batch, nq, nkv, mode, pre, next;
+    bool with_units;
+    std::vector<int64_t> cuq, cukv;
+    bool operator==(const PlanKey &o) const
+    {
+        return batch == o.batch && nq == o.nq && nkv == o.nkv && mode == o.mode && pre == o.pre && next == o.next &&
+               with_units == o.with_units && cuq == o.cuq && cukv == o.cukv;
+    }
+};
+constexpr size_t kPlanCacheSize = 8;
+std::vector<std::pair<PlanKey, std::shared_ptr<const Plan>>> g_plan_cache;  // most recent last
+std::mutex g_plan_mu;
+
+std::shared_ptr<const Plan> get_plan(const Problem &p, bool with_units)
+{
+    PlanKey key{p.batch, p.nq, p.nkv, p.mode, p.pre, p.next, with_units,
+                std::vector<int64_t>(p.cuq, p.cuq + p.batch + 1), std::vector<int64_t>(p.cukv, p.cukv + p.batch + 1)};
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        for (size_t i = g_plan_cache.size(); i-- > 0;) {
+            if (g_plan_cache[i].first == key) {
+                auto hit = g_plan_cache[i];
+                g_plan_cache.erase(g_plan_cache.begin() + (long)i);
+                g_plan_cache.push_back(hit);
+                return hit.second;
+            }
+        }
+    }
+    auto pl = std::make_shared<Plan>();
+    build_plan(p, with_units, *pl);
+    build_image(*pl);
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (g_plan_cache.size() >= kPlanCacheSize) g_plan_cache.erase(g_plan_cache.begin());
+    g_plan_cache.emplace_back(std::move(key), pl);
+    return pl;
+}
+
+bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
+
+// Copies the plan into the workspace and clears the status words (and the
+// dQ chain flags of the tensor-core path).
+tnd_status upload_plan(const Plan &pl, const Layout &L, void *ws, bool clear_flags, const Problem &p,
+                       cudaStream_t s)
+{
+    if (cudaMemcpyAsync(ws, pl.image.data(), pl.image.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return TND_ERR_CUDA;
     if (clear_flags) {
         const size_t bytes = pl.qblk.size() * (size_t)p.nq * sizeof(int32_t);
         if (bytes && cudaMemsetAsync((char *)ws + L.flags, 0, bytes, s) != cudaSuccess) return TND_ERR_CUDA;
@@ -429,9 +493,8 @@ tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int
     tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode, has_drop != 0,
                              has_sink != 0, p);
     if (st != TND_OK) return st;
-    Plan pl;
-    build_plan(p, false, pl);
-    *ws_size = layout_for(p, pl, false, false).total;
+    auto plp = get_plan(p, false);
+    *ws_size = layout_for(p, *plp, false, false).total;
     return TND_OK;
 }
 
@@ -447,8 +510,8 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, (const void *)out, (const void *)smax, (const void *)ssum})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
-    Plan pl;
-    build_plan(p, false, pl);
+    auto plp = get_plan(p, false);
+    const Plan &pl = *plp;
     const Layout L = layout_for(p, pl, false, false);
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
@@ -478,9 +541,8 @@ tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const in
                              has_sink != 0, p);
     if (st != TND_OK) return st;
     const bool tc = grad_tc_supported(p.dtype, (int)p.d);
-    Plan pl;
-    build_plan(p, tc, pl);
-    *ws_size = layout_for(p, pl, true, tc).total;
+    auto plp = get_plan(p, tc);
+    *ws_size = layout_for(p, *plp, true, tc).total;
     return TND_OK;
 }
 
@@ -501,8 +563,8 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
         if (!aligned16(ptr)) return TND_ERR_INVALID;
     const bool tc_layout = grad_tc_supported(p.dtype, (int)p.d);
     const bool tc = use_tc(p);
-    Plan pl;
-    build_plan(p, tc_layout, pl);
+    auto plp = get_plan(p, tc_layout);
+    const Plan &pl = *plp;
     const Layout L = layout_for(p, pl, true, tc_layout);
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;

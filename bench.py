@@ -23,9 +23,7 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -102,56 +100,77 @@ def traffic_record(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled every 10 ms by an
+    NVML thread; summary() keeps the samples taken inside the marked timed
+    region (None when NVML is unavailable)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.samples = []          # (host time, sm MHz, max MHz, reason bits)
+        self.t0 = self.t1 = None
+        self._stop = False
+        self._thread = None
+        self._handle = None
 
-    def __init__(self, device_index: int):
-        self.idx = device_index
-        self.proc = None
-        self.file = None
+    def _open(self):
+        import pynvml
+        import torch
+        pynvml.nvmlInit()
+        props = torch.cuda.get_device_properties(self.dev)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        try:
+            self._handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+        except pynvml.NVMLError:
+            self._handle = pynvml.nvmlDeviceGetHandleByIndex(0)
+        self._nvml = pynvml
+
+    def _reasons(self):
+        n = self._nvml
+        fn = getattr(n, "nvmlDeviceGetCurrentClocksEventReasons", None) or n.nvmlDeviceGetCurrentClocksThrottleReasons
+        return int(fn(self._handle))
+
+    def _run(self):
+        n = self._nvml
+        while not self._stop:
+            try:
+                sm = n.nvmlDeviceGetClockInfo(self._handle, n.NVML_CLOCK_SM)
+                mx = n.nvmlDeviceGetMaxClockInfo(self._handle, n.NVML_CLOCK_SM)
+                self.samples.append((time.perf_counter(), float(sm), float(mx), self._reasons()))
+            except Exception:  # pragma: no cover - transient NVML errors
+                pass
+            time.sleep(0.01)
 
     def __enter__(self):
+        import threading
         try:
-            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.idx)], stdout=self.file,
-                                         stderr=subprocess.DEVNULL)
-        except (OSError, ValueError):
-            self.proc = None
+            self._open()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        except Exception:
+            self._thread = None
         return self
 
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.perf_counter()
+        else:
+            self.t1 = time.perf_counter()
+
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self._stop = True
+        if self._thread is not None:
+            self._thread.join(timeout=2)
 
     def summary(self):
-        if self.proc is None or self.file is None:
+        if not self.samples:
             return None
-        self.file.flush()
-        rows = []
-        with open(self.file.name) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-                except ValueError:
-                    continue
-        os.unlink(self.file.name)
-        if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for _, _, flags in rows for k, fl in enumerate(flags) if fl.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        inside = [x for x in self.samples if self.t0 is not None and self.t1 is not None and self.t0 <= x[0] <= self.t1]
+        rows = inside or self.samples[-3:]
+        bits = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+                "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+        reasons = sorted({name for _, _, _, r in rows for name, b in bits.items() if r & b})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows), "in_timed_region": bool(inside), "source": "nvml"}
 
 
 def workload_config(wl, l2_note=True):
@@ -312,14 +331,17 @@ def run_ours(args, wl, rank, world, local_rank):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(dev) as clk:
+        time.sleep(0.05)
         wall0 = time.perf_counter()
+        clk.mark(True)
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             starts[i].record()
             step()
             ends[i].record()
         torch.cuda.synchronize()
+        clk.mark(False)
         wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
@@ -416,7 +438,7 @@ def run_ours(args, wl, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
