@@ -27,7 +27,7 @@ TND_OPT_GRAD_PATH, TND_OPT_WAIT_LIMIT_MS, TND_OPT_PROFILE = 0, 1, 2
 # exported symbols, in header order
 SYMBOLS = ["tnd_attn_fwd_workspace_size", "tnd_attn_fwd", "tnd_attn_grad_workspace_size", "tnd_attn_grad",
            "tnd_attn_device_status", "tnd_status_string", "tnd_attn_set_option", "tnd_attn_profile_read",
-           "tnd_attn_grad_plan"]
+           "tnd_attn_grad_plan", "tnd_attn_grad_static_ws"]
 
 
 class TndError(RuntimeError):
@@ -65,6 +65,9 @@ def lib():
                                             _i64p, _int, ctypes.POINTER(ctypes.c_int), _int]
         L.tnd_attn_grad_plan.argtypes = [_i64, _i64p, _i64p, _i64, _i64, _i64, _i64, _i64, _i64p, _i64, _i64p,
                                          _i64p]
+        L.tnd_attn_grad_static_ws.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p,
+                                              _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                              _vp, _vp]
         for name in SYMBOLS:
             if name != "tnd_status_string":
                 getattr(L, name).restype = _int
@@ -124,6 +127,20 @@ def tnd_attn_grad(query, key, value, dy, drop_mask, softmax_max, softmax_sum, at
                                dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim, scale_value,
                                keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv, dsink, workspace,
                                workspace_size, stream)
+
+
+def tnd_attn_grad_static_ws(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink, dtype,
+                            batch, cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens,
+                            next_tokens, sparse_mode, dq, dk, dv, dsink, stream):
+    """tnd_attn_grad with the library's own fixed device workspace (no allocation)."""
+    cq, ck = _cu(cu_q), _cu(cu_kv)
+    return lib().tnd_attn_grad_static_ws(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in,
+                                         sink, dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim,
+                                         scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv,
+                                         dsink, stream)
+
+
+TND_STATIC_WS_BYTES = 32 << 20
 
 
 def tnd_attn_device_status(workspace, workspace_size, stream):

@@ -185,6 +185,41 @@ tnd_status tnd_attn_grad_plan(
     int64_t kv_head_num, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
     int64_t *units, int64_t capacity, int64_t *n_units, int64_t *kept_pairs);
 
+/*
+ * Gradient without a caller-provided workspace.  The pages have no
+ * counterpart: their operator always takes a workspace the caller allocates.
+ *
+ * For callers that cannot allocate device memory, for instance code that
+ * runs while a stream is being captured (cudaMalloc is not allowed there),
+ * a plug-in that only receives buffers from its host framework's allocator,
+ * or a process that reserved all device memory at start-up.  Arguments and
+ * results are those of tnd_attn_grad without `workspace` / `workspace_size`;
+ * the caller still passes every input and output.
+ *
+ * The workspace is a fixed device array inside this library of
+ * TND_STATIC_WS_BYTES bytes, held on every GPU that loads the library until
+ * the process exits.  A problem whose tnd_attn_grad_workspace_size exceeds
+ * it returns TND_ERR_WORKSPACE before any device work.  No call allocates
+ * device memory (no cudaMalloc / cudaFree, no allocating library routine).
+ * The first call on each device looks the array's device address up (with
+ * that device current) and keeps it; make that first call before any stream
+ * capture.  Every call shares the one array and it keeps the last call's
+ * contents: each call rewrites the parts that must start at zero (status
+ * words, dQ chain counters) on its stream before its kernels run, so calls
+ * in sequence are independent, but calls that overlap on the GPU (other
+ * streams, other host threads) race on it and give wrong results.  Device
+ * errors of such a call are not reported through tnd_attn_device_status.
+ */
+#define TND_STATIC_WS_BYTES (32ull << 20)
+tnd_status tnd_attn_grad_static_ws(
+    const void *query, const void *key, const void *value, const void *dy,
+    const uint8_t *drop_mask, const float *softmax_max, const float *softmax_sum,
+    const void *attention_in, const float *sink, tnd_dtype dtype, int64_t batch,
+    const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, int64_t head_num,
+    int64_t kv_head_num, int64_t head_dim, double scale_value, double keep_prob,
+    int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode, void *dq, void *dk, void *dv,
+    float *dsink, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
