@@ -72,11 +72,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary of `kernel`, if it
-    was taken on the current kernel source (else None)."""
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel` on
+    `workload`, if it was taken on the current kernel source (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -365,7 +365,7 @@ def run_ours(args, wl, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flop / (main_ms * 1e-3) / 1e12
-    traffic = traffic_record(main)
+    traffic = traffic_record(main, wl.name)
 
     # end to end: pinned host inputs -> device, gradient, device -> pinned host outputs
     host_in = [t.cpu().pin_memory() for t in (q, k, v, dy, out, smax, ssum)]
