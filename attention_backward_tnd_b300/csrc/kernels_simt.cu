@@ -152,28 +152,40 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// gradient prepass: one warp per (token, query head)
+// gradient prepass: one warp per (q block, query head, row of the block);
+// writes the blocked per-row vectors, padded rows included
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t nrows = a.tq * a.nq;
+    const int64_t nrows = (int64_t)a.n_qblk * a.nq * kQBlock;
     const T *dY = (const T *)a.dy, *O = (const T *)a.o;
-    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < nrows; r += (int64_t)gridDim.x * 8) {
-        const int64_t t = r / a.nq;
-        const int h = (int)(r - t * a.nq);
+    for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < nrows; w += (int64_t)gridDim.x * 8) {
+        const int64_t blk = w / kQBlock;               // q block * nq + h
+        const int rr = (int)(w - blk * kQBlock);
+        const int qg = (int)(blk / a.nq), h = (int)(blk - (int64_t)qg * a.nq);
+        const int2 qr = a.qblk_rows[qg];
+        const SeqDesc sd = a.seqs[qr.x];
+        const int64_t i = (int64_t)qr.y + rr;
+        if (i >= sd.sq) {
+            if (lane == 0) {
+                a.drow[w] = 0.0f;
+                a.lse2[w] = INFINITY;
+                if (a.has_sink) a.sinkrow[w] = 0.0f;
+            }
+            continue;
+        }
+        const int64_t r = (sd.tq + i) * a.nq + h;
         float dot = 0.0f;
         for (int c = lane; c < a.d; c += 32) dot += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
         dot = warp_sum(dot);
         if (lane == 0) {
             const float m = a.smax[r * 8], l = a.ssum[r * 8];
             const bool live = l > 0.0f;
-            a.drow[(int64_t)h * a.tq + t] = dot;
-            a.lse2[(int64_t)h * a.tq + t] = live ? m * kLog2e + lg2(l) : INFINITY;
-            if (a.has_sink) {
-                a.sinkrow[(int64_t)h * a.tq + t] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * dot : 0.0f;
-            }
+            a.drow[w] = dot;
+            a.lse2[w] = live ? m * kLog2e + lg2(l) : INFINITY;
+            if (a.has_sink) a.sinkrow[w] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * dot : 0.0f;
         }
     }
 }
@@ -223,8 +235,8 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
             if (threadIdx.x < R) {
                 const int64_t i = qt + threadIdx.x;
                 const bool ok = i < sd.sq;
-                lses[threadIdx.x] = ok ? a.lse2[(int64_t)h * a.tq + sd.tq + i] : INFINITY;
-                Ds[threadIdx.x] = ok ? a.drow[(int64_t)h * a.tq + sd.tq + i] : 0.0f;
+                lses[threadIdx.x] = ok ? a.lse2[row_vec_index(sd, a.nq, h, i)] : INFINITY;
+                Ds[threadIdx.x] = ok ? a.drow[row_vec_index(sd, a.nq, h, i)] : 0.0f;
             }
             __syncthreads();
             for (int rr = 0; rr < R; ++rr) {
@@ -295,8 +307,8 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
         dyreg[k] = ok ? Elem<T>::load(dY + off) : 0.0f;
         acc[k] = 0.0f;
     }
-    const float lse = row_ok ? a.lse2[(int64_t)h * a.tq + sd.tq + i] : INFINITY;
-    const float Di = row_ok ? a.drow[(int64_t)h * a.tq + sd.tq + i] : 0.0f;
+    const float lse = row_ok ? a.lse2[row_vec_index(sd, a.nq, h, i)] : INFINITY;
+    const float Di = row_ok ? a.drow[row_vec_index(sd, a.nq, h, i)] : 0.0f;
     int64_t lo = 1, hi = 0;
     if (row_ok) key_range(a.mask, sd.sq, sd.skv, i, lo, hi);
     int64_t ulo, uhi;
@@ -336,14 +348,19 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// dSink_h = sum over all query rows of the head of -p_sink * D (fixed order)
+// dSink_h = sum over all query rows of the head of -p_sink * D (fixed order;
+// padded rows hold 0)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) sink_reduce_kernel(GradArgs a)
 {
     __shared__ float part[256];
     const int h = blockIdx.x;
     float acc = 0.0f;
-    for (int64_t t = threadIdx.x; t < a.tq; t += 256) acc += a.sinkrow[(int64_t)h * a.tq + t];
+    const int64_t n = (int64_t)a.n_qblk * kQBlock;
+    for (int64_t e = threadIdx.x; e < n; e += 256) {
+        const int64_t qg = e / kQBlock;
+        acc += a.sinkrow[(qg * a.nq + h) * kQBlock + (e - qg * kQBlock)];
+    }
     part[threadIdx.x] = acc;
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
@@ -410,7 +427,7 @@ template <typename T, int DMAX> struct DqLaunch {
 template <typename T, int DMAX> struct PrepassLaunch {
     static cudaError_t run(const GradArgs &a, cudaStream_t s)
     {
-        const int64_t rows = a.tq * a.nq;
+        const int64_t rows = (int64_t)a.n_qblk * a.nq * kQBlock;
         if (rows == 0) return cudaSuccess;
         const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 148 * 16);
         prepass_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(a);

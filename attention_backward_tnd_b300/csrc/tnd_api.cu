@@ -31,9 +31,9 @@ struct ProfEntry {
     cudaEvent_t start, stop;
 };
 const char *kKindNames[] = {"fwd_simt", "grad_prepass", "grad_dkdv_simt", "grad_dq_simt",
-                            "grad_sink_reduce", "grad_tc_main", "grad_zero_dq"};
+                            "grad_sink_reduce", "grad_tc_main", "grad_dq_finalize"};
 constexpr int kNumKinds = sizeof(kKindNames) / sizeof(kKindNames[0]);
-enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_ZERO };
+enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN };
 std::vector<ProfEntry> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 constexpr size_t kProfCap = 4096;
@@ -164,7 +164,7 @@ struct Plan {
     std::vector<int2> q_items, kv_items;
     std::vector<GradUnit> units;
     std::vector<QBlockInfo> qblk;
-    std::vector<int2> uncovered;  // (b, first row) of 64-row q blocks nothing contributes to
+    std::vector<int2> qblk_rows;  // (b, first row) of every 64-row q block, in global order
     int64_t kept_pairs = 0;       // summed over sequences and query heads
     std::vector<unsigned char> image;  // status words + plan arrays, as copied to the workspace
 };
@@ -210,6 +210,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         qblk0 += sd.nqblk;
         for (int64_t r = 0; r < sq; r += kSimtRows) pl.q_items.push_back(make_int2((int)b, (int)r));
         for (int64_t r = 0; r < skv; r += kSimtRows) pl.kv_items.push_back(make_int2((int)b, (int)r));
+        for (int64_t r = 0; r < sq; r += kQBlock) pl.qblk_rows.push_back(make_int2((int)b, (int)r));
         for (int64_t i = 0; i < sq; ++i) {
             int64_t lo, hi;
             key_range(m, sq, skv, i, lo, hi);
@@ -224,7 +225,6 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
             QBlockInfo qi;
             if (ulo > uhi) {
                 qi.jlo = qi.jhi = -1;
-                pl.uncovered.push_back(make_int2((int)b, (int)(qb * kQBlock)));
             } else {
                 qi.jlo = (int32_t)(ulo / kKvBlock);
                 qi.jhi = (int32_t)(uhi / kKvBlock);
@@ -267,7 +267,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-    size_t seqs = 0, q_items = 0, kv_items = 0, units = 0, qblk = 0, uncovered = 0;  // offsets of the
+    size_t seqs = 0, q_items = 0, kv_items = 0, units = 0, qblk = 0, qblk_rows = 0;  // offsets of the
     size_t plan_end = 0;                                                                // copied plan
     size_t flags = 0, lse2 = 0, drow = 0, sinkrow = 0, dqacc = 0, total = 0;
 };
@@ -286,7 +286,7 @@ void plan_offsets(const Plan &pl, Layout &L, size_t &off)
     L.kv_items = take(pl.kv_items.size() * sizeof(int2));
     L.units = take(pl.units.size() * sizeof(GradUnit));
     L.qblk = take(pl.qblk.size() * sizeof(QBlockInfo));
-    L.uncovered = take(pl.uncovered.size() * sizeof(int2));
+    L.qblk_rows = take(pl.qblk_rows.size() * sizeof(int2));
     L.plan_end = off;
 }
 
@@ -301,12 +301,12 @@ Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
         return o;
     };
     if (grad) {
-        const size_t rows = (size_t)p.tq * (size_t)p.nq;
+        const size_t vec = pl.qblk_rows.size() * (size_t)p.nq * kQBlock;  // blocked per-row vectors
         L.flags = take(tc ? pl.qblk.size() * (size_t)p.nq * sizeof(int32_t) : 0);
-        L.lse2 = take(rows * sizeof(float));
-        L.drow = take(rows * sizeof(float));
-        L.sinkrow = take(p.has_sink ? rows * sizeof(float) : 0);
-        L.dqacc = take(tc ? rows * (size_t)p.d * sizeof(float) : 0);
+        L.lse2 = take(vec * sizeof(float));
+        L.drow = take(vec * sizeof(float));
+        L.sinkrow = take(p.has_sink ? vec * sizeof(float) : 0);
+        L.dqacc = take(tc ? (size_t)p.tq * (size_t)p.nq * (size_t)p.d * sizeof(float) : 0);
     }
     L.total = off;
     return L;
@@ -328,7 +328,7 @@ void build_image(Plan &pl)
     put(L.kv_items, pl.kv_items.data(), pl.kv_items.size() * sizeof(int2));
     put(L.units, pl.units.data(), pl.units.size() * sizeof(GradUnit));
     put(L.qblk, pl.qblk.data(), pl.qblk.size() * sizeof(QBlockInfo));
-    put(L.uncovered, pl.uncovered.data(), pl.uncovered.size() * sizeof(int2));
+    put(L.qblk_rows, pl.qblk_rows.data(), pl.qblk_rows.size() * sizeof(int2));
 }
 
 // Plans depend only on the sequence table, head counts and the mask; calls
@@ -594,11 +594,10 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     a.units = (const GradUnit *)(w + L.units);
     a.n_units = (int32_t)pl.units.size();
     a.qblk = (const QBlockInfo *)(w + L.qblk);
-    a.n_qblk = (int32_t)pl.qblk.size();
+    a.qblk_rows = (const int2 *)(w + L.qblk_rows);
+    a.n_qblk = (int32_t)pl.qblk_rows.size();
     a.flags = (int32_t *)(w + L.flags);
     a.dqacc = tc_layout ? (float *)(w + L.dqacc) : nullptr;
-    a.uncovered = (const int2 *)(w + L.uncovered);
-    a.n_uncovered = (int32_t)pl.uncovered.size();
     a.mask_bytes = (mask_bits_total(p) + 7) / 8;
     {
         int dev = 0, khz = 0, sms = 0;
@@ -612,8 +611,7 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     if (timed(K_PREPASS, s, [&] { return launch_prepass(a, tc, s); }) != cudaSuccess) return TND_ERR_CUDA;
     if (tc) {
         if (timed(K_TC, s, [&] { return launch_grad_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
-        if (a.n_uncovered > 0 &&
-            timed(K_ZERO, s, [&] { return launch_zero_dq(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+        if (timed(K_FIN, s, [&] { return launch_dq_finalize(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
     } else {
         if (timed(K_DKDV, s, [&] { return launch_grad_dkdv_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         if (timed(K_DQ, s, [&] { return launch_grad_dq_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;

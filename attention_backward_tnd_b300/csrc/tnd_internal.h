@@ -70,6 +70,15 @@ struct QBlockInfo {
     int32_t jlo, jhi;
 };
 
+// Per-row vectors of the gradient (lse2, D, sink terms) are stored blocked:
+// one 64-float vector per (global 64-row q block, query head), rows past the
+// sequence end padded (lse2 = +inf, D = 0, sink term = 0).  Index of row i of
+// sequence sd, head h:
+__host__ __device__ inline int64_t row_vec_index(const SeqDesc &sd, int32_t nq, int32_t h, int64_t i)
+{
+    return ((int64_t)(sd.qblk0 + (int32_t)(i >> 6)) * nq + h) * kQBlock + (i & (kQBlock - 1));
+}
+
 // Everything a gradient launch needs to know (device pointers into the
 // caller's buffers and the workspace).
 struct GradArgs {
@@ -92,18 +101,17 @@ struct GradArgs {
     int32_t n_q_items;
     const int2 *kv_items;     // (b, first row) per 32-row kv block
     int32_t n_kv_items;
-    float *lse2;              // [Nq][Tq]  m*log2(e) + log2(l)  (+inf if l == 0)
-    float *drow;              // [Nq][Tq]  rowsum(dY o O)
-    float *sinkrow;           // [Nq][Tq]  -p_sink * D  (sink only)
+    const int2 *qblk_rows;    // (b, first row) per global 64-row q block
+    int32_t n_qblk;
+    float *lse2;              // blocked [q block][Nq][64]: m*log2(e) + log2(l)  (+inf if l == 0)
+    float *drow;              // blocked: rowsum(dY o O)
+    float *sinkrow;           // blocked: -p_sink * D  (sink only)
     // tensor-core path
     const GradUnit *units;
     int32_t n_units;
-    const QBlockInfo *qblk;
-    int32_t n_qblk;
+    const QBlockInfo *qblk;   // [n_qblk]
     int32_t *flags;           // [n_qblk][Nq] contributions added so far
     float *dqacc;             // [Tq][Nq][D] fp32 partial sums
-    const int2 *uncovered;    // (b, first row) of q blocks no kv block reaches
-    int32_t n_uncovered;
     int64_t wait_limit_cycles;
     int32_t num_sms;
 };
@@ -135,7 +143,8 @@ cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s);
 // Tensor-core gradient (bf16/fp16, D = 128); false if this build lacks it.
 bool grad_tc_supported(int dtype, int d);
 cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s);
-// Zeroes dQ rows of q blocks that no kv block reaches (tensor-core path).
-cudaError_t launch_zero_dq(const GradArgs &a, cudaStream_t s);
+// dQ = scale * accumulated partial sums, in the output dtype; zero for q
+// blocks that no kv block reaches (tensor-core path).
+cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s);
 
 }  // namespace tnd
