@@ -17,16 +17,18 @@
 // dq_finalize_kernel writes dQ = scale * accumulator in the output dtype.
 // No atomic operation touches data, so results are bitwise deterministic.
 //
-// Warp roles (352 threads, one CTA per SM, persistent over work units taken
+// Warp roles (480 threads, one CTA per SM, persistent over work units taken
 // in plan order from a counter):
 //   warp 0      TMA producer: K (double-buffered) and V (single) per unit,
 //               Q / dY and the tile's lse2 / D vectors per tile, dropout
 //               keep-bits staged in shared memory
 //   warp 1      TMEM allocator and single-thread UMMA issuer
-//   warps 2-5   softmax-gradient warps: thread = TMEM lane = kv row
-//   warps 6-9   epilogue: dQ^T tile TMEM -> shared staging (thread = feature),
+//   warps 2-9   softmax-gradient warps: thread = TMEM lane = kv row, two
+//               warps per lane quarter, each on 32 of the tile's 64 q columns
+//   warps 10-13 epilogue: dQ^T tile TMEM -> shared staging (thread = feature),
 //               dK / dV TMEM -> global (thread = kv row) at unit end
-//   warp 10     dQ writer: orders and issues the accumulator updates
+//   warp 14     dQ writer: orders and issues the accumulator updates
+//   warp 15     counter releases of completed accumulator updates
 // Every wait is bounded; on expiry the kernel records TND_ERR_DEVICE_TIMEOUT
 // in the workspace status word and winds down instead of hanging.
 #include "ptx_sm103.cuh"
@@ -44,66 +46,82 @@ constexpr int HD = 128;                 // head dim
 constexpr int BC = kKvBlock;            // 128 kv rows per block (UMMA M)
 constexpr int BR = kQBlock;             // 64 q rows per block (UMMA N of S^T, dP^T, dQ^T)
 constexpr int NSTAGE = 2;               // Q / dY ring depth
-constexpr int kThreads = 352;
-constexpr int kEpilogueWarp0 = 6;       // warps 6-9
-constexpr int kWriterWarp = 10;
+constexpr int kThreads = 512;
+constexpr int kSoftmaxWarp0 = 2;        // warps 2-9 (two per TMEM lane quarter)
+constexpr int kEpilogueWarp0 = 10;      // warps 10-13
+constexpr int kWriterWarp = 14;
+constexpr int kReleaseWarp = 15;
+constexpr uint32_t kRelRing = 32;       // release queue entries
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns
-constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S0 = 256, TM_DP = 384, TM_DQ = 448;
+// TMEM columns.  Two 64-column S buffers hold, per tile, S^T (fp32), then
+// P^T packed in place, then the tile's dQ^T (fp32) once dV has read P^T.
+// Two 64-column dP buffers hold dP^T, then dS^T packed in place.
+constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S0 = 256, TM_DP0 = 384;
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kKvTile = BC * HD * 2;     // 32768: two 64-column blocks of 128 rows x 128 B
 constexpr uint32_t kKvColBlk = BC * 128;      // 16384
 constexpr uint32_t kQTile = BR * HD * 2;      // 16384: two 64-column blocks of 64 rows x 128 B
 constexpr uint32_t kQColBlk = BR * 128;       // 8192
-constexpr uint32_t kStgBytes = BR * HD * 4;   // 32768: dQ tile, fp32 [64 rows][128 features]
+constexpr uint32_t kStgBytes = BR * HD * 2;   // 16384: half a dQ tile, fp32 [32 rows][128 features]
+constexpr uint32_t kDsBytes = BC * 128;       // 16384: dS^T, 128 kv rows x 64 q (bf16 / fp16)
 constexpr uint32_t kVecBytes = 2 * BR * 4;    // per stage: lse2[64], D[64]
-constexpr uint32_t OFF_K = 0;                                 // 2 buffers
-constexpr uint32_t OFF_V = OFF_K + 2 * kKvTile;               // 1 buffer
+constexpr uint32_t OFF_K = 0;                                 // 1 buffer
+constexpr uint32_t OFF_V = OFF_K + kKvTile;                   // 1 buffer
 constexpr uint32_t OFF_Q = OFF_V + kKvTile;
 constexpr uint32_t OFF_DY = OFF_Q + NSTAGE * kQTile;
-constexpr uint32_t OFF_DS = OFF_DY + NSTAGE * kQTile;         // dS^T: 128 kv rows x 64 q (128 B)
-constexpr uint32_t OFF_STG = OFF_DS + BC * 128;
-constexpr uint32_t OFF_VEC = OFF_STG + kStgBytes;
+constexpr uint32_t OFF_DS = OFF_DY + NSTAGE * kQTile;         // 2 buffers (tile t: t % 2)
+constexpr uint32_t OFF_STG = OFF_DS + 2 * kDsBytes;           // 2 half-tile slots (half k: k % 2)
+constexpr uint32_t OFF_VEC = OFF_STG + 2 * kStgBytes;
 constexpr uint32_t OFF_BITS = OFF_VEC + NSTAGE * kVecBytes;   // per stage: [64 rows][4 words]
 constexpr uint32_t OFF_BAR = OFF_BITS + NSTAGE * BR * 4 * 4;
-constexpr uint32_t kNumBars = 32;
+constexpr uint32_t kNumBars = 36;   // 35 used
 constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr uint32_t kSmemUsed = OFF_MISC + 64;
+constexpr uint32_t OFF_REL = OFF_MISC + 64;                   // release queue: {int *flag; int value}
+constexpr uint32_t kSmemUsed = OFF_REL + kRelRing * 16;
 // The whole 227 KB opt-in: one CTA per SM either way, and every operand
 // descriptor's reach (tile base + strides) stays inside the allocation.
 constexpr uint32_t kSmemBytes = 232448;
 static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory budget");
 static_assert(OFF_STG % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_VEC % 16 == 0, "alignment");
 
-// mbarrier indices
+// mbarrier indices.  Every per-tile barrier whose waiter may lag by more than
+// one tile is split per buffer ([2], tile t uses t % 2): a parity wait is only
+// sound while the barrier is at most one completion past the awaited one.
 enum : int {
-    B_K_FULL = 0,      // [2]  count 1 + tx
-    B_K_EMPTY = 2,     // [2]  count 1 (commit)
-    B_V_FULL = 4,      //      count 1 + tx
-    B_V_EMPTY = 5,     //      count 1 (commit after the unit's last dP)
-    B_Q_FULL = 6,      // [2]  count 32 + tx
-    B_Q_EMPTY = 8,     // [2]  count 1 (commit)
-    B_S_FULL = 10,     // [2]  count 1 (commit)
-    B_P_READY = 12,    // [2]  count 128
-    B_S_FREE = 14,     // [2]  count 1 (commit)
-    B_DP_FULL = 16,    //      count 1 (commit)
-    B_DS_READY = 17,   //      count 128
-    B_DK_DONE = 18,    //      count 1 (commit)
-    B_DQ_FULL = 19,    //      count 1 (commit); also: dS smem of that tile consumed
-    B_DQ_FREE = 20,    //      count 128
-    B_ACC_FULL = 21,   //      count 1 (commit)
-    B_ACC_FREE = 22,   //      count 128
-    B_UNIT_FULL = 23,  // [2]  count 1
-    B_UNIT_EMPTY = 25, // [2]  count 10 (MMA + 4 softmax + 4 epilogue warps + writer)
-    B_DRAIN = 27,      //      count 1 (commit)
-    B_STG_FULL = 28,   //      count 128
-    B_STG_FREE = 29,   //      count 1
+    B_K_FULL = 0,      //      count 1 + tx
+    B_K_EMPTY = 1,     //      count 1 (commit after the unit's last dQ^T)
+    B_V_FULL = 2,      //      count 1 + tx
+    B_V_EMPTY = 3,     //      count 1 (commit after the unit's last dP)
+    B_Q_FULL = 4,      // [2]  count 32 + tx
+    B_Q_EMPTY = 6,     // [2]  count 1 (commit)
+    B_S_FULL = 8,      // [2]  count 1 (commit)
+    B_P_READY = 10,    // [2]  count 256
+    B_PV_DONE = 12,    // [2]  count 1 (commit after dV: P^T consumed, S buffer writable)
+    B_DP_FULL = 14,    // [2]  count 1 (commit)
+    B_DS_READY = 16,   // [2]  count 256 (the softmax may run a tile ahead of the MMA warp)
+    B_DK_DONE = 18,    // [2]  count 1 (commit: dS^T consumed, dP buffer writable)
+    B_DQ_FULL = 20,    // [2]  count 1 (commit); also: that tile's dS smem buffer consumed
+    B_DQ_FREE = 22,    // [2]  count 128 (dQ^T read out of its S buffer)
+    B_ACC_FULL = 24,   //      count 1 (commit)
+    B_ACC_FREE = 25,   //      count 128
+    B_UNIT_FULL = 26,  // [2]  count 1
+    B_UNIT_EMPTY = 28, // [2]  count 14 (MMA + 8 softmax + 4 epilogue warps + writer)
+    B_DRAIN = 30,      //      count 1 (commit)
+    B_STG_FULL = 31,   // [2]  count 128 (per staging slot; half tile k uses slot k % 2)
+    B_STG_FREE = 33,   // [2]  count 1
 };
 
 // misc words
-constexpr uint32_t MISC_TMEM = 0, MISC_RING = 1, MISC_ABORT = 3;
+constexpr uint32_t MISC_TMEM = 0, MISC_RING = 1, MISC_ABORT = 3, MISC_REL_TAIL = 4, MISC_REL_HEAD = 5,
+                   MISC_REL_DONE = 6;
+
+struct RelEntry {
+    int *flag;
+    int value;
+    int pad;
+};
 
 struct Smem {
     uint8_t *base;
@@ -112,22 +130,61 @@ struct Smem {
     __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(misc() + MISC_ABORT); }
 };
 
+#ifdef TND_WAIT_STATS
+// Diagnostic build only: cycles each warp role spends in each wait, summed
+// over warps (lane 0) and CTAs.  Slots 0-39: barrier waits; 40: role time;
+// 41: dQ counter spins; 42: bulk source-read waits; 43: bulk completion waits;
+// 44: proxy fence; 45: counter release batches.
+__device__ unsigned long long g_wait_stats[6][48];
+__device__ __forceinline__ int wait_role()
+{
+    const int w = threadIdx.x >> 5;
+    return w == 0 ? 0 : w == 1 ? 1 : w < 10 ? 2 : w < 14 ? 3 : w == 14 ? 4 : 5;
+}
+__device__ __forceinline__ void wait_stat(int slot, long long t0)
+{
+    if ((threadIdx.x & 31) == 0) atomicAdd(&g_wait_stats[wait_role()][slot], (unsigned long long)(clock64() - t0));
+}
+#define WAIT_STAT(slot, t0) wait_stat(slot, t0)
+// last wait entered by each warp of each CTA: (barrier, completion)
+__device__ unsigned int g_wait_last[160][16][2];
+__device__ __forceinline__ void wait_note(int bar, uint32_t k)
+{
+    if ((threadIdx.x & 31) == 0 && blockIdx.x < 160) {
+        g_wait_last[blockIdx.x][threadIdx.x >> 5][0] = (unsigned)bar;
+        g_wait_last[blockIdx.x][threadIdx.x >> 5][1] = k;
+    }
+}
+#define WAIT_NOTE(bar, k) wait_note(bar, k)
+#else
+#define WAIT_NOTE(bar, k) ((void)0)
+#define WAIT_STAT(slot, t0) ((void)0)
+#endif
+
 // Wait for completion `k` (0-based) of barrier `bar`, bounded.
 __device__ __forceinline__ bool wait_k(const Smem &sm, int bar, uint32_t k, const GradArgs &a)
 {
     uint64_t *b = sm.bar(bar);
     const uint32_t parity = k & 1u;
-    if (mbar_try_wait(b, parity)) return true;
     const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(b, parity)) return true;
-        if (*sm.abort_flag()) return false;
+    bool ok = true;
+    WAIT_NOTE(bar, k);
+    while (!mbar_try_wait(b, parity)) {
+        if (*sm.abort_flag()) {
+            ok = false;
+            break;
+        }
         if (clock64() - t0 > a.wait_limit_cycles) {
-            set_status(a.status, TND_ERR_DEVICE_TIMEOUT, 0x100u + (uint32_t)bar);
+            // detail: completion index, warp, barrier
+            set_status(a.status, TND_ERR_DEVICE_TIMEOUT,
+                       (k << 12) | ((threadIdx.x >> 5) << 6) | (uint32_t)bar);
             *sm.abort_flag() = 1;
-            return false;
+            ok = false;
+            break;
         }
     }
+    WAIT_STAT(bar, t0);
+    return ok;
 }
 
 // Warp-uniform variant: every lane polls, all lanes agree on the outcome.
@@ -204,6 +261,20 @@ __device__ __forceinline__ uint64_t keep_columns(const GradArgs &a, const SeqDes
     return (~0ull << lo) & (~0ull >> (63 - hi));
 }
 
+// Shared-memory descriptors are built once per buffer; adding (byte offset
+// >> 4) to one moves its start address (the 14-bit field never overflows:
+// every address is below 256 KB).
+__device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_off)
+{
+    return base_desc + (uint64_t)(byte_off >> 4);
+}
+
+// TMEM column of the k-th 16-row K slice of a packed 16-bit operand (Pd^T,
+// dS^T): each softmax half packs its 32 q columns into the first 16 columns
+// of its own 32-column range, so slices 0-1 sit at columns 0-15 and 2-3 at
+// columns 32-47.
+__device__ __forceinline__ uint32_t pk_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
@@ -224,30 +295,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Out = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
 
     if (threadIdx.x == 0) {
+        mbar_init(sm.bar(B_K_FULL), 1);
+        mbar_init(sm.bar(B_K_EMPTY), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(sm.bar(B_K_FULL + i), 1);
-            mbar_init(sm.bar(B_K_EMPTY + i), 1);
+            mbar_init(sm.bar(B_STG_FULL + i), 128);
+            mbar_init(sm.bar(B_STG_FREE + i), 1);
             mbar_init(sm.bar(B_Q_FULL + i), 32);
             mbar_init(sm.bar(B_Q_EMPTY + i), 1);
             mbar_init(sm.bar(B_S_FULL + i), 1);
-            mbar_init(sm.bar(B_P_READY + i), 128);
-            mbar_init(sm.bar(B_S_FREE + i), 1);
+            mbar_init(sm.bar(B_P_READY + i), 256);
+            mbar_init(sm.bar(B_PV_DONE + i), 1);
+            mbar_init(sm.bar(B_DP_FULL + i), 1);
             mbar_init(sm.bar(B_UNIT_FULL + i), 1);
-            mbar_init(sm.bar(B_UNIT_EMPTY + i), 10);
+            mbar_init(sm.bar(B_UNIT_EMPTY + i), 14);
         }
         mbar_init(sm.bar(B_V_FULL), 1);
         mbar_init(sm.bar(B_V_EMPTY), 1);
-        mbar_init(sm.bar(B_DP_FULL), 1);
-        mbar_init(sm.bar(B_DS_READY), 128);
-        mbar_init(sm.bar(B_DK_DONE), 1);
-        mbar_init(sm.bar(B_DQ_FULL), 1);
-        mbar_init(sm.bar(B_DQ_FREE), 128);
+        mbar_init(sm.bar(B_DS_READY), 256);
+        mbar_init(sm.bar(B_DS_READY + 1), 256);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(sm.bar(B_DK_DONE + i), 1);
+            mbar_init(sm.bar(B_DQ_FULL + i), 1);
+            mbar_init(sm.bar(B_DQ_FREE + i), 128);
+        }
         mbar_init(sm.bar(B_ACC_FULL), 1);
         mbar_init(sm.bar(B_ACC_FREE), 128);
         mbar_init(sm.bar(B_DRAIN), 1);
-        mbar_init(sm.bar(B_STG_FULL), 128);
-        mbar_init(sm.bar(B_STG_FREE), 1);
+
         *sm.abort_flag() = 0;
+        sm.misc()[MISC_REL_TAIL] = 0;
+        sm.misc()[MISC_REL_HEAD] = 0;
+        sm.misc()[MISC_REL_DONE] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -265,6 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm.misc() + MISC_TMEM);
+#ifdef TND_WAIT_STATS
+    const long long t_role = clock64();
+#endif
 
     if (warp == 0) {
         // ================================================================ producer
@@ -285,12 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const UnitInfo U = unit_info(a, u);
             if (U.ntiles == 0) continue;
             const int z_kv = (int)(U.sd.tk + (int64_t)U.jb * BC);
-            const uint32_t kb = ku & 1u;
-            if (ku >= 2 && !wait_warp(sm, B_K_EMPTY + kb, (ku >> 1) - 1, a)) break;
+            if (ku >= 1 && !wait_warp(sm, B_K_EMPTY, ku - 1, a)) break;
             if (lane == 0) {
-                uint64_t *fb = sm.bar(B_K_FULL + kb);
+                uint64_t *fb = sm.bar(B_K_FULL);
                 mbar_arrive_expect_tx(fb, kKvTile);
-                uint8_t *kt = sm.base + OFF_K + kb * kKvTile;
+                uint8_t *kt = sm.base + OFF_K;
                 tma_load_3d(kt, &tmK, fb, 0, U.g, z_kv);
                 tma_load_3d(kt + kKvColBlk, &tmK, fb, 64, U.g, z_kv);
             }
@@ -363,20 +443,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ku;
             if (!ok) break;
         }
-        // outstanding TMA writes must land before the CTA can leave.  K loads
-        // were issued for units [0, ku), V loads for the same units except
-        // possibly the last one if the wait before it failed: draining a phase
-        // that never started only costs the bounded wait.
+        // outstanding TMA writes must land before the CTA can leave.  K and V
+        // loads were issued for units [0, ku) (V possibly not for the last one
+        // if the wait before it failed: draining a phase that never started
+        // only costs the bounded wait).
         if (*sm.abort_flag() && lane == 0) {
             for (uint32_t s = 0; s < NSTAGE && s < gt; ++s) {
                 const uint32_t last = ((gt - 1 - s) / NSTAGE) * NSTAGE + s;  // last tile that used stage s
                 drain_k(sm, B_Q_FULL + s, last / NSTAGE, a);
             }
-            for (uint32_t kb = 0; kb < 2 && kb < ku; ++kb) {
-                const uint32_t last = ((ku - 1 - kb) / 2) * 2 + kb;
-                drain_k(sm, B_K_FULL + kb, last / 2, a);
+            if (ku >= 1) {
+                drain_k(sm, B_K_FULL, ku - 1, a);
+                drain_k(sm, B_V_FULL, ku - 1, a);
             }
-            if (ku >= 1) drain_k(sm, B_V_FULL, ku - 1, a);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -386,7 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idKV = instr_desc_f16(BF16, 128, HD, false, true);    // dV, dK (A in TMEM)
             const uint32_t idQ = instr_desc_f16(BF16, 128, BR, true, true);      // dQ^T
             const uint32_t sbase = smem_u32(sm.base);
-            const uint32_t vaddr = sbase + OFF_V;
+            // K-major views (S^T, dP^T operands) and MN-major views (dV, dK, dQ^T operands)
+            const uint64_t dK_k0 = smem_desc_sw128(sbase + OFF_K, 16, 1024);
+            const uint64_t dK_m0 = smem_desc_sw128(sbase + OFF_K, kKvColBlk, 1024);
+            const uint64_t dV_k = smem_desc_sw128(sbase + OFF_V, 16, 1024);
+            const uint64_t dQ_k0 = smem_desc_sw128(sbase + OFF_Q, 16, 1024);
+            const uint64_t dQ_m0 = smem_desc_sw128(sbase + OFF_Q, kQColBlk, 1024);
+            const uint64_t dY_k0 = smem_desc_sw128(sbase + OFF_DY, 16, 1024);
+            const uint64_t dY_m0 = smem_desc_sw128(sbase + OFF_DY, kQColBlk, 1024);
+            const uint64_t dS_m = smem_desc_sw128(sbase + OFF_DS, kQColBlk, 1024);
             uint32_t ui = 0, ku = 0, gt = 0;
             bool ok = true;
             while (ok) {
@@ -396,40 +483,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) break;
                 const UnitInfo U = unit_info(a, u);
                 if (U.ntiles == 0) continue;
-                const uint32_t kb = ku & 1u;
-                if (!wait_k(sm, B_K_FULL + kb, ku >> 1, a)) break;
+                if (!wait_k(sm, B_K_FULL, ku, a)) break;
                 tc_fence_after();
-                const uint32_t kaddr = sbase + OFF_K + kb * kKvTile;
+                const uint64_t dK_k = dK_k0, dK_m = dK_m0;
                 const uint32_t g_end = gt + (uint32_t)U.ntiles;
-                // S^T(t) = K Q(t)^T, K-major both
+                // S^T(t) = K Q(t)^T, K-major both, into S buffer t % 2 once the
+                // epilogue has read out dQ^T(t - 2) from it
                 auto issue_s = [&](uint32_t g_t) -> bool {
                     const uint32_t s = g_t % NSTAGE, b = g_t & 1u;
                     if (!wait_k(sm, B_Q_FULL + s, g_t / NSTAGE, a)) return false;
-                    if (g_t >= 2 && !wait_k(sm, B_S_FREE + b, (g_t >> 1) - 1, a)) return false;
+                    if (g_t >= 2 && !wait_k(sm, B_DQ_FREE + b, (g_t >> 1) - 1, a)) return false;
                     tc_fence_after();
-                    const uint32_t qaddr = sbase + OFF_Q + s * kQTile;
+                    const uint64_t dq = desc_at(dQ_k0, s * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t cb = kk >> 2, off = (kk & 3) * 32;
-                        mma_ss(tmem + TM_S0 + b * 64, smem_desc_sw128(kaddr + cb * kKvColBlk + off, 16, 1024),
-                               smem_desc_sw128(qaddr + cb * kQColBlk + off, 16, 1024), idS, kk > 0);
+                        const uint32_t off_k = (kk >> 2) * kKvColBlk + (kk & 3) * 32;
+                        const uint32_t off_q = (kk >> 2) * kQColBlk + (kk & 3) * 32;
+                        mma_ss(tmem + TM_S0 + b * 64, desc_at(dK_k, off_k), desc_at(dq, off_q), idS, kk > 0);
                     }
                     mma_commit(sm.bar(B_S_FULL + b));
                     return true;
                 };
-                // dP^T(t) = V dY(t)^T, once dK(t-1) has consumed dS^T(t-1) from TMEM
+                // dP^T(t) = V dY(t)^T into dP buffer t % 2 once dK(t - 2) has read
+                // dS^T(t - 2) from it
                 auto issue_dp = [&](uint32_t g_t) -> bool {
-                    const uint32_t s = g_t % NSTAGE;
-                    if (g_t >= 1 && !wait_k(sm, B_DK_DONE, g_t - 1, a)) return false;
+                    const uint32_t s = g_t % NSTAGE, b = g_t & 1u;
+                    if (g_t >= 2 && !wait_k(sm, B_DK_DONE + b, (g_t >> 1) - 1, a)) return false;
                     tc_fence_after();
-                    const uint32_t dyaddr = sbase + OFF_DY + s * kQTile;
+                    const uint64_t dy = desc_at(dY_k0, s * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t cb = kk >> 2, off = (kk & 3) * 32;
-                        mma_ss(tmem + TM_DP, smem_desc_sw128(vaddr + cb * kKvColBlk + off, 16, 1024),
-                               smem_desc_sw128(dyaddr + cb * kQColBlk + off, 16, 1024), idS, kk > 0);
+                        const uint32_t off_v = (kk >> 2) * kKvColBlk + (kk & 3) * 32;
+                        const uint32_t off_y = (kk >> 2) * kQColBlk + (kk & 3) * 32;
+                        mma_ss(tmem + TM_DP0 + b * 64, desc_at(dV_k, off_v), desc_at(dy, off_y), idS, kk > 0);
                     }
-                    mma_commit(sm.bar(B_DP_FULL));
+                    mma_commit(sm.bar(B_DP_FULL + b));
                     if (g_t + 1 == g_end) mma_commit(sm.bar(B_V_EMPTY));   // last reader of V
                     return true;
                 };
@@ -438,7 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!issue_dp(gt)) break;
                 for (int t = 0; t < U.ntiles; ++t) {
                     const uint32_t g_t = gt + t, s = g_t % NSTAGE, b = g_t & 1u;
-                    if (t + 1 < U.ntiles && !issue_s(g_t + 1)) {
+                    // the next tile's S^T and dP^T go ahead of this tile's gradients
+                    if (t + 1 < U.ntiles && (!issue_s(g_t + 1) || !issue_dp(g_t + 1))) {
                         ok = false;
                         break;
                     }
@@ -446,54 +535,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    // dV += Pd^T dY(t): A = Pd^T (TMEM, 32 packed columns), B = dY MN-major (N = 128)
+                    // dV += Pd^T dY(t): A = Pd^T (TMEM, packed), B = dY MN-major (N = 128)
                     if (!wait_k(sm, B_P_READY + b, g_t >> 1, a)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qaddr = sbase + OFF_Q + s * kQTile, dyaddr = sbase + OFF_DY + s * kQTile;
+                    const uint64_t dqm = desc_at(dQ_m0, s * kQTile), dym = desc_at(dY_m0, s * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
-                        mma_ts(tmem + TM_DV, tmem + TM_S0 + b * 64 + kk * 8,
-                               smem_desc_sw128(dyaddr + kk * 2048, kQColBlk, 1024), idKV, (t > 0 || kk > 0));
+                        mma_ts(tmem + TM_DV, tmem + TM_S0 + b * 64 + pk_col(kk), desc_at(dym, kk * 2048), idKV,
+                               (t > 0 || kk > 0));
                     }
-                    mma_commit(sm.bar(B_S_FREE + b));
-                    // dK += dS^T Q(t): A = dS^T (TMEM), B = Q MN-major
-                    if (!wait_k(sm, B_DS_READY, g_t, a)) {
+                    mma_commit(sm.bar(B_PV_DONE + b));
+                    // dK += dS^T Q(t): A = dS^T (TMEM, packed), B = Q MN-major
+                    if (!wait_k(sm, B_DS_READY + b, g_t >> 1, a)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
-                        mma_ts(tmem + TM_DK, tmem + TM_DP + kk * 8,
-                               smem_desc_sw128(qaddr + kk * 2048, kQColBlk, 1024), idKV, (t > 0 || kk > 0));
+                        mma_ts(tmem + TM_DK, tmem + TM_DP0 + b * 64 + pk_col(kk), desc_at(dqm, kk * 2048), idKV,
+                               (t > 0 || kk > 0));
                     }
                     mma_commit(sm.bar(B_Q_EMPTY + s));
-                    mma_commit(sm.bar(B_DK_DONE));
-                    // dP^T of the next tile ahead of this tile's dQ^T: the softmax
-                    // warps get it one GEMM earlier
-                    if (t + 1 < U.ntiles && !issue_dp(g_t + 1)) {
-                        ok = false;
-                        break;
-                    }
-                    // dQ^T(t) = K^T dS^T: A = K MN-major (M = 128 features), B = dS^T MN-major (N = 64)
-                    if (g_t >= 1 && !wait_k(sm, B_DQ_FREE, g_t - 1, a)) {
+                    mma_commit(sm.bar(B_DK_DONE + b));
+                    // dQ^T(t) = K^T dS^T into S buffer t % 2 once dV(t) has read P^T:
+                    // A = K MN-major (M = 128 features), B = dS^T MN-major (N = 64)
+                    if (!wait_k(sm, B_PV_DONE + b, g_t >> 1, a)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
-                        mma_ss(tmem + TM_DQ, smem_desc_sw128(kaddr + kk * 2048, kKvColBlk, 1024),
-                               smem_desc_sw128(sbase + OFF_DS + kk * 2048, kQColBlk, 1024), idQ, kk > 0);
+                        mma_ss(tmem + TM_S0 + b * 64, desc_at(dK_m, kk * 2048), desc_at(dS_m, b * kDsBytes + kk * 2048),
+                               idQ, kk > 0);
                     }
-                    mma_commit(sm.bar(B_DQ_FULL));
+                    mma_commit(sm.bar(B_DQ_FULL + b));
                 }
                 if (!ok) break;
                 mma_commit(sm.bar(B_ACC_FULL));
-                mma_commit(sm.bar(B_K_EMPTY + kb));
+                mma_commit(sm.bar(B_K_EMPTY));
                 gt += U.ntiles;
                 ++ku;
             }
@@ -506,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kEpilogueWarp0) {
         // ================================================================ softmax gradient
+        // Two warps per TMEM lane quarter: warps 2-5 take q columns 0-31 of the
+        // tile, warps 6-9 columns 32-63.
         const int quarter = warp & 3;
+        const int half = (warp - kSoftmaxWarp0) >> 2;
         const int jl = quarter * 32 + lane;                 // kv row within the block = TMEM lane
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const float C = a.scale * kLog2e;
@@ -523,91 +610,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t s = gt % NSTAGE, b = gt & 1u;
                 const int64_t q0 = (int64_t)qb * BR;
                 const int64_t jj = (int64_t)U.jb * BC + jl;
-                const uint64_t keep = keep_columns(a, U.sd, q0, jj);
-                const bool full = __all_sync(0xffffffffu, keep == ~0ull);
+                const uint32_t keep = (uint32_t)(keep_columns(a, U.sd, q0, jj) >> (32 * half));
+                const bool full = __all_sync(0xffffffffu, keep == 0xffffffffu);
                 if (!wait_warp(sm, B_Q_FULL + s, gt / NSTAGE, a) || !wait_warp(sm, B_S_FULL + b, gt >> 1, a)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float *lse = reinterpret_cast<const float *>(sm.base + OFF_VEC + s * kVecBytes);
-                const float *dvec = lse + BR;
-                uint64_t zbits = ~0ull;
+                const float4 *lse4 = reinterpret_cast<const float4 *>(sm.base + OFF_VEC + s * kVecBytes) + 8 * half;
+                const float4 *dvec4 = lse4 + BR / 4;
+                uint32_t zbits = 0xffffffffu;
                 if (a.has_drop) {
                     const uint32_t *bits = reinterpret_cast<const uint32_t *>(sm.base + OFF_BITS + s * BR * 16);
                     zbits = 0;
 #pragma unroll 8
-                    for (int c = 0; c < BR; ++c) zbits |= (uint64_t)((bits[c * 4 + quarter] >> lane) & 1u) << c;
+                    for (int c = 0; c < 32; ++c) zbits |= ((bits[(32 * half + c) * 4 + quarter] >> lane) & 1u) << c;
                 }
-                // ---- phase 1: P^T from S^T, Pd^T = P^T o z into TMEM
-                float p[BR];
+                // ---- phase 1: P^T from S^T, Pd^T = P^T o z into TMEM (16 packed columns)
+                float p[32];
                 uint32_t raw[32];
                 const uint32_t s_addr = tmem + lane_addr + TM_S0 + b * 64;
+                tmem_ld32(s_addr + 32 * half, raw);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(s_addr + half * 32, raw);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        p[half * 32 + c] = ex2(fmaf(__uint_as_float(raw[c]), C, -lse[half * 32 + c]));
-                    }
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 l = lse4[c4];
+                    p[4 * c4 + 0] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 0]), C, -l.x));
+                    p[4 * c4 + 1] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 1]), C, -l.y));
+                    p[4 * c4 + 2] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 2]), C, -l.z));
+                    p[4 * c4 + 3] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 3]), C, -l.w));
                 }
                 if (!full) {
 #pragma unroll
-                    for (int c = 0; c < BR; ++c) p[c] = ((keep >> c) & 1ull) ? p[c] : 0.0f;
+                    for (int c = 0; c < 32; ++c) p[c] = ((keep >> c) & 1u) ? p[c] : 0.0f;
                 }
-                uint32_t pk[32];
+                uint32_t pk[16];
                 if (a.has_drop) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float z0 = ((zbits >> (2 * c)) & 1ull) ? a.inv_keep : 0.0f;
-                        const float z1 = ((zbits >> (2 * c + 1)) & 1ull) ? a.inv_keep : 0.0f;
+                    for (int c = 0; c < 16; ++c) {
+                        const float z0 = ((zbits >> (2 * c)) & 1u) ? a.inv_keep : 0.0f;
+                        const float z1 = ((zbits >> (2 * c + 1)) & 1u) ? a.inv_keep : 0.0f;
                         pk[c] = pack2<BF16>(p[2 * c] * z0, p[2 * c + 1] * z1);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) pk[c] = pack2<BF16>(p[2 * c], p[2 * c + 1]);
+                    for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(p[2 * c], p[2 * c + 1]);
                 }
-                tmem_st32(s_addr, pk);
+                tmem_st16(s_addr + 32 * half, pk);      // packed into this half's own columns
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_P_READY + b));
                 // ---- phase 2: dS^T = P^T o (z dP^T - D) into TMEM and shared memory
-                if (!wait_warp(sm, B_DP_FULL, gt, a)) {
+                if (!wait_warp(sm, B_DP_FULL + b, gt >> 1, a)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dp_addr = tmem + lane_addr + TM_DP;
+                const uint32_t dp_addr = tmem + lane_addr + TM_DP0 + b * 64;
+                tmem_ld32(dp_addr + 32 * half, raw);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(dp_addr + half * 32, raw);
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 dv = dvec4[c4];
+                    float dp[4] = {__uint_as_float(raw[4 * c4]), __uint_as_float(raw[4 * c4 + 1]),
+                                   __uint_as_float(raw[4 * c4 + 2]), __uint_as_float(raw[4 * c4 + 3])};
+                    if (a.has_drop) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const int c0 = half * 32 + c;
-                        float dp0 = __uint_as_float(raw[c]), dp1 = __uint_as_float(raw[c + 1]);
-                        if (a.has_drop) {
-                            dp0 = ((zbits >> c0) & 1ull) ? dp0 * a.inv_keep : 0.0f;
-                            dp1 = ((zbits >> (c0 + 1)) & 1ull) ? dp1 * a.inv_keep : 0.0f;
-                        }
-                        pk[(half * 32 + c) >> 1] = pack2<BF16>(p[c0] * (dp0 - dvec[c0]), p[c0 + 1] * (dp1 - dvec[c0 + 1]));
+                        for (int e = 0; e < 4; ++e) dp[e] = ((zbits >> (4 * c4 + e)) & 1u) ? dp[e] * a.inv_keep : 0.0f;
                     }
+                    pk[2 * c4] = pack2<BF16>(p[4 * c4] * (dp[0] - dv.x), p[4 * c4 + 1] * (dp[1] - dv.y));
+                    pk[2 * c4 + 1] = pack2<BF16>(p[4 * c4 + 2] * (dp[2] - dv.z), p[4 * c4 + 3] * (dp[3] - dv.w));
                 }
-                tmem_st32(dp_addr, pk);
-                // the previous tile's dQ^T GEMM must have read the dS^T buffer
-                if (gt >= 1 && !wait_warp(sm, B_DQ_FULL, gt - 1, a)) {
+                tmem_st16(dp_addr + 32 * half, pk);
+                // dS^T buffer t % 2: the dQ^T GEMM of tile t - 2 must have read it
+                if (gt >= 2 && !wait_warp(sm, B_DQ_FULL + b, (gt >> 1) - 1, a)) {
                     ok = false;
                     break;
                 }
                 {
-                    uint8_t *row = sm.base + OFF_DS + jl * 128;
+                    uint8_t *row = sm.base + OFF_DS + b * kDsBytes + jl * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = 4 * half + c;
                         uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        *reinterpret_cast<uint4 *>(row + ((c ^ (jl & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4 *>(row + ((chunk ^ (jl & 7)) << 4)) = v;
                     }
                 }
                 fence_async_smem();
                 tc_fence_before();
-                mbar_arrive(sm.bar(B_DS_READY));
+                mbar_arrive(sm.bar(B_DS_READY + b));
             }
             if (!ok) break;
         }
@@ -640,26 +728,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool ok = true;
             for (int t = 0; t < U.ntiles; ++t, ++gt) {
-                if (!wait_warp(sm, B_DQ_FULL, gt, a)) {
+                if (!wait_warp(sm, B_DQ_FULL + (gt & 1u), gt >> 1, a)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 uint32_t v[BR];
-                tmem_ld32(tmem + lane_addr + TM_DQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(tmem + lane_addr + TM_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                const uint32_t dq_addr = tmem + lane_addr + TM_S0 + (gt & 1u) * 64;
+                tmem_ld32(dq_addr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(dq_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                 tc_fence_before();
-                mbar_arrive(sm.bar(B_DQ_FREE));
-                // staging [64 q rows][128 features] fp32, free once the writer's
-                // previous bulk operation has read it
-                if (gt >= 1 && !wait_warp(sm, B_STG_FREE, gt - 1, a)) {
-                    ok = false;
-                    break;
-                }
+                mbar_arrive(sm.bar(B_DQ_FREE + (gt & 1u)));
+                // staging: a ring of two [32 q rows][128 features] fp32 slots;
+                // half tile k (q rows 32 (k % 2) .. +31 of tile k / 2) goes to slot
+                // k % 2 once the writer's bulk operation has read half k - 2
 #pragma unroll
-                for (int c = 0; c < BR; ++c) stg[c * HD] = __uint_as_float(v[c]);
-                fence_async_smem();
-                mbar_arrive(sm.bar(B_STG_FULL));
+                for (int hs = 0; hs < 2; ++hs) {
+                    const uint32_t k = 2 * gt + hs;
+                    if (k >= 2 && !wait_warp(sm, B_STG_FREE + hs, (k >> 1) - 1, a)) {
+                        ok = false;
+                        break;
+                    }
+                    float *slot = stg + hs * (kStgBytes / 4);
+#pragma unroll
+                    for (int c = 0; c < BR / 2; ++c) slot[c * HD] = __uint_as_float(v[hs * (BR / 2) + c]);
+                    fence_async_smem();
+                    mbar_arrive(sm.bar(B_STG_FULL + hs));
+                }
+                if (!ok) break;
             }
             if (!ok) break;
             // unit epilogue: dV, dK (x scale) out of TMEM
@@ -691,26 +787,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(sm.bar(B_ACC_FREE));
             ++ku;
         }
-    } else {
+    } else if (warp == kWriterWarp) {
         // ================================================================ dQ writer
         // Adds each staged dQ^T tile into the fp32 accumulator of its (q block,
         // head): the first contributor stores, later ones add, each after the
         // previous contributor's counter says its update has completed.  A
-        // counter is released one tile late (when the next bulk group is in
-        // flight), but never held while this thread waits on another counter.
+        // tile goes out as two bulk groups (q rows 0-31, 32-63) so that the
+        // epilogue refills one staging half while the other is read.  Once a
+        // tile's groups have completed (checked while handling the next tile)
+        // its counter update goes to the release warp's queue, so this thread
+        // never runs a GPU-scope fence and never holds an unreleased counter
+        // while it waits on another one.
         if (lane == 0) {
-            uint32_t ui = 0, gt = 0;
+            uint32_t ui = 0, gt = 0, rel_tail = 0;
             int *pend_flag = nullptr;
             int pend_val = 0;
-            auto release_pending = [&](bool all) {
-                if (!pend_flag) return;
-                if (all) bulk_wait0();
-                else bulk_wait1();
-                fence_async_global();
-                st_release_gpu(pend_flag, pend_val);
-                pend_flag = nullptr;
-            };
+            const uint8_t *stg = sm.base + OFF_STG;
+            RelEntry *ring = reinterpret_cast<RelEntry *>(sm.base + OFF_REL);
+            const uint32_t *rel_head = sm.misc() + MISC_REL_HEAD;
             bool ok = true;
+            // the previous tile's groups have completed: counter queued
+            auto finish_prev = [&]() -> bool {
+                if (!pend_flag) return true;
+                const long long tw = clock64();
+                (void)tw;
+                bulk_wait0();
+                fence_async_global();
+                WAIT_STAT(43, tw);
+                const long long t0 = clock64();
+                while (rel_tail - ld_acquire_cta_shared(rel_head) >= kRelRing) {
+                    if (*sm.abort_flag() || clock64() - t0 > a.wait_limit_cycles) return false;
+                }
+                RelEntry &e = ring[rel_tail % kRelRing];
+                e.flag = pend_flag;
+                e.value = pend_val;
+                st_release_cta_shared(sm.misc() + MISC_REL_TAIL, ++rel_tail);
+                pend_flag = nullptr;
+                return true;
+            };
             while (ok) {
                 int u;
                 if (!read_unit1(sm, ui, a, u)) break;
@@ -720,63 +834,128 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < U.ntiles; ++t, ++gt) {
                     const int qb = U.qb_lo + t / G, h = U.g * G + t % G;
                     const int qg = U.sd.qblk0 + qb;
+                    // contributor range and the counter, both loaded while the
+                    // epilogue is still staging the tile
                     const QBlockInfo qi = a.qblk[qg];
                     int *flag = a.flags + (int64_t)qg * a.nq + h;
+                    const int seen = ld_acquire_gpu(flag);
                     const int64_t q0 = (int64_t)qb * BR;
                     const int rows = (int)min((int64_t)BR, (int64_t)U.sd.sq - q0);
-                    const int pos = qi.jhi - U.jb;
-                    if (!wait_k(sm, B_STG_FULL, gt, a)) {
+                    if (!wait_k(sm, B_STG_FULL, gt, a) || !finish_prev()) {
                         ok = false;
                         break;
                     }
-                    if (pos > 0) {
-                        if (ld_acquire_gpu(flag) < pos) {
-                            release_pending(true);
-                            const long long t0 = clock64();
-                            while (ld_acquire_gpu(flag) < pos) {
-                                if (*sm.abort_flag()) {
-                                    ok = false;
-                                    break;
-                                }
-                                if (clock64() - t0 > a.wait_limit_cycles) {
-                                    set_status(a.status, TND_ERR_DEVICE_TIMEOUT, 0x200u);
-                                    *sm.abort_flag() = 1;
-                                    ok = false;
-                                    break;
-                                }
-                                __nanosleep(32);
+                    const int pos = qi.jhi - U.jb;
+                    if (pos > 0 && seen < pos) {
+                        const long long tf = clock64();
+                        (void)tf;
+                        const long long t0 = clock64();
+                        WAIT_NOTE(60, (uint32_t)(qg * a.nq + h) | ((uint32_t)pos << 24));
+                        while (ld_acquire_gpu(flag) < pos) {
+                            if (*sm.abort_flag()) {
+                                ok = false;
+                                break;
                             }
-                            if (!ok) break;
+                            if (clock64() - t0 > a.wait_limit_cycles) {
+                                // detail: the awaited position and the (q block, head) counter
+                                set_status(a.status, TND_ERR_DEVICE_TIMEOUT,
+                                           0x80000000u | ((uint32_t)pos << 24) | (uint32_t)(qg * a.nq + h));
+                                *sm.abort_flag() = 1;
+                                ok = false;
+                                break;
+                            }
+                            __nanosleep(32);
                         }
-                        fence_async_global();
+                        if (!ok) break;
+                        WAIT_STAT(41, tf);
                     }
-                    const uint8_t *stg = sm.base + OFF_STG;
+                    if (pos > 0) fence_async_global();    // counter acquire before the bulk reduction
                     const int z = (int)(U.sd.tq + q0);
-                    if (rows == BR) {
-                        if (pos == 0) tma_store_3d(&tmDQ, stg, 0, h, z);
-                        else tma_reduce_add_3d(&tmDQ, stg, 0, h, z);
-                    } else {
-                        // ragged last block of a sequence: only its own rows
-                        for (int r = 0; r < rows; ++r) {
-                            float *dst = a.dqacc + ((int64_t)(z + r) * a.nq + h) * HD;
-                            if (pos == 0) bulk_s2g(dst, stg + r * HD * 4, HD * 4);
-                            else bulk_reduce_add_f32(dst, stg + r * HD * 4, HD * 4);
+#pragma unroll 1
+                    for (int hs = 0; hs < 2; ++hs) {
+                        if (hs == 1 && !wait_k(sm, B_STG_FULL + 1, gt, a)) {
+                            ok = false;
+                            break;
                         }
+                        const uint8_t *slot = stg + hs * kStgBytes;
+                        const int r0 = hs * (BR / 2);
+                        if (rows == BR) {
+                            if (pos == 0) tma_store_3d(&tmDQ, slot, 0, h, z + r0);
+                            else tma_reduce_add_3d(&tmDQ, slot, 0, h, z + r0);
+                        } else {
+                            // ragged last block of a sequence: only its own rows
+                            for (int r = r0; r < min(rows, r0 + BR / 2); ++r) {
+                                float *dst = a.dqacc + ((int64_t)(z + r) * a.nq + h) * HD;
+                                if (pos == 0) bulk_s2g(dst, slot + (r - r0) * HD * 4, HD * 4);
+                                else bulk_reduce_add_f32(dst, slot + (r - r0) * HD * 4, HD * 4);
+                            }
+                        }
+                        bulk_commit();
+                        // slot 0 is freed once half 1 is in flight, slot 1 at the end of
+                        // the tile, so no slot waits for the next tile's counter
+                        const long long tr = clock64();
+                        (void)tr;
+                        if (hs == 1) {
+                            bulk_wait_read1();
+                            mbar_arrive(sm.bar(B_STG_FREE));
+                            bulk_wait_read0();
+                            mbar_arrive(sm.bar(B_STG_FREE + 1));
+                        }
+                        WAIT_STAT(42, tr);
                     }
-                    bulk_commit();
-                    bulk_wait_read0();
-                    mbar_arrive(sm.bar(B_STG_FREE));
-                    release_pending(false);
+                    if (!ok) break;
                     pend_flag = flag;
                     pend_val = pos + 1;
                 }
             }
-            release_pending(true);
+            if (ok) finish_prev();
             bulk_wait0();
+            st_release_cta_shared(sm.misc() + MISC_REL_DONE, 1u);
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ counter releases
+        // Publishes queued counter values with one GPU-scope fence per batch:
+        // the queue entry was pushed (CTA-scope release) after its bulk group
+        // completed, so fence + relaxed store is a release of those writes.
+        if (lane == 0) {
+            uint32_t head = 0;
+            const RelEntry *ring = reinterpret_cast<const RelEntry *>(sm.base + OFF_REL);
+            long long idle0 = clock64();
+            while (true) {
+                const uint32_t tail = ld_acquire_cta_shared(sm.misc() + MISC_REL_TAIL);
+                if (tail != head) {
+                    const long long tr = clock64();
+                    (void)tr;
+                    fence_acq_rel_gpu();
+                    for (; head != tail; ++head) {
+                        const RelEntry &e = ring[head % kRelRing];
+                        st_relaxed_gpu(e.flag, e.value);
+                    }
+                    st_release_cta_shared(sm.misc() + MISC_REL_HEAD, head);   // entries read before reuse
+                    WAIT_STAT(45, tr);
+                    idle0 = clock64();
+                    continue;
+                }
+                if (ld_acquire_cta_shared(sm.misc() + MISC_REL_DONE)) {
+                    if (ld_acquire_cta_shared(sm.misc() + MISC_REL_TAIL) == head) break;
+                    continue;
+                }
+                if (*sm.abort_flag()) break;
+                if (clock64() - idle0 > 4 * a.wait_limit_cycles) {
+                    set_status(a.status, TND_ERR_DEVICE_TIMEOUT, 0x300u);
+                    *sm.abort_flag() = 1;
+                    break;
+                }
+                __nanosleep(256);
+            }
         }
         __syncwarp();
     }
 
+#ifdef TND_WAIT_STATS
+    WAIT_STAT(40, t_role);
+#endif
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -848,14 +1027,14 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t heads, int 
     return r == CUDA_SUCCESS;
 }
 
-// dQ accumulator [rows, heads, 128] fp32, boxes of 128 features x 1 head x 64 rows (no swizzle)
-bool make_acc_map(CUtensorMap *m, const float *ptr, int64_t rows, int64_t heads)
+// dQ accumulator [rows, heads, 128] fp32, boxes of 128 features x 1 head x `box_rows` rows (no swizzle)
+bool make_acc_map(CUtensorMap *m, const float *ptr, int64_t rows, int64_t heads, int box_rows)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)heads, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)HD * 4, (cuuint64_t)(heads * HD * 4)};
-    cuuint32_t box[3] = {HD, 1, BR};
+    cuuint32_t box[3] = {HD, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -874,7 +1053,7 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
     CUtensorMap mq, mk, mv, mdy, mdq;
     if (!make_map(&mq, a.q, a.tq, a.nq, BR, bf16) || !make_map(&mk, a.k, a.tkv, a.nkv, BC, bf16) ||
         !make_map(&mv, a.v, a.tkv, a.nkv, BC, bf16) || !make_map(&mdy, a.dy, a.tq, a.nq, BR, bf16) ||
-        !make_acc_map(&mdq, a.dqacc, a.tq, a.nq))
+        !make_acc_map(&mdq, a.dqacc, a.tq, a.nq, BR / 2))
         return cudaErrorInvalidValue;
     const int grid = std::min<int>(a.num_sms, a.n_units);
     cudaError_t e;
@@ -889,6 +1068,24 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
     }
     return cudaGetLastError();
 }
+
+#ifdef TND_WAIT_STATS
+}  // namespace tnd
+extern "C" int tnd_debug_wait_last(unsigned int *out)
+{
+    return cudaMemcpyFromSymbol(out, tnd::g_wait_last, sizeof(tnd::g_wait_last)) != cudaSuccess;
+}
+extern "C" int tnd_debug_wait_stats(unsigned long long *out, int reset)
+{
+    if (cudaMemcpyFromSymbol(out, tnd::g_wait_stats, sizeof(tnd::g_wait_stats)) != cudaSuccess) return 1;
+    if (reset) {
+        static unsigned long long zero[6][48] = {};
+        if (cudaMemcpyToSymbol(tnd::g_wait_stats, zero, sizeof(zero)) != cudaSuccess) return 1;
+    }
+    return 0;
+}
+namespace tnd {
+#endif
 
 cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s)
 {

@@ -6,6 +6,7 @@
 #include "tnd_internal.h"
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <memory>
@@ -372,6 +373,36 @@ std::shared_ptr<const Plan> get_plan(const Problem &p, bool with_units)
     return pl;
 }
 
+// Clock rate and SM count of the current device, queried once per device
+// (the clock-rate query costs hundreds of microseconds on some drivers).
+struct DeviceInfo {
+    int clock_khz = 0, num_sms = 0;
+};
+DeviceInfo device_info()
+{
+    constexpr int kMaxDev = 64;
+    static DeviceInfo cache[kMaxDev];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = -1;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        if (cache[dev].num_sms > 0) return cache[dev];
+    }
+    DeviceInfo di;
+    if (dev >= 0) {
+        cudaDeviceGetAttribute(&di.clock_khz, cudaDevAttrClockRate, dev);
+        cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    if (di.clock_khz <= 0) di.clock_khz = 2000000;
+    if (di.num_sms <= 0) di.num_sms = 148;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        cache[dev] = di;
+    }
+    return di;
+}
+
 bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
 
 // Copies the plan into the workspace and clears the status words (and the
@@ -412,10 +443,38 @@ void fill_common(A &a, const Problem &p, const Plan &pl, const Layout &L, void *
     a.n_q_items = (int32_t)pl.q_items.size();
 }
 
+#ifdef TND_HOST_STATS
+// Diagnostic build only: host microseconds per phase of tnd_attn_grad.
+double g_host_us[8];
+struct HostClock {
+    std::chrono::steady_clock::time_point t = std::chrono::steady_clock::now();
+    void lap(int i)
+    {
+        const auto n = std::chrono::steady_clock::now();
+        g_host_us[i] += std::chrono::duration<double, std::micro>(n - t).count();
+        t = n;
+    }
+};
+#define HOST_LAP(i) hc.lap(i)
+#else
+struct HostClock {};
+#define HOST_LAP(i) ((void)0)
+#endif
+
 }  // namespace
 }  // namespace tnd
 
 using namespace tnd;
+
+#ifdef TND_HOST_STATS
+extern "C" void tnd_debug_host_stats(double *out, int reset)
+{
+    for (int i = 0; i < 8; ++i) {
+        out[i] = g_host_us[i];
+        if (reset) g_host_us[i] = 0.0;
+    }
+}
+#endif
 
 extern "C" {
 
@@ -554,6 +613,8 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
 {
     if (!q || !k || !v || !dy || !smax || !ssum || !o || !dq || !dk || !dv) return TND_ERR_NULLPTR;
     if (sink && !dsink) return TND_ERR_NULLPTR;
+    HostClock hc;
+    (void)hc;
     Problem p;
     tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode,
                              drop_mask != nullptr, sink != nullptr, p);
@@ -561,6 +622,7 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     for (const void *ptr : {q, k, v, dy, (const void *)smax, (const void *)ssum, o, (const void *)dq,
                             (const void *)dk, (const void *)dv})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
+    HOST_LAP(0);
     const bool tc_layout = grad_tc_supported(p.dtype, (int)p.d);
     const bool tc = use_tc(p);
     auto plp = get_plan(p, tc_layout);
@@ -568,8 +630,10 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     const Layout L = layout_for(p, pl, true, tc_layout);
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
+    HOST_LAP(1);
     st = upload_plan(pl, L, ws, tc, p, s);
     if (st != TND_OK) return st;
+    HOST_LAP(2);
     GradArgs a{};
     fill_common(a, p, pl, L, ws);
     char *w = (char *)ws;
@@ -600,18 +664,18 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     a.dqacc = tc_layout ? (float *)(w + L.dqacc) : nullptr;
     a.mask_bytes = (mask_bits_total(p) + 7) / 8;
     {
-        int dev = 0, khz = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (khz <= 0) khz = 2000000;
-        a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)khz;
-        a.num_sms = sms > 0 ? sms : 148;
+        const DeviceInfo di = device_info();
+        a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)di.clock_khz;
+        a.num_sms = di.num_sms;
     }
+    HOST_LAP(3);
     if (timed(K_PREPASS, s, [&] { return launch_prepass(a, tc, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    HOST_LAP(4);
     if (tc) {
         if (timed(K_TC, s, [&] { return launch_grad_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+        HOST_LAP(5);
         if (timed(K_FIN, s, [&] { return launch_dq_finalize(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+        HOST_LAP(6);
     } else {
         if (timed(K_DKDV, s, [&] { return launch_grad_dkdv_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         if (timed(K_DQ, s, [&] { return launch_grad_dq_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
