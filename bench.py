@@ -113,31 +113,37 @@ class ClockSampler:
         self._handle = None
 
     def _open(self):
-        import pynvml
+        """NVML through the driver's own library (ctypes), which every GPU machine has."""
+        import ctypes
         import torch
-        pynvml.nvmlInit()
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
         props = torch.cuda.get_device_properties(self.dev)
-        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
-        try:
-            self._handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-        except pynvml.NVMLError:
-            self._handle = pynvml.nvmlDeviceGetHandleByIndex(0)
-        self._nvml = pynvml
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(0), ctypes.byref(h)) != 0:
+                raise RuntimeError("no NVML device handle")
+        self._nv, self._handle = nv, h
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reason_fn = fn if fn is not None else nv.nvmlDeviceGetCurrentClocksThrottleReasons
 
-    def _reasons(self):
-        n = self._nvml
-        fn = getattr(n, "nvmlDeviceGetCurrentClocksEventReasons", None) or n.nvmlDeviceGetCurrentClocksThrottleReasons
-        return int(fn(self._handle))
+    def _sample(self):
+        import ctypes
+        sm, mx, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        nv, h = self._nv, self._handle
+        if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) != 0:      # NVML_CLOCK_SM = 1
+            return None
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        self._reason_fn(h, ctypes.byref(rs))
+        return float(sm.value), float(mx.value), int(rs.value)
 
     def _run(self):
-        n = self._nvml
         while not self._stop:
-            try:
-                sm = n.nvmlDeviceGetClockInfo(self._handle, n.NVML_CLOCK_SM)
-                mx = n.nvmlDeviceGetMaxClockInfo(self._handle, n.NVML_CLOCK_SM)
-                self.samples.append((time.perf_counter(), float(sm), float(mx), self._reasons()))
-            except Exception:  # pragma: no cover - transient NVML errors
-                pass
+            x = self._sample()
+            if x is not None:
+                self.samples.append((time.perf_counter(),) + x)
             time.sleep(0.01)
 
     def __enter__(self):
