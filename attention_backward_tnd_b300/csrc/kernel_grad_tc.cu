@@ -45,7 +45,7 @@ using namespace ptx;
 constexpr int HD = 128;                 // head dim
 constexpr int BC = kKvBlock;            // 128 kv rows per block (UMMA M)
 constexpr int BR = kQBlock;             // 64 q rows per block (UMMA N of S^T, dP^T, dQ^T)
-constexpr int NSTAGE = 2;               // Q / dY ring depth
+constexpr int NSTAGE = 3;               // Q / dY ring depth
 constexpr int kThreads = 512;
 constexpr int kSoftmaxWarp0 = 2;        // warps 2-9 (two per TMEM lane quarter)
 constexpr int kEpilogueWarp0 = 10;      // warps 10-13
@@ -71,19 +71,19 @@ constexpr uint32_t OFF_K = 0;                                 // 1 buffer
 constexpr uint32_t OFF_V = OFF_K + kKvTile;                   // 1 buffer
 constexpr uint32_t OFF_Q = OFF_V + kKvTile;
 constexpr uint32_t OFF_DY = OFF_Q + NSTAGE * kQTile;
-constexpr uint32_t OFF_DS = OFF_DY + NSTAGE * kQTile;         // 2 buffers (tile t: t % 2)
-constexpr uint32_t OFF_STG = OFF_DS + 2 * kDsBytes;           // 2 half-tile slots (half k: k % 2)
+constexpr uint32_t OFF_DS = OFF_DY + NSTAGE * kQTile;         // 1 buffer
+constexpr uint32_t OFF_STG = OFF_DS + kDsBytes;               // 2 half-tile slots (half k: k % 2)
 constexpr uint32_t OFF_VEC = OFF_STG + 2 * kStgBytes;
 constexpr uint32_t OFF_BITS = OFF_VEC + NSTAGE * kVecBytes;   // per stage: [64 rows][4 words]
 constexpr uint32_t OFF_BAR = OFF_BITS + NSTAGE * BR * 4 * 4;
-constexpr uint32_t kNumBars = 36;   // 35 used
+constexpr uint32_t kNumBars = 38;   // 37 used
 constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr uint32_t OFF_REL = OFF_MISC + 64;                   // release queue: {int *flag; int value}
 constexpr uint32_t kSmemUsed = OFF_REL + kRelRing * 16;
 // The whole 227 KB opt-in: one CTA per SM either way, and every operand
 // descriptor's reach (tile base + strides) stays inside the allocation.
 constexpr uint32_t kSmemBytes = 232448;
-static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory budget");
+static_assert(kSmemUsed + 1024 + 64 <= kSmemBytes, "shared memory budget (64 B: diagnostic counters)");
 static_assert(OFF_STG % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_VEC % 16 == 0, "alignment");
 
 // mbarrier indices.  Every per-tile barrier whose waiter may lag by more than
@@ -94,23 +94,23 @@ enum : int {
     B_K_EMPTY = 1,     //      count 1 (commit after the unit's last dQ^T)
     B_V_FULL = 2,      //      count 1 + tx
     B_V_EMPTY = 3,     //      count 1 (commit after the unit's last dP)
-    B_Q_FULL = 4,      // [2]  count 32 + tx
-    B_Q_EMPTY = 6,     // [2]  count 1 (commit)
-    B_S_FULL = 8,      // [2]  count 1 (commit)
-    B_P_READY = 10,    // [2]  count 256
-    B_PV_DONE = 12,    // [2]  count 1 (commit after dV: P^T consumed, S buffer writable)
-    B_DP_FULL = 14,    // [2]  count 1 (commit)
-    B_DS_READY = 16,   // [2]  count 256 (the softmax may run a tile ahead of the MMA warp)
-    B_DK_DONE = 18,    // [2]  count 1 (commit: dS^T consumed, dP buffer writable)
-    B_DQ_FULL = 20,    // [2]  count 1 (commit); also: that tile's dS smem buffer consumed
-    B_DQ_FREE = 22,    // [2]  count 128 (dQ^T read out of its S buffer)
-    B_ACC_FULL = 24,   //      count 1 (commit)
-    B_ACC_FREE = 25,   //      count 128
-    B_UNIT_FULL = 26,  // [2]  count 1
-    B_UNIT_EMPTY = 28, // [2]  count 14 (MMA + 8 softmax + 4 epilogue warps + writer)
-    B_DRAIN = 30,      //      count 1 (commit)
-    B_STG_FULL = 31,   // [2]  count 128 (per staging slot; half tile k uses slot k % 2)
-    B_STG_FREE = 33,   // [2]  count 1
+    B_Q_FULL = 4,      // [3]  count 32 + tx (Q / dY stage t % 3)
+    B_Q_EMPTY = 7,     // [3]  count 1 (commit)
+    B_S_FULL = 10,     // [2]  count 1 (commit)
+    B_P_READY = 12,    // [2]  count 256
+    B_PV_DONE = 14,    // [2]  count 1 (commit after dV: P^T consumed, S buffer writable)
+    B_DP_FULL = 16,    // [2]  count 1 (commit)
+    B_DS_READY = 18,   // [2]  count 256 (the softmax may run a tile ahead of the MMA warp)
+    B_DK_DONE = 20,    // [2]  unused (dK(t) completion is implied by DQ_FREE(t))
+    B_DQ_FULL = 22,    // [2]  count 1 (commit); also: the dS smem buffer consumed
+    B_DQ_FREE = 24,    // [2]  count 128 (dQ^T read out of its S buffer)
+    B_ACC_FULL = 26,   //      count 1 (commit)
+    B_ACC_FREE = 27,   //      count 128
+    B_UNIT_FULL = 28,  // [2]  count 1
+    B_UNIT_EMPTY = 30, // [2]  count 14 (MMA + 8 softmax + 4 epilogue warps + writer)
+    B_DRAIN = 32,      //      count 1 (commit)
+    B_STG_FULL = 33,   // [2]  count 128 (per staging slot)
+    B_STG_FREE = 35,   // [2]  count 1
 };
 
 // misc words
@@ -135,7 +135,7 @@ struct Smem {
 // over warps (lane 0) and CTAs.  Slots 0-39: barrier waits; 40: role time;
 // 41: dQ counter spins; 42: bulk source-read waits; 43: bulk completion waits;
 // 44: proxy fence; 45: counter release batches.
-__device__ unsigned long long g_wait_stats[6][48];
+__device__ unsigned long long g_wait_stats[6][56];
 __device__ __forceinline__ int wait_role()
 {
     const int w = threadIdx.x >> 5;
@@ -161,6 +161,56 @@ __device__ __forceinline__ void wait_note(int bar, uint32_t k)
 #define WAIT_STAT(slot, t0) ((void)0)
 #endif
 
+#ifdef TND_TRACE
+// Diagnostic build only: an event timeline of CTA 0, per warp (lane 0):
+// {start clock, end clock, (event << 20) | tile}.  Events 0-39: barrier waits;
+// 64 + barrier: arrivals; 100 + slot: UMMA issue of S, dP, dV, dK, dQ.
+constexpr int kTraceLen = 4096;
+__device__ long long g_trace[16][kTraceLen][3];
+__device__ unsigned int g_trace_n[16];
+__device__ __forceinline__ void trace_ev(uint32_t code, long long t0)
+{
+    // per-warp event counts in the unused tail of the dynamic shared memory:
+    // zeroed at kernel start, copied out at its end
+    extern __shared__ uint8_t smem_raw[];
+    unsigned int *s_trace_n = reinterpret_cast<unsigned int *>(
+        ((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) + kSmemUsed);
+    if ((threadIdx.x & 31) == 0 && blockIdx.x == 0) {
+        const int w = threadIdx.x >> 5;
+        volatile unsigned int *n = s_trace_n;
+        if (code == 0xffffffffu) {
+            if (t0 == 0) n[w] = 0;
+            else g_trace_n[w] = n[w];
+            return;
+        }
+        const long long t1 = clock64();   // before the counter's shared-memory load
+        const unsigned i = n[w];
+        n[w] = i + 1;
+        if (i < (unsigned)kTraceLen) {
+            g_trace[w][i][0] = t0;
+            g_trace[w][i][1] = t1;
+            g_trace[w][i][2] = code;
+        }
+    }
+}
+#define TRACE_EV(ev, k, t0) trace_ev(((uint32_t)(ev) << 20) | ((uint32_t)(k) & 0xfffffu), t0)
+#define TRACE_ARR(bar, k) trace_ev(((uint32_t)(64 + (bar)) << 20) | ((uint32_t)(k) & 0xfffffu), clock64())
+#else
+#define TRACE_EV(ev, k, t0) ((void)0)
+#define TRACE_ARR(bar, k) ((void)0)
+#endif
+#if defined(TND_WAIT_STATS) || defined(TND_TRACE)
+#define ISSUE_T0(var) const long long var = clock64()
+#define ISSUE_MARK(slot, var, k) \
+    do {                         \
+        WAIT_STAT(slot, var);    \
+        TRACE_EV(100 + (slot) - 46, k, var); \
+    } while (0)
+#else
+#define ISSUE_T0(var) ((void)0)
+#define ISSUE_MARK(slot, var, k) ((void)0)
+#endif
+
 // Wait for completion `k` (0-based) of barrier `bar`, bounded.
 __device__ __forceinline__ bool wait_k(const Smem &sm, int bar, uint32_t k, const GradArgs &a)
 {
@@ -184,6 +234,7 @@ __device__ __forceinline__ bool wait_k(const Smem &sm, int bar, uint32_t k, cons
         }
     }
     WAIT_STAT(bar, t0);
+    TRACE_EV(bar, k, t0);
     return ok;
 }
 
@@ -297,11 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(sm.bar(B_K_FULL), 1);
         mbar_init(sm.bar(B_K_EMPTY), 1);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(sm.bar(B_Q_FULL + i), 32);
+            mbar_init(sm.bar(B_Q_EMPTY + i), 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(sm.bar(B_STG_FULL + i), 128);
             mbar_init(sm.bar(B_STG_FREE + i), 1);
-            mbar_init(sm.bar(B_Q_FULL + i), 32);
-            mbar_init(sm.bar(B_Q_EMPTY + i), 1);
             mbar_init(sm.bar(B_S_FULL + i), 1);
             mbar_init(sm.bar(B_P_READY + i), 256);
             mbar_init(sm.bar(B_PV_DONE + i), 1);
@@ -345,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm.misc() + MISC_TMEM);
 #ifdef TND_WAIT_STATS
     const long long t_role = clock64();
+#endif
+#ifdef TND_TRACE
+    trace_ev(0xffffffffu, 0);
 #endif
 
     if (warp == 0) {
@@ -416,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(qt + kQColBlk, &tmQ, fb, 64, h, z);
                     tma_load_3d(dyt, &tmDY, fb, 0, h, z);
                     tma_load_3d(dyt + kQColBlk, &tmDY, fb, 64, h, z);
+                    TRACE_ARR(B_Q_FULL, gt);
                     const int64_t vidx = ((int64_t)(U.sd.qblk0 + qb) * a.nq + h) * BR;
                     uint8_t *vec = sm.base + OFF_VEC + s * kVecBytes;
                     bulk_g2s(vec, a.lse2 + vidx, BR * 4, fb);
@@ -489,11 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t g_end = gt + (uint32_t)U.ntiles;
                 // S^T(t) = K Q(t)^T, K-major both, into S buffer t % 2 once the
                 // epilogue has read out dQ^T(t - 2) from it
-                auto issue_s = [&](uint32_t g_t) -> bool {
+                auto issue_s = [&](uint32_t g_t, bool need_q) -> bool {
                     const uint32_t s = g_t % NSTAGE, b = g_t & 1u;
-                    if (!wait_k(sm, B_Q_FULL + s, g_t / NSTAGE, a)) return false;
+                    if (need_q && !wait_k(sm, B_Q_FULL + s, g_t / NSTAGE, a)) return false;
                     if (g_t >= 2 && !wait_k(sm, B_DQ_FREE + b, (g_t >> 1) - 1, a)) return false;
                     tc_fence_after();
+                    ISSUE_T0(ti);
                     const uint64_t dq = desc_at(dQ_k0, s * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
@@ -502,14 +560,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ss(tmem + TM_S0 + b * 64, desc_at(dK_k, off_k), desc_at(dq, off_q), idS, kk > 0);
                     }
                     mma_commit(sm.bar(B_S_FULL + b));
+                    ISSUE_MARK(46, ti, g_t);
                     return true;
                 };
-                // dP^T(t) = V dY(t)^T into dP buffer t % 2 once dK(t - 2) has read
-                // dS^T(t - 2) from it
+                // dP^T(t) = V dY(t)^T into dP buffer t % 2.  Issued right after S^T(t),
+                // whose waits cover it: Q_FULL(t) (dY(t) landed) and DQ_FREE(t - 2),
+                // which the epilogue arrives after observing the commit that follows
+                // dQ^T(t - 2), and a commit tracks every earlier UMMA of the thread, so
+                // dK(t - 2) has read dS^T(t - 2) out of this buffer by then.  Each
+                // barrier wait on this thread costs hundreds of cycles of tensor-pipe
+                // idle time, hence no wait of its own.
                 auto issue_dp = [&](uint32_t g_t) -> bool {
                     const uint32_t s = g_t % NSTAGE, b = g_t & 1u;
-                    if (g_t >= 2 && !wait_k(sm, B_DK_DONE + b, (g_t >> 1) - 1, a)) return false;
-                    tc_fence_after();
+                    ISSUE_T0(ti47);
                     const uint64_t dy = desc_at(dY_k0, s * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
@@ -518,16 +581,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ss(tmem + TM_DP0 + b * 64, desc_at(dV_k, off_v), desc_at(dy, off_y), idS, kk > 0);
                     }
                     mma_commit(sm.bar(B_DP_FULL + b));
+                    ISSUE_MARK(47, ti47, g_t);
                     if (g_t + 1 == g_end) mma_commit(sm.bar(B_V_EMPTY));   // last reader of V
                     return true;
                 };
-                if (!issue_s(gt)) break;
+                if (!issue_s(gt, true)) break;
                 if (!wait_k(sm, B_V_FULL, ku, a)) break;
+                tc_fence_after();
                 if (!issue_dp(gt)) break;
                 for (int t = 0; t < U.ntiles; ++t) {
                     const uint32_t g_t = gt + t, s = g_t % NSTAGE, b = g_t & 1u;
                     // the next tile's S^T and dP^T go ahead of this tile's gradients
-                    if (t + 1 < U.ntiles && (!issue_s(g_t + 1) || !issue_dp(g_t + 1))) {
+                    if (t + 1 < U.ntiles && (!issue_s(g_t + 1, true) || !issue_dp(g_t + 1))) {
                         ok = false;
                         break;
                     }
@@ -541,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    ISSUE_T0(ti48);
                     const uint64_t dqm = desc_at(dQ_m0, s * kQTile), dym = desc_at(dY_m0, s * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
@@ -548,32 +614,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (t > 0 || kk > 0));
                     }
                     mma_commit(sm.bar(B_PV_DONE + b));
+                    ISSUE_MARK(48, ti48, g_t);
                     // dK += dS^T Q(t): A = dS^T (TMEM, packed), B = Q MN-major
                     if (!wait_k(sm, B_DS_READY + b, g_t >> 1, a)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    ISSUE_T0(ti49);
 #pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
                         mma_ts(tmem + TM_DK, tmem + TM_DP0 + b * 64 + pk_col(kk), desc_at(dqm, kk * 2048), idKV,
                                (t > 0 || kk > 0));
                     }
                     mma_commit(sm.bar(B_Q_EMPTY + s));
-                    mma_commit(sm.bar(B_DK_DONE + b));
-                    // dQ^T(t) = K^T dS^T into S buffer t % 2 once dV(t) has read P^T:
+                    ISSUE_MARK(49, ti49, g_t);
+                    // dQ^T(t) = K^T dS^T into S buffer t % 2: dV(t) has read P^T from it
+                    // (the softmax arrives DS_READY(t) only after observing PV_DONE(t)):
                     // A = K MN-major (M = 128 features), B = dS^T MN-major (N = 64)
-                    if (!wait_k(sm, B_PV_DONE + b, g_t >> 1, a)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
+                    ISSUE_T0(ti50);
 #pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
-                        mma_ss(tmem + TM_S0 + b * 64, desc_at(dK_m, kk * 2048), desc_at(dS_m, b * kDsBytes + kk * 2048),
+                        mma_ss(tmem + TM_S0 + b * 64, desc_at(dK_m, kk * 2048), desc_at(dS_m, kk * 2048),
                                idQ, kk > 0);
                     }
                     mma_commit(sm.bar(B_DQ_FULL + b));
+                    ISSUE_MARK(50, ti50, g_t);
                 }
                 if (!ok) break;
                 mma_commit(sm.bar(B_ACC_FULL));
@@ -658,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st16(s_addr + 32 * half, pk);      // packed into this half's own columns
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_P_READY + b));
+                TRACE_ARR(B_P_READY, gt);
                 // ---- phase 2: dS^T = P^T o (z dP^T - D) into TMEM and shared memory
                 if (!wait_warp(sm, B_DP_FULL + b, gt >> 1, a)) {
                     ok = false;
@@ -679,13 +747,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[2 * c4 + 1] = pack2<BF16>(p[4 * c4 + 2] * (dp[2] - dv.z), p[4 * c4 + 3] * (dp[3] - dv.w));
                 }
                 tmem_st16(dp_addr + 32 * half, pk);
-                // dS^T buffer t % 2: the dQ^T GEMM of tile t - 2 must have read it
-                if (gt >= 2 && !wait_warp(sm, B_DQ_FULL + b, (gt >> 1) - 1, a)) {
+                // the dS^T buffer: the dQ^T GEMM of tile t - 1 must have read it
+                if (gt >= 1 && !wait_warp(sm, B_DQ_FULL + (b ^ 1u), (gt - 1) >> 1, a)) {
                     ok = false;
                     break;
                 }
                 {
-                    uint8_t *row = sm.base + OFF_DS + b * kDsBytes + jl * 128;
+                    uint8_t *row = sm.base + OFF_DS + jl * 128;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int chunk = 4 * half + c;
@@ -695,7 +763,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_async_smem();
                 tc_fence_before();
+                // dV(t) has consumed P^T: DS_READY(t) then also frees the S buffer
+                // for dQ^T(t), and the MMA warp needs no wait of its own for it
+                if (!wait_warp(sm, B_PV_DONE + b, gt >> 1, a)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive(sm.bar(B_DS_READY + b));
+                TRACE_ARR(B_DS_READY, gt);
             }
             if (!ok) break;
         }
@@ -739,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(dq_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_DQ_FREE + (gt & 1u)));
+                TRACE_ARR(B_DQ_FREE, gt);
                 // staging: a ring of two [32 q rows][128 features] fp32 slots;
                 // half tile k (q rows 32 (k % 2) .. +31 of tile k / 2) goes to slot
                 // k % 2 once the writer's bulk operation has read half k - 2
@@ -754,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < BR / 2; ++c) slot[c * HD] = __uint_as_float(v[hs * (BR / 2) + c]);
                     fence_async_smem();
                     mbar_arrive(sm.bar(B_STG_FULL + hs));
+                    TRACE_ARR(B_STG_FULL, 2 * gt + hs);
                 }
                 if (!ok) break;
             }
@@ -785,6 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(sm.bar(B_ACC_FREE));
+            TRACE_ARR(B_ACC_FREE, ku);
             ++ku;
         }
     } else if (warp == kWriterWarp) {
@@ -806,7 +884,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             RelEntry *ring = reinterpret_cast<RelEntry *>(sm.base + OFF_REL);
             const uint32_t *rel_head = sm.misc() + MISC_REL_HEAD;
             bool ok = true;
-            // the previous tile's groups have completed: counter queued
+            // the previous tile's groups have completed: counter queued.  Done
+            // before this tile's operations: other CTAs' chains wait on it
             auto finish_prev = [&]() -> bool {
                 if (!pend_flag) return true;
                 const long long tw = clock64();
@@ -898,8 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hs == 1) {
                             bulk_wait_read1();
                             mbar_arrive(sm.bar(B_STG_FREE));
+                            TRACE_ARR(B_STG_FREE, 2 * gt);
                             bulk_wait_read0();
                             mbar_arrive(sm.bar(B_STG_FREE + 1));
+                            TRACE_ARR(B_STG_FREE, 2 * gt + 1);
                         }
                         WAIT_STAT(42, tr);
                     }
@@ -955,6 +1036,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 #ifdef TND_WAIT_STATS
     WAIT_STAT(40, t_role);
+#endif
+#ifdef TND_TRACE
+    trace_ev(0xffffffffu, 1);
 #endif
     tc_fence_before();
     __syncthreads();
@@ -1079,8 +1163,22 @@ extern "C" int tnd_debug_wait_stats(unsigned long long *out, int reset)
 {
     if (cudaMemcpyFromSymbol(out, tnd::g_wait_stats, sizeof(tnd::g_wait_stats)) != cudaSuccess) return 1;
     if (reset) {
-        static unsigned long long zero[6][48] = {};
+        static unsigned long long zero[6][56] = {};
         if (cudaMemcpyToSymbol(tnd::g_wait_stats, zero, sizeof(zero)) != cudaSuccess) return 1;
+    }
+    return 0;
+}
+namespace tnd {
+#endif
+#ifdef TND_TRACE
+}  // namespace tnd
+extern "C" int tnd_debug_trace(long long *events, unsigned int *counts, int reset)
+{
+    if (cudaMemcpyFromSymbol(events, tnd::g_trace, sizeof(tnd::g_trace)) != cudaSuccess) return 1;
+    if (cudaMemcpyFromSymbol(counts, tnd::g_trace_n, sizeof(tnd::g_trace_n)) != cudaSuccess) return 1;
+    if (reset) {
+        static unsigned int zero[16] = {};
+        if (cudaMemcpyToSymbol(tnd::g_trace_n, zero, sizeof(zero)) != cudaSuccess) return 1;
     }
     return 0;
 }
