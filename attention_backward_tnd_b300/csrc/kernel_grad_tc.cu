@@ -168,6 +168,14 @@ __device__ __forceinline__ void wait_note(int bar, uint32_t k)
 constexpr int kTraceLen = 4096;
 __device__ long long g_trace[16][kTraceLen][3];
 __device__ unsigned int g_trace_n[16];
+// every CTA: global timer at start and end, tiles processed (MMA thread)
+__device__ unsigned long long g_cta_time[1024][3];
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 __device__ __forceinline__ void trace_ev(uint32_t code, long long t0)
 {
     // per-warp event counts in the unused tail of the dynamic shared memory:
@@ -396,11 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm.misc() + MISC_TMEM);
+#ifdef TND_TRACE
+    unsigned long long mma_tiles = 0;
+#endif
 #ifdef TND_WAIT_STATS
     const long long t_role = clock64();
 #endif
 #ifdef TND_TRACE
     trace_ev(0xffffffffu, 0);
+    if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_time[blockIdx.x][0] = global_ns();
 #endif
 
     if (warp == 0) {
@@ -646,6 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(sm.bar(B_ACC_FULL));
                 mma_commit(sm.bar(B_K_EMPTY));
                 gt += U.ntiles;
+#ifdef TND_TRACE
+                mma_tiles += U.ntiles;
+#endif
                 ++ku;
             }
             // every issued UMMA must finish before TMEM is released
@@ -1039,6 +1054,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 #ifdef TND_TRACE
     trace_ev(0xffffffffu, 1);
+    if (threadIdx.x == 32 && blockIdx.x < 1024) {
+        g_cta_time[blockIdx.x][1] = global_ns();
+        g_cta_time[blockIdx.x][2] = mma_tiles;
+    }
 #endif
     tc_fence_before();
     __syncthreads();
@@ -1181,6 +1200,10 @@ extern "C" int tnd_debug_trace(long long *events, unsigned int *counts, int rese
         if (cudaMemcpyToSymbol(tnd::g_trace_n, zero, sizeof(zero)) != cudaSuccess) return 1;
     }
     return 0;
+}
+extern "C" int tnd_debug_cta_times(unsigned long long *out)
+{
+    return cudaMemcpyFromSymbol(out, tnd::g_cta_time, sizeof(tnd::g_cta_time)) != cudaSuccess;
 }
 namespace tnd {
 #endif

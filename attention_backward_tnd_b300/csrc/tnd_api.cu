@@ -251,11 +251,16 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         gw.push_back({work, (int32_t)b});
     }
     if (!with_units) return;
-    // Sequences with the most work first; every kv head of a sequence in turn.
+    // Sequences with the most work first; within a sequence, kv blocks in
+    // descending order (every kv head's chain is dispatched in chain order, so
+    // no unit ever waits on one not yet handed out) with all kv heads of a
+    // block together.  Under a causal mask the low kv blocks carry the most
+    // tiles; interleaving the heads makes the last units handed out similar in
+    // size instead of one head's largest blocks, which keeps the tail short.
     std::stable_sort(gw.begin(), gw.end(), [](const GroupWork &x, const GroupWork &y) { return x.work > y.work; });
     for (const GroupWork &w : gw) {
-        for (int64_t g = 0; g < p.nkv; ++g) {
-            for (GradUnit u : seq_units[w.b]) {
+        for (GradUnit u : seq_units[w.b]) {
+            for (int64_t g = 0; g < p.nkv; ++g) {
                 u.g = (int32_t)g;
                 pl.units.push_back(u);
             }
