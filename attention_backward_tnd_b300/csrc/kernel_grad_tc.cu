@@ -300,6 +300,72 @@ __device__ __forceinline__ bool read_unit1(const Smem &sm, uint32_t ui, const Gr
     return true;
 }
 
+// Dropout keep-bits.  Bit p of the packed mask (little-endian within each
+// byte) is bit p % 64 of the little-endian 64-bit word p / 64.  Row ii of head
+// h starts at bit mask_base + (h * sq + ii) * skv; a tile needs the 128 bits
+// of kv block jb.  With an 8-byte aligned mask, three aligned words cover any
+// bit offset; fetch_keep_rows issues them for rows q0 + lane and q0 + lane + 32
+// (independent loads, one memory latency per tile), keep_row_words extracts
+// the four 32-bit words.  Words that reach past the mask's end, and an
+// unaligned mask, take the byte path.
+__device__ __forceinline__ int64_t keep_row_bit(const SeqDesc &sd, int h, int64_t ii, int jb)
+{
+    return sd.mask_base + ((int64_t)h * sd.sq + ii) * sd.skv + (int64_t)jb * kKvBlock;
+}
+
+__device__ __forceinline__ void fetch_keep_rows(const GradArgs &a, const SeqDesc &sd, int h, int64_t q0, int jb,
+                                                int lane, uint64_t (&mw)[2][3])
+{
+    const bool aligned = (reinterpret_cast<uintptr_t>(a.drop_mask) & 7) == 0;
+    const uint64_t *m64 = reinterpret_cast<const uint64_t *>(a.drop_mask);
+    const int64_t nwords = a.mask_bytes >> 3;   // whole words inside the mask
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int64_t ii = q0 + lane + 32 * rr;
+        const int64_t w0 = keep_row_bit(sd, h, ii, jb) >> 6;
+#pragma unroll
+        for (int e = 0; e < 3; ++e) {
+            mw[rr][e] = (aligned && ii < sd.sq && w0 + e < nwords) ? __ldg(m64 + w0 + e) : 0ull;
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 keep_row_words(const uint64_t (&w)[3], const GradArgs &a, const SeqDesc &sd, int h,
+                                                int64_t ii, int jb)
+{
+    if (ii >= sd.sq) return make_uint4(0, 0, 0, 0);
+    const int64_t p0 = keep_row_bit(sd, h, ii, jb);
+    const bool aligned = (reinterpret_cast<uintptr_t>(a.drop_mask) & 7) == 0;
+    uint32_t out[4];
+    if (aligned && (p0 >> 6) + 3 <= (a.mask_bytes >> 3)) {
+        const int sh = (int)(p0 & 63);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int b = sh + 32 * k, q = b >> 6, off = b & 63;   // q <= 2; the word never crosses w[2]
+            // registers, not an indexed array: q is not a compile-time constant
+            const uint64_t wq = q == 0 ? w[0] : q == 1 ? w[1] : w[2];
+            const uint64_t wn = q == 0 ? w[1] : w[2];
+            const uint64_t lo = wq >> off;
+            const uint64_t hi = (off > 32 && q < 2) ? (wn << (64 - off)) : 0ull;
+            out[k] = (uint32_t)(lo | hi);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t pos = p0 + 32 * k;
+            const int64_t byte0 = pos >> 3;
+            uint64_t acc = 0;
+#pragma unroll
+            for (int bb = 0; bb < 5; ++bb) {
+                const int64_t bi = byte0 + bb;
+                acc |= (uint64_t)((bi < a.mask_bytes) ? a.drop_mask[bi] : 0) << (8 * bb);
+            }
+            out[k] = (uint32_t)(acc >> (pos & 7));
+        }
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // Columns [c_lo, c_hi] of the q block (rows q0 + c) that keep kv row jj.
 __device__ __forceinline__ uint64_t keep_columns(const GradArgs &a, const SeqDesc &sd, int64_t q0, int64_t jj)
 {
@@ -446,32 +512,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < U.ntiles; ++t, ++gt) {
                 const int qb = U.qb_lo + t / G, h = U.g * G + t % G;
                 const uint32_t s = gt % NSTAGE, k = gt / NSTAGE;
+                const int64_t q0 = (int64_t)qb * BR;
+                // dropout keep-bits of the tile: 128 kv bits of each of its 64 q
+                // rows, two rows per lane, fetched before the stage wait
+                uint64_t mw[2][3];
+                if (a.has_drop) fetch_keep_rows(a, U.sd, h, q0, U.jb, lane, mw);
                 if (k >= 1 && !wait_warp(sm, B_Q_EMPTY + s, k - 1, a)) {
                     ok = false;
                     break;
                 }
-                const int64_t q0 = (int64_t)qb * BR;
                 if (a.has_drop) {
                     uint32_t *bits = reinterpret_cast<uint32_t *>(sm.base + OFF_BITS + s * BR * 16);
-                    for (int w = lane; w < BR * 4; w += 32) {
-                        const int r = w >> 2, wi = w & 3;
-                        const int64_t ii = q0 + r;
-                        uint32_t word = 0;
-                        if (ii < U.sd.sq) {
-                            const int64_t pos = U.sd.mask_base + ((int64_t)h * U.sd.sq + ii) * U.sd.skv +
-                                                (int64_t)U.jb * BC + 32 * wi;
-                            const int64_t byte0 = pos >> 3;
-                            const int sh = (int)(pos & 7);
-                            uint64_t acc = 0;
 #pragma unroll
-                            for (int bb = 0; bb < 5; ++bb) {
-                                const int64_t bi = byte0 + bb;
-                                const uint64_t v = (bi < a.mask_bytes) ? (uint64_t)a.drop_mask[bi] : 0ull;
-                                acc |= v << (8 * bb);
-                            }
-                            word = (uint32_t)(acc >> sh);
-                        }
-                        bits[w] = word;
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const uint4 v = keep_row_words(mw[rr], a, U.sd, h, q0 + lane + 32 * rr, U.jb);
+                        *reinterpret_cast<uint4 *>(bits + (lane + 32 * rr) * 4) = v;
                     }
                 }
                 __syncwarp();

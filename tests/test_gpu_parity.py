@@ -57,6 +57,22 @@ def test_small_cases_match_oracle(name, grad_path):
 
 
 @pytest.mark.parametrize("grad_path", [0, 1], ids=["auto", "cuda_core"])
+def test_dropout_mask_at_unaligned_address(grad_path):
+    # the keep-bit gather reads the packed mask as 64-bit words when its
+    # address is 8-byte aligned; one byte past an aligned base takes the
+    # byte-wise path and must give the same gradients
+    inp = _small("band_dropout_bf16", seed=778)
+    dev = gh.upload(inp)
+    n = dev["mask"].numel()
+    buf = torch.zeros(n + 1, dtype=torch.uint8, device="cuda")
+    buf[1:] = dev["mask"]
+    dev["mask"] = buf[1:]
+    assert dev["mask"].data_ptr() % 8 != 0
+    got = gh.run_library(inp, dev=dev, grad_path=grad_path)
+    gh.compare_all(inp, got, gh.oracle_reference(inp))
+
+
+@pytest.mark.parametrize("grad_path", [0, 1], ids=["auto", "cuda_core"])
 def test_tiny_varlen_fp16_workload(grad_path):
     inp = workloads.make_inputs(workloads.workload("tiny_varlen_fp16"))
     got = gh.run_library(inp, grad_path=grad_path)
