@@ -246,6 +246,42 @@ __device__ __forceinline__ bool wait_k(const Smem &sm, int bar, uint32_t k, cons
     return ok;
 }
 
+// Single-thread polling variant for the UMMA issuer: mbarrier.test_wait does
+// not suspend the thread, so it reacts to the phase flip without a resume delay.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool wait_poll(const Smem &sm, int bar, uint32_t k, const GradArgs &a)
+{
+    uint64_t *b = sm.bar(bar);
+    const uint32_t parity = k & 1u;
+    const long long t0 = clock64();
+    bool ok = true;
+    while (!mbar_test_wait(b, parity)) {
+        if (*sm.abort_flag()) {
+            ok = false;
+            break;
+        }
+        if (clock64() - t0 > a.wait_limit_cycles) {
+            set_status(a.status, TND_ERR_DEVICE_TIMEOUT, (k << 12) | ((threadIdx.x >> 5) << 6) | (uint32_t)bar);
+            *sm.abort_flag() = 1;
+            ok = false;
+            break;
+        }
+    }
+    TRACE_EV(bar, k, t0);
+    return ok;
+}
+
 // Warp-uniform variant: every lane polls, all lanes agree on the outcome.
 __device__ __forceinline__ bool wait_warp(const Smem &sm, int bar, uint32_t k, const GradArgs &a)
 {
@@ -607,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) break;
                 const UnitInfo U = unit_info(a, u);
                 if (U.ntiles == 0) continue;
-                if (!wait_k(sm, B_K_FULL, ku, a)) break;
+                if (!wait_poll(sm, B_K_FULL, ku, a)) break;
                 tc_fence_after();
                 const uint64_t dK_k = dK_k0, dK_m = dK_m0;
                 const uint32_t g_end = gt + (uint32_t)U.ntiles;
@@ -615,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // epilogue has read out dQ^T(t - 2) from it
                 auto issue_s = [&](uint32_t g_t, bool need_q) -> bool {
                     const uint32_t s = g_t % NSTAGE, b = g_t & 1u;
-                    if (need_q && !wait_k(sm, B_Q_FULL + s, g_t / NSTAGE, a)) return false;
-                    if (g_t >= 2 && !wait_k(sm, B_DQ_FREE + b, (g_t >> 1) - 1, a)) return false;
+                    if (need_q && !wait_poll(sm, B_Q_FULL + s, g_t / NSTAGE, a)) return false;
+                    if (g_t >= 2 && !wait_poll(sm, B_DQ_FREE + b, (g_t >> 1) - 1, a)) return false;
                     tc_fence_after();
                     ISSUE_T0(ti);
                     const uint64_t dq = desc_at(dQ_k0, s * kQTile);
@@ -653,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 if (!issue_s(gt, true)) break;
-                if (!wait_k(sm, B_V_FULL, ku, a)) break;
+                if (!wait_poll(sm, B_V_FULL, ku, a)) break;
                 tc_fence_after();
                 if (!issue_dp(gt)) break;
                 for (int t = 0; t < U.ntiles; ++t) {
@@ -663,12 +699,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (t == 0 && ku >= 1 && !wait_k(sm, B_ACC_FREE, ku - 1, a)) {
+                    if (t == 0 && ku >= 1 && !wait_poll(sm, B_ACC_FREE, ku - 1, a)) {
                         ok = false;
                         break;
                     }
                     // dV += Pd^T dY(t): A = Pd^T (TMEM, packed), B = dY MN-major (N = 128)
-                    if (!wait_k(sm, B_P_READY + b, g_t >> 1, a)) {
+                    if (!wait_poll(sm, B_P_READY + b, g_t >> 1, a)) {
                         ok = false;
                         break;
                     }
@@ -683,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(sm.bar(B_PV_DONE + b));
                     ISSUE_MARK(48, ti48, g_t);
                     // dK += dS^T Q(t): A = dS^T (TMEM, packed), B = Q MN-major
-                    if (!wait_k(sm, B_DS_READY + b, g_t >> 1, a)) {
+                    if (!wait_poll(sm, B_DS_READY + b, g_t >> 1, a)) {
                         ok = false;
                         break;
                     }
