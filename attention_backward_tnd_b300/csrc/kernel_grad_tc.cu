@@ -17,9 +17,9 @@
 // dq_finalize_kernel writes dQ = scale * accumulator in the output dtype.
 // No atomic operation touches data, so results are bitwise deterministic.
 //
-// Warp roles (480 threads, one CTA per SM, persistent over work units taken
+// Warp roles (512 threads, one CTA per SM, persistent over work units taken
 // in plan order from a counter):
-//   warp 0      TMA producer: K (double-buffered) and V (single) per unit,
+//   warp 0      TMA producer: K and V (one buffer each) per unit,
 //               Q / dY and the tile's lse2 / D vectors per tile, dropout
 //               keep-bits staged in shared memory
 //   warp 1      TMEM allocator and single-thread UMMA issuer
