@@ -195,3 +195,30 @@ def test_plan_covers_every_kept_tile_once_in_chain_order(case):
     for (b, g, qb), lst in order.items():
         js = [j for _, j in sorted(lst)]
         assert js == sorted(js, reverse=True), (b, g, qb, js)
+
+
+@pytest.mark.parametrize("case", range(len(PLANS)))
+def test_plan_hands_out_kv_heads_of_a_block_together(case):
+    # units of one sequence come kv block by kv block (descending), every kv
+    # head of a block in a row; sequences with more tiles come first
+    sq, skv, nq, nkv, mode, pre, nxt = PLANS[case]
+    cu_q = np.concatenate([[0], np.cumsum(sq)])
+    cu_kv = np.concatenate([[0], np.cumsum(skv)])
+    st, units, _ = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode)
+    assert st == tnd.TND_OK
+    groups = [units[i:i + nkv] for i in range(0, len(units), nkv)]
+    for grp in groups:
+        assert len(set(grp[:, 0])) == 1 and len(set(grp[:, 2])) == 1, grp
+        assert list(grp[:, 1]) == list(range(nkv)), grp
+    seq_order = []
+    for grp in groups:
+        b, j = int(grp[0, 0]), int(grp[0, 2])
+        if not seq_order or seq_order[-1][0] != b:
+            seq_order.append((b, []))
+        seq_order[-1][1].append(j)
+    assert len({b for b, _ in seq_order}) == len(seq_order), "a sequence's units are split"
+    for b, js in seq_order:
+        assert js == sorted(js, reverse=True), (b, js)
+    work = {b: sum(int(u[4] - u[3]) + 1 for u in units if u[0] == b and u[1] == 0) for b, _ in seq_order}
+    ws = [work[b] for b, _ in seq_order]
+    assert ws == sorted(ws, reverse=True), ws
