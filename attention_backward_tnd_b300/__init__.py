@@ -22,12 +22,12 @@ LIB_PATH = os.path.join(_HERE, "libtndattn.so")
 TND_OK, TND_ERR_NULLPTR, TND_ERR_INVALID, TND_ERR_UNSUPPORTED = 0, 1, 2, 3
 TND_ERR_WORKSPACE, TND_ERR_CUDA, TND_ERR_DEVICE_TIMEOUT, TND_ERR_DEVICE_CHECK = 4, 5, 6, 7
 TND_F16, TND_BF16, TND_F32 = 0, 1, 2
-TND_OPT_GRAD_PATH, TND_OPT_WAIT_LIMIT_MS, TND_OPT_PROFILE = 0, 1, 2
+TND_OPT_GRAD_PATH, TND_OPT_WAIT_LIMIT_MS, TND_OPT_PROFILE, TND_OPT_TEST_SKIP_LOAD = 0, 1, 2, 3
 
 # exported symbols, in header order
 SYMBOLS = ["tnd_attn_fwd_workspace_size", "tnd_attn_fwd", "tnd_attn_grad_workspace_size", "tnd_attn_grad",
            "tnd_attn_device_status", "tnd_status_string", "tnd_attn_set_option", "tnd_attn_profile_read",
-           "tnd_attn_grad_plan", "tnd_attn_grad_static_ws"]
+           "tnd_attn_grad_plan", "tnd_attn_grad_static_ws", "tnd_attn_grad_static_ws_status"]
 
 
 class TndError(RuntimeError):
@@ -68,6 +68,7 @@ def lib():
         L.tnd_attn_grad_static_ws.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p,
                                               _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp,
                                               _vp, _vp]
+        L.tnd_attn_grad_static_ws_status.argtypes = [_vp]
         for name in SYMBOLS:
             if name != "tnd_status_string":
                 getattr(L, name).restype = _int
@@ -141,6 +142,11 @@ def tnd_attn_grad_static_ws(query, key, value, dy, drop_mask, softmax_max, softm
 
 
 TND_STATIC_WS_BYTES = 32 << 20
+
+
+def tnd_attn_grad_static_ws_status(stream):
+    """Device status of the last tnd_attn_grad_static_ws call on the current device (waits for `stream`)."""
+    return lib().tnd_attn_grad_static_ws_status(stream)
 
 
 def tnd_attn_device_status(workspace, workspace_size, stream):

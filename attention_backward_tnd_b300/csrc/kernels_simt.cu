@@ -2,7 +2,7 @@
 // prepass (rowsum(dY o O), log2-sum-exp, sink terms), a dK/dV kernel, a dQ
 // kernel and the dSink reduction.  They serve every dtype (fp32 included)
 // and every head dim up to 256; the tensor-core gradient replaces the dK/dV
-// and dQ kernels for bf16/fp16 at D = 128.
+// and dQ kernels for bf16/fp16 at D = 64 and 128.
 //
 // Formulas: "aclnnFlashAttentionUnpaddingScoreGrad", function description
 // (forward Y = Dropout(Softmax(Mask(scale Q K^T)), keep_prob) V; backward
@@ -152,40 +152,94 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// gradient prepass: one warp per (q block, query head, row of the block);
-// writes the blocked per-row vectors, padded rows included
+// gradient prepass: writes the blocked per-row vectors (padded rows
+// included).  Eight lanes share a row and read dY and O with 16-byte loads
+// when the row length allows it (D * sizeof(T) a multiple of 16); a warp
+// covers four rows per step.  With tc_state it also zeroes the dQ chain
+// counters and the dQ rows of q blocks that no kv block reaches (the
+// tensor-core gradient writes every other dQ row).
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256) prepass_kernel(GradArgs a)
+__device__ __forceinline__ float dot16(const uint4 &x, const uint4 &y)
 {
-    const int lane = threadIdx.x & 31;
+    const T *a = reinterpret_cast<const T *>(&x);
+    const T *b = reinterpret_cast<const T *>(&y);
+    float s = 0.0f;
+#pragma unroll
+    for (int e = 0; e < (int)(16 / sizeof(T)); ++e) s += Elem<T>::load(a + e) * Elem<T>::load(b + e);
+    return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
+{
+    const int lane = threadIdx.x & 31, sub = lane & 7;
     const int64_t nrows = (int64_t)a.n_qblk * a.nq * kQBlock;
     const T *dY = (const T *)a.dy, *O = (const T *)a.o;
-    for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < nrows; w += (int64_t)gridDim.x * 8) {
-        const int64_t blk = w / kQBlock;               // q block * nq + h
-        const int rr = (int)(w - blk * kQBlock);
-        const int qg = (int)(blk / a.nq), h = (int)(blk - (int64_t)qg * a.nq);
-        const int2 qr = a.qblk_rows[qg];
-        const SeqDesc sd = a.seqs[qr.x];
-        const int64_t i = (int64_t)qr.y + rr;
-        if (i >= sd.sq) {
-            if (lane == 0) {
+    const int64_t warps = (int64_t)gridDim.x * 8;
+    const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const bool vec = ((a.d * (int)sizeof(T)) & 15) == 0;
+    const int chunks = a.d * (int)sizeof(T) / 16;          // 16-byte chunks per row
+    for (int64_t w0 = wid * 4; w0 < nrows; w0 += warps * 4) {
+        const int64_t w = w0 + (lane >> 3);                 // this lane's row of the four
+        bool have = w < nrows;
+        int64_t r = 0;
+        int h = 0;
+        bool live_row = false;
+        if (have) {
+            const int64_t blk = w / kQBlock;                // q block * nq + h
+            const int rr = (int)(w - blk * kQBlock);
+            const int qg = (int)(blk / a.nq);
+            h = (int)(blk - (int64_t)qg * a.nq);
+            const int2 qr = a.qblk_rows[qg];
+            const SeqDesc sd = a.seqs[qr.x];
+            const int64_t i = (int64_t)qr.y + rr;
+            live_row = i < sd.sq;
+            r = (sd.tq + i) * a.nq + h;
+        }
+        float dot = 0.0f;
+        if (live_row) {
+            if (vec) {
+                const uint4 *y4 = reinterpret_cast<const uint4 *>(dY + r * a.d);
+                const uint4 *o4 = reinterpret_cast<const uint4 *>(O + r * a.d);
+                for (int c = sub; c < chunks; c += 8) dot += dot16<T>(__ldg(y4 + c), __ldg(o4 + c));
+            } else {
+                for (int c = sub; c < a.d; c += 8) dot += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
+            }
+        }
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+        if (have && sub == 0) {
+            if (!live_row) {
                 a.drow[w] = 0.0f;
                 a.lse2[w] = INFINITY;
                 if (a.has_sink) a.sinkrow[w] = 0.0f;
+            } else {
+                const float m = a.smax[r * 8], l = a.ssum[r * 8];
+                const bool live = l > 0.0f;
+                a.drow[w] = dot;
+                a.lse2[w] = live ? m * kLog2e + lg2(l) : INFINITY;
+                if (a.has_sink) a.sinkrow[w] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * dot : 0.0f;
             }
-            continue;
         }
-        const int64_t r = (sd.tq + i) * a.nq + h;
-        float dot = 0.0f;
-        for (int c = lane; c < a.d; c += 32) dot += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
-        dot = warp_sum(dot);
-        if (lane == 0) {
-            const float m = a.smax[r * 8], l = a.ssum[r * 8];
-            const bool live = l > 0.0f;
-            a.drow[w] = dot;
-            a.lse2[w] = live ? m * kLog2e + lg2(l) : INFINITY;
-            if (a.has_sink) a.sinkrow[w] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * dot : 0.0f;
+    }
+    if (!tc_state) return;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t nflags = (int64_t)a.n_qblk * a.nq;
+    for (int64_t e = tid; e < nflags; e += nthreads) a.flags[e] = 0;
+    // dQ rows of q blocks without contributors (rare): zero, one (q block,
+    // head) per thread
+    const int per_row = a.d * (int)sizeof(T) / 16;
+    for (int64_t e = tid; e < nflags; e += nthreads) {
+        const int qg = (int)(e / a.nq), h = (int)(e - (int64_t)qg * a.nq);
+        if (a.qblk[qg].jlo >= 0) continue;
+        const int2 qr = a.qblk_rows[qg];
+        const SeqDesc sd = a.seqs[qr.x];
+        for (int64_t i = qr.y; i < min((int64_t)qr.y + kQBlock, (int64_t)sd.sq); ++i) {
+            uint4 *dst = reinterpret_cast<uint4 *>((T *)a.dq + ((sd.tq + i) * a.nq + h) * a.d);
+            for (int c = 0; c < per_row; ++c) dst[c] = make_uint4(0, 0, 0, 0);
         }
     }
 }
@@ -425,12 +479,13 @@ template <typename T, int DMAX> struct DqLaunch {
 };
 
 template <typename T, int DMAX> struct PrepassLaunch {
-    static cudaError_t run(const GradArgs &a, cudaStream_t s)
+    static cudaError_t run(const GradArgs &a, bool tc_state, cudaStream_t s)
     {
         const int64_t rows = (int64_t)a.n_qblk * a.nq * kQBlock;
         if (rows == 0) return cudaSuccess;
-        const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 148 * 16);
-        prepass_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(a);
+        // 8 warps per block, 4 rows per warp step; up to 8 resident blocks per SM
+        const int64_t blocks = std::min<int64_t>((rows + 31) / 32, (int64_t)a.num_sms * 8);
+        prepass_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(a, tc_state ? 1 : 0);
         return cudaGetLastError();
     }
 };
@@ -441,7 +496,10 @@ cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s) { return dispatch<
 cudaError_t launch_grad_dkdv_simt(const GradArgs &a, cudaStream_t s) { return dispatch<DkdvLaunch>(a.dtype, a.d, a, s); }
 cudaError_t launch_grad_dq_simt(const GradArgs &a, cudaStream_t s) { return dispatch<DqLaunch>(a.dtype, a.d, a, s); }
 
-cudaError_t launch_prepass(const GradArgs &a, bool, cudaStream_t s) { return dispatch<PrepassLaunch>(a.dtype, a.d, a, s); }
+cudaError_t launch_prepass(const GradArgs &a, bool tc_state, cudaStream_t s)
+{
+    return dispatch<PrepassLaunch>(a.dtype, a.d, a, tc_state, s);
+}
 
 cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s)
 {

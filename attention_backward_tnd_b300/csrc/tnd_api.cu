@@ -23,6 +23,7 @@ struct Options {
     int grad_path = 0;
     int64_t wait_limit_ms = 2000;
     int profile = 0;
+    int test_skip_load = 0;
 };
 Options g_opt;
 std::mutex g_mu;
@@ -32,9 +33,9 @@ struct ProfEntry {
     cudaEvent_t start, stop;
 };
 const char *kKindNames[] = {"fwd_simt", "grad_prepass", "grad_dkdv_simt", "grad_dq_simt",
-                            "grad_sink_reduce", "grad_tc_main", "grad_dq_finalize"};
+                            "grad_sink_reduce", "grad_tc_main"};
 constexpr int kNumKinds = sizeof(kKindNames) / sizeof(kKindNames[0]);
-enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN };
+enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC };
 std::vector<ProfEntry> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 constexpr size_t kProfCap = 4096;
@@ -410,18 +411,70 @@ DeviceInfo device_info()
 
 bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
 
-// Copies the plan into the workspace and clears the status words (and the
-// dQ chain flags of the tensor-core path).
-tnd_status upload_plan(const Plan &pl, const Layout &L, void *ws, bool clear_flags, const Problem &p,
-                       cudaStream_t s)
+// Pinned host staging of plan uploads.  A copy from pageable host memory may
+// make the runtime wait for the stream before it starts, so a run call would
+// block its caller until earlier work on the stream has drained.  Each device
+// gets a ring of pinned slots; a slot is refilled only once the event recorded
+// after its previous copy has completed, which with kStageSlots slots is
+// normally long past.  Slots grow (rarely) by reallocation.
+constexpr int kStageSlots = 8;
+constexpr int kStageDevices = 64;
+struct StageSlot {
+    void *host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+};
+struct StageRing {
+    std::mutex mu;
+    StageSlot slot[kStageSlots];
+    unsigned next = 0;
+};
+StageRing g_stage[kStageDevices];
+
+// Enqueues a copy of `bytes` host bytes to device address `dst` on stream s
+// without waiting for the stream.  Falls back to a plain copy when pinned
+// memory cannot be had.
+cudaError_t staged_copy(void *dst, const void *src, size_t bytes, cudaStream_t s)
 {
-    if (cudaMemcpyAsync(ws, pl.image.data(), pl.image.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return TND_ERR_CUDA;
-    if (clear_flags) {
-        const size_t bytes = pl.qblk.size() * (size_t)p.nq * sizeof(int32_t);
-        if (bytes && cudaMemsetAsync((char *)ws + L.flags, 0, bytes, s) != cudaSuccess) return TND_ERR_CUDA;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStageDevices)
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
+    StageRing &r = g_stage[dev];
+    std::lock_guard<std::mutex> lk(r.mu);
+    StageSlot &sl = r.slot[r.next++ % kStageSlots];
+    if (!sl.done && cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming) != cudaSuccess) {
+        sl.done = nullptr;
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
     }
-    return TND_OK;
+    if (cudaEventSynchronize(sl.done) != cudaSuccess) return cudaErrorUnknown;
+    if (sl.cap < bytes) {
+        if (sl.host) cudaFreeHost(sl.host);
+        sl.host = nullptr;
+        sl.cap = 0;
+        size_t cap = 64 << 10;
+        while (cap < bytes) cap *= 2;
+        if (cudaHostAlloc(&sl.host, cap, cudaHostAllocPortable) != cudaSuccess) {
+            sl.host = nullptr;
+            cudaGetLastError();
+            return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
+        }
+        sl.cap = cap;
+    }
+    std::memcpy(sl.host, src, bytes);
+    cudaError_t e = cudaMemcpyAsync(dst, sl.host, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecord(sl.done, s);
+}
+
+// Copies the plan image (zeroed status words, then the plan arrays) into the
+// workspace.  `pinned` selects the staged copy; without it the copy reads the
+// plan's own (pageable) image and nothing is allocated.  The dQ chain
+// counters are zeroed by the prepass kernel.
+tnd_status upload_plan(const Plan &pl, void *ws, cudaStream_t s, bool pinned = true)
+{
+    const cudaError_t ce = pinned ? staged_copy(ws, pl.image.data(), pl.image.size(), s)
+                                  : cudaMemcpyAsync(ws, pl.image.data(), pl.image.size(), cudaMemcpyHostToDevice, s);
+    return ce == cudaSuccess ? TND_OK : TND_ERR_CUDA;
 }
 
 template <typename A>
@@ -514,6 +567,10 @@ tnd_status tnd_attn_set_option(tnd_option option, int64_t value)
         if (value != 0 && value != 1) return TND_ERR_INVALID;
         g_opt.profile = (int)value;
         return TND_OK;
+    case TND_OPT_TEST_SKIP_LOAD:
+        if (value != 0 && value != 1) return TND_ERR_INVALID;
+        g_opt.test_skip_load = (int)value;
+        return TND_OK;
     }
     return TND_ERR_INVALID;
 }
@@ -579,7 +636,7 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
     const Layout L = layout_for(p, pl, false, false);
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
-    st = upload_plan(pl, L, ws, false, p, s);
+    st = upload_plan(pl, ws, s);
     if (st != TND_OK) return st;
     FwdArgs a{};
     fill_common(a, p, pl, L, ws);
@@ -610,11 +667,15 @@ tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const in
     return TND_OK;
 }
 
-tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                         const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
-                         int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv,
-                         int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq,
-                         void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream)
+}  // extern "C"
+
+namespace tnd {
+
+tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
+                    const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
+                    int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv, int64_t d,
+                    double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv,
+                    float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload)
 {
     if (!q || !k || !v || !dy || !smax || !ssum || !o || !dq || !dk || !dv) return TND_ERR_NULLPTR;
     if (sink && !dsink) return TND_ERR_NULLPTR;
@@ -636,7 +697,7 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     HOST_LAP(1);
-    st = upload_plan(pl, L, ws, tc, p, s);
+    st = upload_plan(pl, ws, s, pinned_upload);
     if (st != TND_OK) return st;
     HOST_LAP(2);
     GradArgs a{};
@@ -672,6 +733,7 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
         const DeviceInfo di = device_info();
         a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)di.clock_khz;
         a.num_sms = di.num_sms;
+        a.test_flags = g_opt.test_skip_load ? 1 : 0;
     }
     HOST_LAP(3);
     if (timed(K_PREPASS, s, [&] { return launch_prepass(a, tc, s); }) != cudaSuccess) return TND_ERR_CUDA;
@@ -679,8 +741,6 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
     if (tc) {
         if (timed(K_TC, s, [&] { return launch_grad_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         HOST_LAP(5);
-        if (timed(K_FIN, s, [&] { return launch_dq_finalize(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
-        HOST_LAP(6);
     } else {
         if (timed(K_DKDV, s, [&] { return launch_grad_dkdv_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         if (timed(K_DQ, s, [&] { return launch_grad_dq_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
@@ -689,6 +749,20 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
         if (timed(K_SINK, s, [&] { return launch_sink_reduce(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
     }
     return TND_OK;
+}
+
+}  // namespace tnd
+
+extern "C" {
+
+tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
+                         const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
+                         int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv,
+                         int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq,
+                         void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream)
+{
+    return grad_run(q, k, v, dy, drop_mask, smax, ssum, o, sink, dtype, batch, cuq, cukv, nq, nkv, d, scale, keep,
+                    pre, next, mode, dq, dk, dv, dsink, ws, ws_size, stream, true);
 }
 
 tnd_status tnd_attn_device_status(const void *ws, uint64_t ws_size, void *stream)

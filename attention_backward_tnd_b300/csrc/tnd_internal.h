@@ -11,7 +11,7 @@ namespace tnd {
 
 // Rows per block of the tensor-core gradient: kv block (UMMA M) and q block.
 constexpr int kKvBlock = 128;
-constexpr int kQBlock = 64;
+constexpr int kQBlock = 128;
 // Rows per block of the CUDA-core kernels.
 constexpr int kSimtRows = 32;
 
@@ -71,12 +71,12 @@ struct QBlockInfo {
 };
 
 // Per-row vectors of the gradient (lse2, D, sink terms) are stored blocked:
-// one 64-float vector per (global 64-row q block, query head), rows past the
+// one 128-float vector per (global 128-row q block, query head), rows past the
 // sequence end padded (lse2 = +inf, D = 0, sink term = 0).  Index of row i of
 // sequence sd, head h:
 __host__ __device__ inline int64_t row_vec_index(const SeqDesc &sd, int32_t nq, int32_t h, int64_t i)
 {
-    return ((int64_t)(sd.qblk0 + (int32_t)(i >> 6)) * nq + h) * kQBlock + (i & (kQBlock - 1));
+    return ((int64_t)(sd.qblk0 + (int32_t)(i / kQBlock)) * nq + h) * kQBlock + (i % kQBlock);
 }
 
 // Everything a gradient launch needs to know (device pointers into the
@@ -110,10 +110,11 @@ struct GradArgs {
     const GradUnit *units;
     int32_t n_units;
     const QBlockInfo *qblk;   // [n_qblk]
-    int32_t *flags;           // [n_qblk][Nq] contributions added so far
+    int32_t *flags;           // [n_qblk][Nq] dQ chain counters (8 per completed contribution)
     float *dqacc;             // [Tq][Nq][D] fp32 partial sums
     int64_t wait_limit_cycles;
     int32_t num_sms;
+    int32_t test_flags;       // bit 0: CTA 0 skips its first K load (bounded-wait test)
 };
 
 struct FwdArgs {
@@ -136,15 +137,23 @@ struct FwdArgs {
 
 // Kernel launchers (each returns the CUDA error of its launch).
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s);
-cudaError_t launch_prepass(const GradArgs &a, bool zero_tc_state, cudaStream_t s);
+// Gradient prepass: the blocked per-row vectors; with tc_state also the dQ
+// chain counters (zeroed) and the dQ rows of q blocks no kv block reaches.
+cudaError_t launch_prepass(const GradArgs &a, bool tc_state, cudaStream_t s);
 cudaError_t launch_grad_dkdv_simt(const GradArgs &a, cudaStream_t s);
 cudaError_t launch_grad_dq_simt(const GradArgs &a, cudaStream_t s);
 cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s);
-// Tensor-core gradient (bf16/fp16, D = 128); false if this build lacks it.
+// Tensor-core gradient (bf16/fp16, D = 64 or 128); false where it does not apply.
 bool grad_tc_supported(int dtype, int d);
 cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s);
-// dQ = scale * accumulated partial sums, in the output dtype; zero for q
-// blocks that no kv block reaches (tensor-core path).
-cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s);
+
+// The gradient call behind tnd_attn_grad.  pinned_upload = false copies the
+// plan from pageable host memory and allocates nothing (the library's pinned
+// staging slots are allocated on first use).
+tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
+                    const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
+                    int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv, int64_t d,
+                    double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv,
+                    float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload);
 
 }  // namespace tnd

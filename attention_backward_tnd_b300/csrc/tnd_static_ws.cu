@@ -1,21 +1,22 @@
 // Gradient entry point for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc: code running while a CUDA stream is
-// being captured into a graph, plug-ins that receive device buffers from a
-// host framework's own allocator and have no allocator of their own, or
-// processes that have reserved all device memory up front.  For them
+// Some callers cannot call cudaMalloc: plug-ins that receive device buffers
+// from a host framework's own allocator and have no allocator of their own,
+// or processes that have reserved all device memory up front.  For them
 // tnd_attn_grad_static_ws runs the same gradient as tnd_attn_grad with its
 // workspace taken from a fixed, file-scope device array instead of a buffer
-// the caller allocates.
+// the caller allocates, and it uploads its plan without the library's pinned
+// staging slots (which are allocated on first use), so it allocates nothing.
 //
 // The array is a static __device__ object: every GPU that loads this
 // library holds it (kStaticWsBytes) until the process exits.  Host code
 // cannot use the array's name as a device address (on the host it names a
-// shadow variable), so the address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made
-// while it is current.
+// shadow variable), so the address is looked up with cudaGetSymbolAddress,
+// with that device current, on the first call made on the device, and looked
+// up again if the device's context has changed since (after cudaDeviceReset).
 #include "tnd_internal.h"
 
+#include <cudaTypedefs.h>
 #include <mutex>
 
 namespace tnd {
@@ -28,6 +29,24 @@ static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
+void *g_static_ctx[kMaxDevices] = {};
+
+// The current context of the calling thread (nullptr if it cannot be read).
+void *current_context()
+{
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 
 // Device address of g_static_ws on the current device (nullptr on failure).
 void *static_ws_address()
@@ -39,6 +58,15 @@ void *static_ws_address()
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) return nullptr;
         g_static_ptr[dev] = p;
+        g_static_ctx[dev] = current_context();
+        return p;
+    }
+    void *ctx = current_context();
+    if (ctx != g_static_ctx[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) return nullptr;
+        g_static_ptr[dev] = p;
+        g_static_ctx[dev] = ctx;
     }
     return g_static_ptr[dev];
 }
@@ -62,8 +90,15 @@ tnd_status tnd_attn_grad_static_ws(const void *q, const void *k, const void *v, 
     if (need > tnd::kStaticWsBytes) return TND_ERR_WORKSPACE;
     void *ws = tnd::static_ws_address();
     if (!ws) return TND_ERR_CUDA;
-    return tnd_attn_grad(q, k, v, dy, drop_mask, smax, ssum, o, sink, dtype, batch, cuq, cukv, nq, nkv, d, scale,
-                         keep, pre, next, mode, dq, dk, dv, dsink, ws, tnd::kStaticWsBytes, stream);
+    return tnd::grad_run(q, k, v, dy, drop_mask, smax, ssum, o, sink, dtype, batch, cuq, cukv, nq, nkv, d, scale,
+                         keep, pre, next, mode, dq, dk, dv, dsink, ws, tnd::kStaticWsBytes, stream, false);
+}
+
+tnd_status tnd_attn_grad_static_ws_status(void *stream)
+{
+    void *ws = tnd::static_ws_address();
+    if (!ws) return TND_ERR_CUDA;
+    return tnd_attn_device_status(ws, tnd::kStaticWsBytes, stream);
 }
 
 }  // extern "C"

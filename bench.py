@@ -36,6 +36,11 @@ import workloads  # noqa: E402
 METRIC = "attention-grad TFLOP/s (mask-adjusted) & % of B300 dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "causal_varlen_bf16"
 FLUSH_BYTES = 256 << 20
+# one oracle sample (forward + gradient in fp64 on the host cores): about
+# ORACLE_TARGET_S of work, never more than ORACLE_MAX_S; the same sample for
+# the cpu_baseline leg and every step of the reference arm
+ORACLE_TARGET_S = 3.0
+ORACLE_MAX_S = 8.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -100,8 +105,8 @@ def traffic_record(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """SM clock and clock-event (throttle) reasons sampled every 10 ms by an
-    NVML thread; summary() keeps the samples taken inside the marked timed
+    """SM clock and clock-event (throttle) reasons sampled every millisecond by
+    an NVML thread; summary() keeps the samples taken inside the marked timed
     region (None when NVML is unavailable)."""
 
     def __init__(self, torch_device):
@@ -144,7 +149,7 @@ class ClockSampler:
             x = self._sample()
             if x is not None:
                 self.samples.append((time.perf_counter(),) + x)
-            time.sleep(0.01)
+            time.sleep(0.001)
 
     def __enter__(self):
         import threading
@@ -265,18 +270,19 @@ def run_reference(args, wl, rank):
         return
     inp = workloads.make_inputs(wl)
     for _ in range(args.warmup):
-        oracle_sample(wl, inp, target_s=1.0, max_s=3.0)
+        oracle_sample(wl, inp, target_s=ORACLE_TARGET_S, max_s=ORACLE_MAX_S)
     vals, secs, text, threads = [], [], "", 1
     for _ in range(args.steps):
-        v, dt, text, threads = oracle_sample(wl, inp, target_s=1.0, max_s=3.0)
+        v, dt, text, threads = oracle_sample(wl, inp, target_s=ORACLE_TARGET_S, max_s=ORACLE_MAX_S)
         vals.append(v)
         secs.append(dt)
-    value = statistics.mean(vals)
+    value = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl, l2_note=False),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": text},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "threads_used": threads,
+                             "kind": "oracle", "sample": text},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -356,12 +362,11 @@ def run_ours(args, wl, rank, world, local_rank):
         raise SystemExit(f"device status after timed steps: {tnd.tnd_status_string(st)}")
     prof = tnd.tnd_attn_profile_read(reset=True)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(step_ms))
+    ms_per_step = float(statistics.median(step_ms))
     if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
+        t = torch.tensor([ms_per_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
+        ms_per_step = float(t.item())
     flop = grad_flop(wl)
     value = world * flop / (ms_per_step * 1e-3) / 1e12
     launches = int(sum(n for _, n in prof.values()))
@@ -441,9 +446,9 @@ def run_ours(args, wl, rank, world, local_rank):
             "wall_s_timed_region": wall,
         }
         if world == 1 and not args.no_cpu_baseline:
-            v_cpu, dt, text, threads = oracle_sample(wl, inp, target_s=12.0, max_s=30.0)
-            line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                    "sample": text, "seconds": dt}
+            v_cpu, dt, text, threads = oracle_sample(wl, inp, target_s=ORACLE_TARGET_S, max_s=ORACLE_MAX_S)
+            line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                    "threads_used": threads, "kind": "oracle", "sample": text, "seconds": dt}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

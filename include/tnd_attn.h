@@ -157,8 +157,20 @@ const char *tnd_status_string(tnd_status status);
  *   TND_OPT_WAIT_LIMIT_MS: upper bound of every device-side wait (default 2000).
  *   TND_OPT_PROFILE: 1 = record CUDA events around each kernel of every call
  *                    (read with tnd_attn_profile_read), 0 = off (default).
+ *   TND_OPT_TEST_SKIP_LOAD: test hook for the bounded waits ([UnpadGrad]
+ *                    constraints: a wait that cannot finish must end in a
+ *                    timeout error, not a hang).  1 = the tensor-core
+ *                    gradient's first CTA never loads its first K tile, so
+ *                    the wait for it expires and the call reports
+ *                    TND_ERR_DEVICE_TIMEOUT through tnd_attn_device_status
+ *                    (its outputs are then invalid); 0 = off (default).
  */
-typedef enum tnd_option { TND_OPT_GRAD_PATH = 0, TND_OPT_WAIT_LIMIT_MS = 1, TND_OPT_PROFILE = 2 } tnd_option;
+typedef enum tnd_option {
+    TND_OPT_GRAD_PATH = 0,
+    TND_OPT_WAIT_LIMIT_MS = 1,
+    TND_OPT_PROFILE = 2,
+    TND_OPT_TEST_SKIP_LOAD = 3
+} tnd_option;
 tnd_status tnd_attn_set_option(tnd_option option, int64_t value);
 
 /*
@@ -178,7 +190,7 @@ tnd_status tnd_attn_profile_read(const char **names, double *total_ms, int64_t *
  * first q block, end q block) in the order the tensor-core kernel takes
  * them, the unit count to *n_units and the number of kept (q-row, kv-row)
  * pairs summed over sequences and query heads to *kept_pairs.  Blocks are
- * 128 kv rows and 64 q rows.
+ * 128 kv rows and 128 q rows.
  */
 tnd_status tnd_attn_grad_plan(
     int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, int64_t head_num,
@@ -189,10 +201,9 @@ tnd_status tnd_attn_grad_plan(
  * Gradient without a caller-provided workspace.  The pages have no
  * counterpart: their operator always takes a workspace the caller allocates.
  *
- * For callers that cannot allocate device memory, for instance code that
- * runs while a stream is being captured (cudaMalloc is not allowed there),
- * a plug-in that only receives buffers from its host framework's allocator,
- * or a process that reserved all device memory at start-up.  Arguments and
+ * For callers that cannot allocate device memory, for instance a plug-in
+ * that only receives buffers from its host framework's allocator, or a
+ * process that reserved all device memory at start-up.  Arguments and
  * results are those of tnd_attn_grad without `workspace` / `workspace_size`;
  * the caller still passes every input and output.
  *
@@ -200,15 +211,18 @@ tnd_status tnd_attn_grad_plan(
  * TND_STATIC_WS_BYTES bytes, held on every GPU that loads the library until
  * the process exits.  A problem whose tnd_attn_grad_workspace_size exceeds
  * it returns TND_ERR_WORKSPACE before any device work.  No call allocates
- * device memory (no cudaMalloc / cudaFree, no allocating library routine).
- * The first call on each device looks the array's device address up (with
- * that device current) and keeps it; make that first call before any stream
- * capture.  Every call shares the one array and it keeps the last call's
- * contents: each call rewrites the parts that must start at zero (status
- * words, dQ chain counters) on its stream before its kernels run, so calls
- * in sequence are independent, but calls that overlap on the GPU (other
- * streams, other host threads) race on it and give wrong results.  Device
- * errors of such a call are not reported through tnd_attn_device_status.
+ * memory (no cudaMalloc / cudaFree, no pinned host staging, no allocating
+ * library routine); the plan is copied from pageable host memory, so the
+ * call may wait for earlier work on `stream` before it returns.  The first
+ * call on each device looks the array's device address up (with that device
+ * current) and keeps it, looking it up again if the device's context changes
+ * (cudaDeviceReset); make that first call before any stream capture.  Every
+ * call shares the one array and it keeps the last call's contents: each
+ * call rewrites the parts that must start at zero (status words, dQ chain
+ * counters) on its stream before its kernels run, so calls in sequence are
+ * independent, but calls that overlap on the GPU (other streams, other host
+ * threads) race on it and give wrong results.  Device-side errors of these
+ * calls are read with tnd_attn_grad_static_ws_status.
  */
 #define TND_STATIC_WS_BYTES (32ull << 20)
 tnd_status tnd_attn_grad_static_ws(
@@ -219,6 +233,13 @@ tnd_status tnd_attn_grad_static_ws(
     int64_t kv_head_num, int64_t head_dim, double scale_value, double keep_prob,
     int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode, void *dq, void *dk, void *dv,
     float *dsink, void *stream);
+
+/*
+ * tnd_attn_device_status for the fixed workspace of tnd_attn_grad_static_ws
+ * on the current device: waits for `stream`, then returns TND_OK,
+ * TND_ERR_DEVICE_TIMEOUT or TND_ERR_DEVICE_CHECK for the last such call.
+ */
+tnd_status tnd_attn_grad_static_ws_status(void *stream);
 
 #ifdef __cplusplus
 }

@@ -66,27 +66,163 @@ def oracle_reference(inp: workloads.Inputs, **kw):
     return {"out": out, "smax": smax, "ssum": ssum, "dq": dq, "dk": dk, "dv": dv, "dsink": dsink}
 
 
-def tolerance(dtype: str, ref: np.ndarray):
-    """Per-element bound: bf16/fp16 |err| <= 1e-2 + 2e-2|ref|; fp32 relative
-    1e-4, with an absolute floor of 1e-5 x the tensor's RMS for elements whose
-    reference nearly cancels (fp32 sums of O(1) terms carry ~1e-7 absolute
-    error however small the result)."""
+U32 = 2.0 ** -24          # unit roundoff of fp32
+EPS_APPROX = 2.0 ** -21   # bound used for the relative error of ex2.approx / lg2.approx.f32 (PTX ISA: ~2 ulp)
+
+
+def gamma(n):
+    """gamma_n = n u / (1 - n u): the standard bound on the relative error of an
+    n-term fp32 sum or dot product (|fl(x.y) - x.y| <= gamma_n sum |x_i y_i|)."""
+    nu = np.asarray(n, dtype=np.float64) * U32
+    return nu / (1.0 - nu)
+
+
+def fp32_error_bound(inp: workloads.Inputs, ref: dict) -> dict:
+    """First-order bound, per output element, on the rounding error of any
+    fp32 evaluation of the forward and gradient of this problem.
+
+    Each sum of the method gets the dot-product bound gamma_n * (sum of the
+    absolute values of its terms), each exp2 / log2 the fast-approximation
+    error EPS_APPROX, each product or subtraction one rounding u; errors are
+    carried forward through P, O, D, dP, dS to dQ, dK, dV and dSink.  Inputs
+    are the exact stored values, so the arithmetic is the only error source.
+    The sum of first-order terms is doubled to cover second-order ones.
+    Only for small problems: it forms the dense Sq x Skv matrices."""
+    wl = inp.wl
+    g = wl.nq // wl.nkv
+    d = wl.d
+    out = {n: np.zeros_like(ref[n]) for n in ("out", "dq", "dk", "dv")}
+    out["dsink"] = np.zeros(wl.nq)
+    p = oracle_problem(inp)
+    for b in range(wl.batch):
+        sq, skv = wl.seqlens_q[b], wl.seqlens_kv[b]
+        if sq == 0 or skv == 0:
+            continue
+        q0, k0 = wl.cu_q[b], wl.cu_kv[b]
+        keep = np.array([[oracle.keep(wl.sparse_mode, wl.pre_tokens, wl.next_tokens, sq, skv, i, j)
+                          for j in range(skv)] for i in range(sq)], dtype=bool)
+        nk = keep.sum(axis=1) + (1 if inp.sink is not None else 0)
+        base = p.mask_base(b)
+        for h in range(wl.nq):
+            kv = h // g
+            Q, dY = inp.q64[q0:q0 + sq, h], inp.dy64[q0:q0 + sq, h]
+            K, V = inp.k64[k0:k0 + skv, kv], inp.v64[k0:k0 + skv, kv]
+            O = ref["out"][q0:q0 + sq, h]
+            m, l = ref["smax"][q0:q0 + sq, h], ref["ssum"][q0:q0 + sq, h]
+            if inp.mask is not None:
+                idx = base + (h * sq + np.arange(sq))[:, None] * skv + np.arange(skv)[None, :]
+                bits = (inp.mask[idx >> 3] >> (idx & 7)) & 1
+                Z = bits / wl.keep_prob
+            else:
+                Z = np.ones((sq, skv))
+            live = l > 0
+            S = wl.scale * Q @ K.T
+            Sabs = wl.scale * np.abs(Q) @ np.abs(K).T
+            P = np.where(keep & live[:, None], np.exp(S - np.where(live, m, 0)[:, None])
+                         / np.where(live, l, 1)[:, None], 0.0)
+            smax_abs = np.where(keep, Sabs, 0).max(axis=1)
+            epsP = 3 * gamma(d) * smax_abs + 2 * gamma(nk) + 4 * EPS_APPROX + 8 * U32
+            PZ = P * np.abs(Z)
+            errO = (PZ * (epsP + gamma(nk))[:, None]) @ np.abs(V)
+            D = np.sum(dY * O, axis=1)
+            errD = gamma(d) * np.sum(np.abs(dY * O), axis=1) + np.sum(np.abs(dY) * errO, axis=1)
+            dP = dY @ V.T
+            dPabs = np.abs(dY) @ np.abs(V).T
+            dS = P * (Z * dP - D[:, None])
+            errdS = np.abs(dS) * (epsP + 2 * U32)[:, None] + P * (np.abs(Z) * gamma(d) * dPabs + errD[:, None])
+            out["out"][q0:q0 + sq, h] += errO
+            out["dq"][q0:q0 + sq, h] += wl.scale * ((errdS + gamma(nk)[:, None] * np.abs(dS)) @ np.abs(K)) \
+                + U32 * np.abs(ref["dq"][q0:q0 + sq, h])
+            nm = g * sq
+            out["dk"][k0:k0 + skv, kv] += wl.scale * ((errdS + gamma(nm) * np.abs(dS)).T @ np.abs(Q))
+            out["dv"][k0:k0 + skv, kv] += (PZ * (epsP + gamma(nm))[:, None]).T @ np.abs(dY)
+            if inp.sink is not None:
+                ps = np.where(live, np.exp(float(inp.sink[h]) - np.where(live, m, 0)) / np.where(live, l, 1), 0.0)
+                out["dsink"][h] += np.sum(ps * (np.abs(D) * (epsP + gamma(wl.tq)) + errD))
+    for n in ("out", "dq", "dk", "dv", "dsink"):
+        out[n] *= 2.0
+    out["dk"] += U32 * np.abs(ref["dk"])
+    return out
+
+
+def plain_fp32_eval(inp: workloads.Inputs) -> dict:
+    """Textbook fp32 evaluation of the forward and gradient with torch on the
+    CPU (float32 throughout, dense masked softmax): the accuracy yardstick
+    for the fp32 path.  Small problems only."""
+    wl = inp.wl
+    g = wl.nq // wl.nkv
+    import torch
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).float()  # noqa: E731
+    q, k, v, dy = t(inp.q64), t(inp.k64), t(inp.v64), t(inp.dy64)
+    out = torch.zeros_like(q)
+    dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    dsink = torch.zeros(wl.nq)
+    p = oracle_problem(inp)
+    for b in range(wl.batch):
+        sq, skv = wl.seqlens_q[b], wl.seqlens_kv[b]
+        q0, k0 = wl.cu_q[b], wl.cu_kv[b]
+        keep = torch.tensor([[oracle.keep(wl.sparse_mode, wl.pre_tokens, wl.next_tokens, sq, skv, i, j)
+                              for j in range(skv)] for i in range(sq)])
+        base = p.mask_base(b)
+        for h in range(wl.nq):
+            kv = h // g
+            Q, dY = q[q0:q0 + sq, h], dy[q0:q0 + sq, h]
+            K, V = k[k0:k0 + skv, kv], v[k0:k0 + skv, kv]
+            S = (Q @ K.T) * wl.scale
+            S = torch.where(keep, S, torch.tensor(-float("inf")))
+            m = S.max(dim=1).values
+            if inp.sink is not None:
+                m = torch.maximum(m, torch.tensor(float(inp.sink[h])))
+            E = torch.exp(S - m[:, None])
+            l = E.sum(dim=1) + (torch.exp(torch.tensor(float(inp.sink[h])) - m) if inp.sink is not None else 0)
+            P = E / l[:, None]
+            if inp.mask is not None:
+                idx = base + (h * sq + np.arange(sq))[:, None] * skv + np.arange(skv)[None, :]
+                Z = torch.from_numpy(((inp.mask[idx >> 3] >> (idx & 7)) & 1) / wl.keep_prob).float()
+            else:
+                Z = torch.ones(sq, skv)
+            O = (P * Z) @ V
+            out[q0:q0 + sq, h] = O
+            D = (dY * O).sum(dim=1)
+            dS = P * (Z * (dY @ V.T) - D[:, None])
+            dq[q0:q0 + sq, h] = (dS @ K) * wl.scale
+            dk[k0:k0 + skv, kv] += (dS.T @ Q) * wl.scale
+            dv[k0:k0 + skv, kv] += (P * Z).T @ dY
+            if inp.sink is not None:
+                dsink[h] += -(torch.exp(torch.tensor(float(inp.sink[h])) - m) / l * D).sum()
+    return {n: x.double().numpy() for n, x in dict(out=out, dq=dq, dk=dk, dv=dv, dsink=dsink).items()}
+
+
+def tolerance(dtype: str, ref: np.ndarray, bound=None):
+    """Per-element bound.  bf16/fp16: |err| <= 1e-2 + 2e-2|ref|.  fp32: 1e-4
+    relative, plus the fp32 rounding bound of that element (fp32_error_bound)
+    for elements whose reference nearly cancels: a relative bound alone
+    cannot hold where the exact result is far smaller than its terms."""
     if dtype in ("bf16", "f16"):
         return 1e-2 + 2e-2 * np.abs(ref)
-    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
-    return 1e-4 * np.abs(ref) + 1e-5 * max(rms, 1e-30)
+    assert bound is not None, "fp32 comparisons need the element-wise rounding bound"
+    return 1e-4 * np.abs(ref) + bound
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str, mask=None):
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str, mask=None, bound=None):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if bound is not None:
+        bound = np.broadcast_to(np.asarray(bound, dtype=np.float64), ref.shape)
     if mask is not None:
         got, ref = got[mask], ref[mask]
+        bound = None if bound is None else bound[mask]
     if got.size == 0:
         return 0.0
     err = np.abs(got - ref)
-    tol = tolerance(dtype, ref)
+    if dtype == "f32":
+        # "1e-4 relative" read for the tensor as a whole (norm-wise) ...
+        nrm = float(np.linalg.norm(ref))
+        assert float(np.linalg.norm(err)) <= 1e-4 * nrm or nrm == 0.0, (
+            f"{what}: norm-wise relative error {np.linalg.norm(err) / nrm:.3e} > 1e-4")
+    # ... and element by element with the rounding bound where the result cancels
+    tol = tolerance(dtype, ref, bound)
     bad = ~(err <= tol)
     maxnorm = float(np.nanmax(err)) if not np.isnan(err).all() else float("nan")
     if bad.any():
@@ -105,9 +241,31 @@ def stat_lanes_equal(t: torch.Tensor) -> bool:
     return bool(same.all()) and finite.numel() > 0
 
 
+def smax_bound(inp: workloads.Inputs, ref_smax: np.ndarray) -> np.ndarray:
+    """Rounding bound of the forward's softmax max m_i: every logit is an
+    fp32 dot product of length D (|error| <= gamma_D scale sum|q||k| <=
+    gamma_D scale ||q_i|| ||k_j|| by Cauchy-Schwarz), plus a few roundings
+    of the log2 / natural-log unit changes; doubled like fp32_error_bound."""
+    wl = inp.wl
+    g = wl.nq // wl.nkv
+    qn = np.linalg.norm(inp.q64, axis=2)                    # [Tq, Nq]
+    kn = np.linalg.norm(inp.k64, axis=2)                    # [Tkv, Nkv]
+    bound = np.zeros((wl.tq, wl.nq))
+    for b in range(wl.batch):
+        q0, q1, k0, k1 = wl.cu_q[b], wl.cu_q[b + 1], wl.cu_kv[b], wl.cu_kv[b + 1]
+        if q1 == q0 or k1 == k0:
+            continue
+        kmax = kn[k0:k1].max(axis=0)                       # [Nkv]
+        bound[q0:q1] = wl.scale * qn[q0:q1] * np.repeat(kmax, g)[None, :]
+    m = np.where(np.isfinite(ref_smax), np.abs(ref_smax), 0.0)
+    return 2.0 * (gamma(wl.d + 2) * bound + 4 * U32 * m)
+
+
 def compare_all(inp: workloads.Inputs, got: dict, ref: dict, q_rows=None, kv_rows=None, heads=None):
     """Compare forward and gradient outputs; q_rows / kv_rows / heads select
-    the part the oracle computed (numpy boolean masks over T and N)."""
+    the part the oracle computed (numpy boolean masks over T and N).  fp32
+    problems are compared with their element-wise rounding bound, which is
+    only formed for small problems."""
     wl = inp.wl
     nq, nkv, g = wl.nq, wl.nkv, wl.nq // wl.nkv
     hsel = np.zeros(nq, bool)
@@ -121,20 +279,26 @@ def compare_all(inp: workloads.Inputs, got: dict, ref: dict, q_rows=None, kv_row
     km = np.ones(wl.tkv, bool) if kv_rows is None else kv_rows
     qsel = qm[:, None] & hsel[None, :]
     ksel = km[:, None] & gsel[None, :]
+    bnd = fp32_error_bound(inp, ref) if wl.dtype == "f32" else {}
     res = {}
     out = host64(got["out"])
-    res["out"] = assert_close(out, ref["out"], wl.dtype, "attention_out", qsel[..., None].repeat(wl.d, -1))
+    res["out"] = assert_close(out, ref["out"], wl.dtype, "attention_out", qsel[..., None].repeat(wl.d, -1),
+                              bnd.get("out"))
     smax = got["smax"].cpu().numpy().astype(np.float64)
     ssum = got["ssum"].cpu().numpy().astype(np.float64)
     assert stat_lanes_equal(got["smax"]) and stat_lanes_equal(got["ssum"])
     fin = np.isfinite(ref["smax"]) & qsel
     assert np.array_equal(np.isfinite(smax[..., 0]) & qsel, fin), "softmax_max finiteness"
-    assert_close(smax[..., 0], ref["smax"], "f32", "softmax_max", fin)
+    assert_close(smax[..., 0], ref["smax"], "f32", "softmax_max", fin, smax_bound(inp, ref["smax"]))
     np.testing.assert_allclose(ssum[..., 0][qsel], ref["ssum"][qsel], rtol=2e-5, atol=1e-6)
-    res["dq"] = assert_close(host64(got["dq"]), ref["dq"], wl.dtype, "dq", qsel[..., None].repeat(wl.d, -1))
-    res["dk"] = assert_close(host64(got["dk"]), ref["dk"], wl.dtype, "dk", ksel[..., None].repeat(wl.d, -1))
-    res["dv"] = assert_close(host64(got["dv"]), ref["dv"], wl.dtype, "dv", ksel[..., None].repeat(wl.d, -1))
+    res["dq"] = assert_close(host64(got["dq"]), ref["dq"], wl.dtype, "dq", qsel[..., None].repeat(wl.d, -1),
+                             bnd.get("dq"))
+    res["dk"] = assert_close(host64(got["dk"]), ref["dk"], wl.dtype, "dk", ksel[..., None].repeat(wl.d, -1),
+                             bnd.get("dk"))
+    res["dv"] = assert_close(host64(got["dv"]), ref["dv"], wl.dtype, "dv", ksel[..., None].repeat(wl.d, -1),
+                             bnd.get("dv"))
     if got["dsink"] is not None:
         ds = got["dsink"].cpu().numpy().astype(np.float64)
-        res["dsink"] = assert_close(ds, ref["dsink"], "bf16" if wl.dtype != "f32" else "f32", "dsink", hsel)
+        res["dsink"] = assert_close(ds, ref["dsink"], "bf16" if wl.dtype != "f32" else "f32", "dsink", hsel,
+                                    bnd.get("dsink"))
     return res

@@ -148,7 +148,7 @@ def _tiles(mode, pre, nxt, sq, skv):
     for i in range(sq):
         for j in range(skv):
             if _keep(mode, pre, nxt, sq, skv, i, j):
-                tiles.add((i // 64, j // 128))
+                tiles.add((i // 128, j // 128))
                 kept += 1
     return tiles, kept
 

@@ -54,6 +54,14 @@ def test_small_cases_match_oracle(name, grad_path):
     got = gh.run_library(inp, grad_path=grad_path)
     ref = gh.oracle_reference(inp)
     gh.compare_all(inp, got, ref)
+    if inp.wl.dtype == "f32":
+        # accuracy class: no worse than a textbook fp32 evaluation of the
+        # same formulas, within a factor of 4, in the max norm
+        plain = gh.plain_fp32_eval(inp)
+        for n in ("out", "dq", "dk", "dv"):
+            e_lib = float(np.max(np.abs(gh.host64(got[n]) - ref[n])))
+            e_plain = float(np.max(np.abs(plain[n] - ref[n])))
+            assert e_lib <= 4.0 * e_plain, (n, e_lib, e_plain)
 
 
 @pytest.mark.parametrize("grad_path", [0, 1], ids=["auto", "cuda_core"])
@@ -164,6 +172,55 @@ def test_long_causal_sink_bf16_workload_sampled():
     expect = -(psink * D).sum(axis=0)
     np.testing.assert_allclose(got["dsink"].cpu().numpy(), expect, rtol=1e-3, atol=1e-3)
     assert res["dq"] >= 0
+
+
+def test_long_causal_sink_dsink_matches_oracle():
+    """dSink sums -p_sink,i D_i over every query row of a head, so it is
+    checked in full against the oracle on a long (4096-row) causal sequence
+    with a sink, together with every other output."""
+    wl = workloads.custom("long_sink_4096", "bf16", [4096], [4096], 2, 2, 128, sparse_mode=3, has_sink=True,
+                          seed=905)
+    inp = workloads.make_inputs(wl)
+    got = gh.run_library(inp)
+    ref = gh.oracle_reference(inp)
+    res = gh.compare_all(inp, got, ref)
+    assert "dsink" in res
+
+
+def test_grad_call_returns_before_earlier_stream_work_finishes():
+    """The run call only enqueues: with a long kernel queued ahead of it on
+    the same stream, tnd_attn_grad returns while that kernel still runs."""
+    import time
+    inp = _small("causal_bf16_ragged")
+    wl = inp.wl
+    dev = gh.upload(inp)
+    out, smax, ssum = tnd_mod().fwd(dev["q"], dev["k"], dev["v"], wl.cu_q, wl.cu_kv, wl.scale)
+    ws = torch.empty(max(tnd_mod().grad_workspace_bytes(dev["q"], dev["k"], wl.cu_q, wl.cu_kv, wl.scale,
+                                                        sparse_mode=wl.sparse_mode), 256),
+                     dtype=torch.uint8, device="cuda")
+    outs = (torch.empty_like(dev["q"]), torch.empty_like(dev["k"]), torch.empty_like(dev["v"]), None)
+
+    def call():
+        tnd_mod().grad(dev["q"], dev["k"], dev["v"], dev["dy"], out, smax, ssum, wl.cu_q, wl.cu_kv, wl.scale,
+                       sparse_mode=wl.sparse_mode, workspace=ws, outputs=outs)
+
+    call()                                  # plan cached, kernels loaded
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e9 * 0.5))       # about half a second of spinning at ~2 GHz
+    marker = torch.cuda.Event()
+    marker.record()
+    t0 = time.perf_counter()
+    call()
+    dt = time.perf_counter() - t0
+    still_running = not marker.query()
+    torch.cuda.synchronize()
+    assert still_running, f"the sleep kernel had finished when the call returned ({dt * 1e3:.1f} ms)"
+    assert dt < 0.1, dt
+
+
+def tnd_mod():
+    import attention_backward_tnd_b300 as tnd
+    return tnd
 
 
 def test_bilinear_identities_on_gpu_outputs():

@@ -1,16 +1,15 @@
 """The gradient entry point that allocates nothing (tnd_attn_grad_static_ws).
 
-It serves callers that cannot allocate device memory, such as code running
-during stream capture, where cudaMalloc is not allowed, or a plug-in that only
-gets buffers from its host framework.  Its workspace is a fixed device array
-inside the library.  This file is named so that pytest collects it last:
+It serves callers that cannot allocate device memory, such as a plug-in that
+only gets buffers from its host framework's allocator, or a process that
+reserved all device memory at start-up.  Its workspace is a fixed device
+array inside the library.  This file is named so that pytest collects it last:
 if it fails, a run that stops at the first failure has already run every
 other test.
 """
 
 import ctypes
 
-import numpy as np
 import pytest
 
 import attention_backward_tnd_b300 as tnd
@@ -41,15 +40,20 @@ def test_static_ws_rejects_problems_beyond_its_capacity():
 
 @pytest.mark.gpu
 def test_static_ws_matches_workspace_entry_point_twice():
+    """Both entry points run the same deterministic kernels, so their outputs
+    must be bit-identical.  Problems run large, small, large again, each call
+    twice in a row, so a stale word left in the shared array by a larger or
+    an earlier call would show."""
     torch = pytest.importorskip("torch")
     from tests import gpu_helpers as gh
 
-    cases = [workloads.custom("static_ws_causal_sink", "bf16", [300, 77, 129], [300, 77, 129], 4, 2, 128,
-                              sparse_mode=3, has_sink=True, seed=31),
-             workloads.custom("static_ws_band_dropout", "bf16", [260, 190], [260, 190], 4, 1, 128,
-                              keep_prob=0.9, pre_tokens=64, next_tokens=3, sparse_mode=4, seed=32)]
+    large = workloads.custom("static_ws_causal_sink", "bf16", [300, 77, 129], [300, 77, 129], 4, 2, 128,
+                             sparse_mode=3, has_sink=True, seed=31)
+    small = workloads.custom("static_ws_band_dropout", "bf16", [60, 19], [60, 19], 2, 1, 128,
+                             keep_prob=0.9, pre_tokens=64, next_tokens=3, sparse_mode=4, seed=32)
     stream = torch.cuda.current_stream().cuda_stream
-    for wl in cases:
+    prepared = {}
+    for wl in (large, small):
         inp = workloads.make_inputs(wl)
         dev = gh.upload(inp)
         dev["out"], dev["smax"], dev["ssum"] = tnd.fwd(dev["q"], dev["k"], dev["v"], wl.cu_q, wl.cu_kv, wl.scale,
@@ -58,15 +62,20 @@ def test_static_ws_matches_workspace_entry_point_twice():
         ref = tnd.grad(dev["q"], dev["k"], dev["v"], dev["dy"], dev["out"], dev["smax"], dev["ssum"], wl.cu_q,
                        wl.cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens, wl.next_tokens, wl.sparse_mode,
                        dev["mask"], dev["sink"])
-        outs = (torch.full_like(dev["q"], float("nan")), torch.full_like(dev["k"], float("nan")),
-                torch.full_like(dev["v"], float("nan")),
-                None if dev["sink"] is None else torch.full((wl.nq,), float("nan"), device="cuda"))
-        st = _call_static(dev, wl, outs, stream)
-        assert st == tnd.TND_OK, tnd.tnd_status_string(st)
-        torch.cuda.synchronize()
-        for name, got, want in zip(("dq", "dk", "dv", "dsink"), outs, ref):
-            if want is None:
-                continue
-            g, w = gh.host64(got), gh.host64(want)
-            assert not np.isnan(g).any(), (wl.name, name)
-            assert np.all(np.abs(g - w) <= 1e-2 + 2e-2 * np.abs(w)), (wl.name, name, float(np.abs(g - w).max()))
+        prepared[wl.name] = (dev, ref)
+    for wl in (large, small, large):
+        dev, ref = prepared[wl.name]
+        for _ in range(2):
+            outs = (torch.full_like(dev["q"], float("nan")), torch.full_like(dev["k"], float("nan")),
+                    torch.full_like(dev["v"], float("nan")),
+                    None if dev["sink"] is None else torch.full((wl.nq,), float("nan"), device="cuda"))
+            st = _call_static(dev, wl, outs, stream)
+            assert st == tnd.TND_OK, tnd.tnd_status_string(st)
+            st = tnd.tnd_attn_grad_static_ws_status(stream)
+            assert st == tnd.TND_OK, tnd.tnd_status_string(st)
+            for name, got, want in zip(("dq", "dk", "dv", "dsink"), outs, ref):
+                if want is None:
+                    continue
+                assert got.dtype == want.dtype
+                bits = torch.int16 if got.element_size() == 2 else torch.int32
+                assert torch.equal(got.view(bits), want.view(bits)), (wl.name, name)
