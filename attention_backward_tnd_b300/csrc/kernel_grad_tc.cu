@@ -13,32 +13,34 @@
 //     dQ_i^T = K_j^T dS^T                    (UMMA, smem x smem -> TMEM)
 // dK_j (x scale) and dV_j leave TMEM once per unit.  The dQ tile of every
 // (q block, head) is combined across its contributing kv blocks in a fixed
-// order, highest kv block first: the first contributor stores its partial
-// into an fp32 accumulator, later ones add theirs with global reduce-adds,
-// each only after its predecessor's counter says that update is complete,
-// and the last contributor adds its partial to the accumulator, scales and
-// writes dQ in the output dtype.  The adds are read-modify-writes in global
-// memory, but their order is fixed, so results are bitwise deterministic.
+// order, highest kv block first: the compute warps stage each tile's dQ^T in
+// shared memory, and a writer warp stores it into an fp32 accumulator with
+// TMA (first contributor) or adds it with TMA bulk reduce-adds (later ones),
+// each only after its predecessor's counter says that update is complete.
+// dq_finalize_kernel then writes dQ = scale * accumulator in the output
+// dtype.  The adds are read-modify-writes in global memory, but their order
+// is fixed, so results are bitwise deterministic.
 //
 // Tiles are 128 kv rows x 128 q rows, so S^T, dP^T and dQ^T are N = 128
 // UMMAs.  TMEM (512 columns): dV, dK accumulators; S^T (then P^T packed in
-// place until dV has read it); dP^T (then, once the softmax has read it, the
-// tile's dQ^T).  dS^T goes to its own shared-memory buffer, the A operand of
-// dK and the B operand of dQ^T.  The UMMA issue order per tile t is dV(t),
-// dK(t), dQ^T(t), S^T(t+1), dP^T(t+1): each buffer hand-off is covered by the
-// GEMMs issued in between.
+// place until dV and dS have read it); dP^T (then, once the compute warps
+// have read it, the tile's dQ^T).  dS^T goes to its own shared-memory
+// buffer, the A operand of dK and the B operand of dQ^T.  The UMMA issue
+// order per tile t is dV(t), dP^T(t), [dS^T(t) ready] S^T(t+1), dK(t),
+// dQ^T(t): the compute warps' P^T(t+1) overlaps dK(t) and dQ^T(t).
 //
-// Warp roles (320 threads, one CTA per SM, persistent over work units taken
+// Warp roles (352 threads, one CTA per SM, persistent over work units taken
 // in plan order from a counter):
 //   warp 0      TMA producer: K, V per unit; Q (+ lse2 / D vectors) and dY
 //               per tile (two stages each)
 //   warp 1      TMEM allocator and single-thread UMMA issuer
 //   warps 2-9   compute warps, two per TMEM lane quarter, each on 64 of the
-//               tile's 128 q columns.  Per tile: the softmax gradient (thread
-//               = kv row: P^T, then dS^T), then the dQ^T epilogue (thread =
-//               feature: out of TMEM, into the accumulator / dQ in chain
-//               order), which overlaps the dK, dQ^T and next S^T UMMAs;
-//               dK, dV (thread = kv row) at unit end
+//               tile's 128 q columns.  Per tile: P^T (thread = kv row), the
+//               epilogue of the previous tile (dQ^T out of TMEM, thread =
+//               feature, into shared-memory staging; dK, dV at unit end),
+//               then dS^T
+//   warp 10     dQ writer: chain order, TMA store / reduce-add of the staged
+//               tile, counter release
 // Every wait is bounded; on expiry the kernel records TND_ERR_DEVICE_TIMEOUT
 // in the workspace status word and winds down instead of hanging.
 #include "ptx_sm103.cuh"
@@ -54,10 +56,10 @@ using namespace ptx;
 
 constexpr int BC = kKvBlock;            // 128 kv rows per block (UMMA M)
 constexpr int BR = kQBlock;             // 128 q rows per block (UMMA N of S^T, dP^T, dQ^T)
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kComputeWarp0 = 2;        // warps 2-9 (two per TMEM lane quarter)
 constexpr int kComputeThreads = 256;
-constexpr int kEpiWarps = 8;            // each adds 1 to a dQ chain counter per contribution
+constexpr int kWriterWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_S = 256, TM_DP = 384;   // S^T / P^T; dP^T / dQ^T
 constexpr uint32_t kColBlk = 128 * 128;       // one 64-element column block of 128 rows (16 KB)
@@ -79,7 +81,7 @@ struct Geo {
     static constexpr uint32_t OFF_DS = OFF_DY + 2 * kQTile;
     static constexpr uint32_t OFF_VEC = OFF_DS + kDsBytes;  // 2 stages
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * kVecBytes;
-    static constexpr uint32_t kNumBars = 28;
+    static constexpr uint32_t kNumBars = 30;
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = OFF_MISC + 64;
     // For HD = 64 the dQ^T UMMA has M = 128 and its A operand's second
@@ -101,7 +103,8 @@ enum : int {
     B_Q_FULL = 4,      // [2]  count 1 + tx (Q tile + lse2 / D vectors, stage t % 2)
     B_Q_EMPTY = 6,     // [2]  count 1 (commit after dK)
     B_DY_FULL = 8,     // [2]  count 1 + tx
-    B_DY_EMPTY = 10,   // [2]  count 1 (commit after dV)
+    B_DY_EMPTY = 10,   // [2]  count 2 (commit after dV and dP^T; the writer, once the dQ^T
+                       //      staged in this stage has been read)
     B_S_FULL = 12,     //      count 1 (commit)
     B_P_READY = 13,    // [2]  count 128 (per softmax half: q columns 0-63, 64-127)
     B_PV_DONE = 15,    //      count 1 (commit after dV: P^T consumed, S buffer free)
@@ -112,12 +115,51 @@ enum : int {
     B_ACC_FULL = 20,   //      count 1 (commit after the unit's last tile)
     B_ACC_FREE = 21,   //      count 256 (dK / dV read out)
     B_UNIT_FULL = 22,  // [2]  count 1
-    B_UNIT_EMPTY = 24, // [2]  count 9 (MMA + 8 compute warps)
+    B_UNIT_EMPTY = 24, // [2]  count 10 (MMA + 8 compute warps + writer)
     B_DRAIN = 26,      //      count 1 (commit)
+    B_STG_FULL = 27,   //      count 256 (dQ^T staged)
+    B_STG_FREE = 28,   //      count 1 (the writer's TMA has read the staging)
 };
 
 // misc words
 constexpr uint32_t MISC_TMEM = 0, MISC_RING = 1, MISC_ABORT = 3;
+
+#ifdef TND_TRACE
+// Diagnostic build only: a clock-stamped event log of the first kTraceCtas
+// CTAs, one ring per warp (lane 0 records): {clock64, (event << 24) | tile}.
+constexpr int kTraceCtas = 2, kTraceLen = 8192;
+__device__ unsigned long long g_trace[kTraceCtas][11][kTraceLen][2];
+__device__ unsigned int g_trace_n[kTraceCtas][11];
+__device__ unsigned long long g_cta_span[1024][2];
+__device__ __forceinline__ void trace(uint32_t ev, uint32_t k)
+{
+    if ((threadIdx.x & 31) != 0 || blockIdx.x >= kTraceCtas) return;
+    const int w = threadIdx.x >> 5;
+    const unsigned i = g_trace_n[blockIdx.x][w]++;
+    if (i < (unsigned)kTraceLen) {
+        g_trace[blockIdx.x][w][i][0] = (unsigned long long)clock64();
+        g_trace[blockIdx.x][w][i][1] = ((unsigned long long)ev << 24) | (k & 0xffffffu);
+    }
+}
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+#define TRACE(ev, k) trace((ev), (k))
+#else
+#define TRACE(ev, k) ((void)0)
+#endif
+// trace events
+enum : uint32_t {
+    EV_UNIT = 1, EV_W_QFULL, EV_W_DYFULL, EV_W_KFULL, EV_W_VFULL, EV_W_PVDONE, EV_W_DQFREE, EV_W_ACCFREE,
+    EV_W_P0, EV_W_P1, EV_W_DS, EV_I_S, EV_I_DP, EV_I_DV, EV_I_DK, EV_I_DQ,                  // MMA issuer
+    EV_C_SFULL = 20, EV_C_PDONE, EV_C_DPFULL, EV_C_DSDONE, EV_C_DQFULL, EV_C_DQFREE, EV_C_CHAIN, EV_C_EPIDONE,
+    EV_C_UNITOUT,                                                                             // compute warps
+    EV_L_Q = 40, EV_L_DY, EV_L_K, EV_L_V,                                                     // producer
+    EV_W_STG = 50, EV_W_CHAIN, EV_W_ISSUED, EV_W_READ, EV_W_WRITTEN,                          // dQ writer
+};
 
 struct Smem {
     uint8_t *base;
@@ -344,21 +386,17 @@ __device__ __forceinline__ float2 unpack_h2(uint32_t w)
     return __half22float2(h);
 }
 
-__device__ __forceinline__ void red_add_f32(float *p, float v)
+// two bf16 (low half first) to fp32: exact, by moving the bits up
+__device__ __forceinline__ float2 unpack_bf2(uint32_t w)
 {
-    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_add_s32(int *p, int v)
-{
-    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     grad_tc_kernel(const __grid_constant__ GradArgs a, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const __grid_constant__ CUtensorMap tmDY)
+                   const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmDQ)
 {
     using G_ = Geo<HD>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -385,10 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sm.bar(B_Q_FULL + i), 1);
             mbar_init(sm.bar(B_Q_EMPTY + i), 1);
             mbar_init(sm.bar(B_DY_FULL + i), 1);
-            mbar_init(sm.bar(B_DY_EMPTY + i), 1);
+            mbar_init(sm.bar(B_DY_EMPTY + i), 2);
             mbar_init(sm.bar(B_P_READY + i), 128);
             mbar_init(sm.bar(B_UNIT_FULL + i), 1);
-            mbar_init(sm.bar(B_UNIT_EMPTY + i), 1 + kEpiWarps);
+            mbar_init(sm.bar(B_UNIT_EMPTY + i), 10);
         }
         mbar_init(sm.bar(B_S_FULL), 1);
         mbar_init(sm.bar(B_PV_DONE), 1);
@@ -399,6 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(sm.bar(B_ACC_FULL), 1);
         mbar_init(sm.bar(B_ACC_FREE), kComputeThreads);
         mbar_init(sm.bar(B_DRAIN), 1);
+        mbar_init(sm.bar(B_STG_FULL), kComputeThreads);
+        mbar_init(sm.bar(B_STG_FREE), 1);
         *sm.abort_flag() = 0;
         fence_mbar_init();
     }
@@ -411,11 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmDY);
+        prefetch_tmap(&tmDQ);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm.misc() + MISC_TMEM);
+#ifdef TND_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_span[blockIdx.x][0] = global_ns();
+#endif
     uint32_t drain_arm[6] = {0, 0, 0, 0, 0, 0};   // producer: phases armed per load barrier
 
     if (warp == 0) {
@@ -437,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ui;
             if (u >= a.n_units) break;
             const UnitInfo U = unit_info(a, u);
+            TRACE(EV_UNIT, (uint32_t)u);
             if (U.ntiles == 0) continue;
             const int z_kv = (int)(U.sd.tk + (int64_t)U.jb * BC);
             // V first: its buffer frees at the previous unit's last dP^T
@@ -468,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_g2s(vec + BR * 4, a.drow + vidx, BR * 4, fb);
                 }
                 ++armed_q[s];
+                TRACE(EV_L_Q, gt);
                 if (k >= 1 && !wait_warp(sm, B_DY_EMPTY + s, k - 1, a)) {
                     ok = false;
                     break;
@@ -480,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(dyt + cb * kColBlk, &tmDY, fb, 64 * cb, h, z);
                 }
                 ++armed_dy[s];
+                TRACE(EV_L_DY, gt);
                 if (t == 0) {
                     // K after the unit's first Q / dY: its buffer frees when the
                     // previous unit's last dQ^T completes
@@ -497,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(sm.base + G_::OFF_K + cb * kColBlk, &tmK, kb, 64 * cb, U.g, z_kv);
                     }
                     if (!skip) ++armed_k;
+                    TRACE(EV_L_K, gt);
                 }
             }
             ++ku;
@@ -529,12 +577,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int KS = HD / 16;     // K steps of S^T / dP^T
             uint32_t ui = 0, ku = 0, gt = 0;
             bool ok = true;
-            // S^T(t) = K Q(t)^T into the S buffer once dV(t - 1) has read P^T(t - 1)
+            // S^T(t) = K Q(t)^T into the S buffer: dV(t - 1) has read Pd^T(t - 1)
+            // (PV_DONE) and the compute warps have read P^T(t - 1) (their
+            // DS_READY(t - 1), awaited before every S^T but a unit's first)
             auto issue_s = [&](uint32_t g, bool first) -> bool {
                 const uint32_t s = g & 1u;
                 if (!wait_poll(sm, B_Q_FULL + s, g >> 1, a)) return false;
+                TRACE(EV_W_QFULL, g);
                 if (g >= 1 && !wait_poll(sm, B_PV_DONE, g - 1, a)) return false;
+                TRACE(EV_W_PVDONE, g);
                 if (first && !wait_poll(sm, B_K_FULL, ku, a)) return false;
+                TRACE(EV_W_KFULL, g);
                 tc_fence_after();
                 const uint64_t dq = desc_at(dQ_k0, s * G_::kQTile);
 #pragma unroll
@@ -543,15 +596,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tmem + TM_S, desc_at(dK_k, off), desc_at(dq, off), idS, kk > 0);
                 }
                 mma_commit(sm.bar(B_S_FULL));
+                TRACE(EV_I_S, g);
                 return true;
             };
-            // dP^T(t) = V dY(t)^T into the dP buffer once the epilogue has read
-            // dQ^T(t - 1) out of it
-            auto issue_dp = [&](uint32_t g, bool first, bool last) -> bool {
+            // dP^T(t) = V dY(t)^T into the dP buffer once the compute warps have
+            // read dQ^T(t - 1) out of it
+            auto issue_dp = [&](uint32_t g, bool first) -> bool {
                 const uint32_t s = g & 1u;
                 if (!wait_poll(sm, B_DY_FULL + s, g >> 1, a)) return false;
+                TRACE(EV_W_DYFULL, g);
                 if (g >= 1 && !wait_poll(sm, B_DQ_FREE, g - 1, a)) return false;
+                TRACE(EV_W_DQFREE, g);
                 if (first && !wait_poll(sm, B_V_FULL, ku, a)) return false;
+                TRACE(EV_W_VFULL, g);
                 tc_fence_after();
                 const uint64_t dy = desc_at(dY_k0, s * G_::kQTile);
 #pragma unroll
@@ -560,9 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tmem + TM_DP, desc_at(dV_k, off), desc_at(dy, off), idS, kk > 0);
                 }
                 mma_commit(sm.bar(B_DP_FULL));
-                if (last) mma_commit(sm.bar(B_V_EMPTY));   // last reader of V
+                TRACE(EV_I_DP, g);
                 return true;
             };
+            // Per tile t: dV(t); dP^T(t) (a unit's first tile: before the loop);
+            // then, once dS^T(t) is ready, S^T(t + 1), dK(t), dQ^T(t).  The
+            // compute warps' P^T(t + 1) thus overlaps dK(t) and dQ^T(t).
             while (ok) {
                 int u;
                 if (!read_unit1(sm, ui, a, u)) break;
@@ -572,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (U.ntiles == 0) continue;
                 const uint32_t g0 = gt, g_end = gt + (uint32_t)U.ntiles;
                 // V arrives before K (K waits for the previous unit's last dQ^T)
-                if (!issue_dp(g0, true, g0 + 1 == g_end) || !issue_s(g0, true)) break;
+                if (!issue_dp(g0, true) || !issue_s(g0, true)) break;
                 for (uint32_t g = g0; g < g_end; ++g) {
                     const uint32_t s = g & 1u;
                     const bool first = g == g0;
@@ -580,8 +640,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    TRACE(EV_W_ACCFREE, g);
                     // dV += Pd^T dY(t): A = Pd^T (TMEM, packed), B = dY MN-major (N = HD);
-                    // the two K halves follow the two softmax halves
+                    // the two K halves follow the two softmax halves.  dV(t) comes before
+                    // dP^T(t) (a unit's first tile aside), so it waits for dY(t) itself.
+                    if (!first && !wait_poll(sm, B_DY_FULL + s, g >> 1, a)) {
+                        ok = false;
+                        break;
+                    }
                     const uint64_t dym = desc_at(dY_m0, s * G_::kQTile);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
@@ -589,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
+                        TRACE(EV_W_P0 + hf, g);
                         tc_fence_after();
 #pragma unroll
                         for (int kq = 0; kq < 4; ++kq) {
@@ -599,13 +666,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!ok) break;
                     mma_commit(sm.bar(B_PV_DONE));
-                    mma_commit(sm.bar(B_DY_EMPTY + s));
-                    // dK += dS^T Q(t): A = dS^T smem K-major, B = Q MN-major
+                    TRACE(EV_I_DV, g);
+                    if (!first && !issue_dp(g, false)) {
+                        ok = false;
+                        break;
+                    }
+                    mma_commit(sm.bar(B_DY_EMPTY + s));      // dP^T(t) and dV(t) issued: dY(t)'s readers
+                    if (g + 1 == g_end) mma_commit(sm.bar(B_V_EMPTY));   // the unit's last dP^T issued
                     if (!wait_poll(sm, B_DS_READY, g, a)) {
                         ok = false;
                         break;
                     }
+                    TRACE(EV_W_DS, g);
                     tc_fence_after();
+                    if (g + 1 < g_end && !issue_s(g + 1, false)) {
+                        ok = false;
+                        break;
+                    }
+                    // dK += dS^T Q(t): A = dS^T smem K-major, B = Q MN-major
                     const uint64_t dqm = desc_at(dQ_m0, s * G_::kQTile);
 #pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
@@ -613,19 +691,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ss(tmem + HD, desc_at(dS_k, off), desc_at(dqm, kk * 2048), idKV, (!first || kk > 0));
                     }
                     mma_commit(sm.bar(B_Q_EMPTY + s));
-                    // dQ^T = K^T dS^T into the dP buffer (the softmax has read dP^T(t)):
-                    // A = K MN-major (M = 128 features), B = dS^T MN-major (N = 128 q)
+                    TRACE(EV_I_DK, g);
+                    // dQ^T = K^T dS^T into the dP buffer (the compute warps have read
+                    // dP^T(t)): A = K MN-major (M = 128 features), B = dS^T MN-major
 #pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
                         mma_ss(tmem + TM_DP, desc_at(dK_m, kk * 2048), desc_at(dS_m, kk * 2048), idQ, kk > 0);
                     }
                     mma_commit(sm.bar(B_DQ_FULL));
+                    TRACE(EV_I_DQ, g);
                     if (g + 1 == g_end) {
                         mma_commit(sm.bar(B_ACC_FULL));
                         mma_commit(sm.bar(B_K_EMPTY));
-                    } else if (!issue_s(g + 1, false) || !issue_dp(g + 1, false, g + 2 == g_end)) {
-                        ok = false;
-                        break;
                     }
                 }
                 if (!ok) break;
@@ -639,23 +716,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < kWriterWarp) {
         // ================================================================ compute warps
         // Two warps per TMEM lane quarter: warps 2-5 take q columns 0-63 of
         // the tile, warps 6-9 columns 64-127 (the same split serves dQ^T,
         // whose TMEM columns are q rows, and dK / dV, whose columns are
-        // features).
+        // features).  Per tile t: P^T(t); the epilogue of tile t - 1 (before
+        // P^T(t) when t starts a unit); dS^T(t).
         const int quarter = warp & 3;
         const int half = (warp - kComputeWarp0) >> 2;
         const int ln = quarter * 32 + lane;                 // TMEM lane: kv row (S^T, dP^T, dK, dV) or feature (dQ^T)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const float C = a.scale * kLog2e;
+        // dS uses a separate fp16 copy of P^T: Pd^T is 0 where dropout drops a
+        // key, and a bf16 P^T doubles the rounding error of dS
+        const bool sep_p = true;
         Out *dK = reinterpret_cast<Out *>(a.dk);
         Out *dV = reinterpret_cast<Out *>(a.dv);
-        Out *dQ = reinterpret_cast<Out *>(a.dq);
         uint32_t ui = 0, ku = 0, gt = 0;
         bool ok = true;
-        // dK, dV of the unit (x scale for dK) out of TMEM; thread = kv row,
+        // dK, dV of a unit (x scale for dK) out of TMEM; thread = kv row,
         // columns [half * HD / 2, (half + 1) * HD / 2)
         auto unit_out = [&](const UnitInfo &U, bool zeros) -> bool {
             const int64_t jj = (int64_t)U.jb * BC + ln;
@@ -699,6 +779,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ku;
             return true;
         };
+        // Epilogue of tile pg (the previous tile): dQ^T out of TMEM (thread =
+        // feature ln, q rows 64 half .. + 63), the dP buffer released, the
+        // unit's dK / dV out if pg ended its unit, then dQ^T staged as fp32
+        // [64 q rows][HD] for the writer warp: rows 0-63 of the tile in the
+        // dY stage of tile pg (its readers are done), rows 64-127 in the dS^T
+        // buffer (dK(pg) and dQ^T(pg) have read it).
+        bool pend = false;
+        uint32_t pg = 0;
+        UnitInfo pU;
+        bool p_last = false;
+        auto epilogue = [&]() -> bool {
+            if (!wait_warp(sm, B_DQ_FULL, pg, a)) return false;
+            TRACE(EV_C_DQFULL, pg);
+            tc_fence_after();
+            uint32_t v[64];
+            const uint32_t dq_addr = tmem + lane_addr + TM_DP + 64 * half;
+            tmem_ld32(dq_addr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(dq_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tc_fence_before();
+            mbar_arrive(sm.bar(B_DQ_FREE));
+            TRACE(EV_C_DQFREE, pg);
+            if (p_last && !unit_out(pU, false)) return false;
+            float *stg = reinterpret_cast<float *>(
+                             sm.base + (half == 0 ? G_::OFF_DY + (pg & 1u) * G_::kQTile : G_::OFF_DS)) + ln;
+            if (ln < HD) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) stg[c * HD] = __uint_as_float(v[c]);
+            }
+            fence_async_smem();
+            mbar_arrive(sm.bar(B_STG_FULL));
+            TRACE(EV_C_EPIDONE, pg);
+            return true;
+        };
         while (ok) {
             int u;
             if (!read_unit(sm, ui, a, u)) break;
@@ -718,10 +831,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = __all_sync(0xffffffffu, keep == ~0ull);
                 KeepWin kw;
                 if (a.has_drop) keep_fetch(a, U.sd, h, qc0, (int64_t)U.jb * BC + quarter * 32, lane, kw);
+                // a unit's first S^T is issued after its first dP^T, which needs
+                // the previous tile's dQ^T read out: that epilogue goes first
+                if (t == 0 && pend) {
+                    if (!epilogue()) {
+                        ok = false;
+                        break;
+                    }
+                    pend = false;
+                }
                 if (!wait_warp(sm, B_Q_FULL + s, gt >> 1, a) || !wait_warp(sm, B_S_FULL, gt, a)) {
                     ok = false;
                     break;
                 }
+                TRACE(EV_C_SFULL, gt);
                 tc_fence_after();
                 const float *vec = reinterpret_cast<const float *>(sm.base + G_::OFF_VEC + s * G_::kVecBytes);
                 const float4 *lse4 = reinterpret_cast<const float4 *>(vec) + 16 * half;
@@ -763,29 +886,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(p[2 * c], p[2 * c + 1]);
                     }
+                    if (sep_p) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) pk[16 + c] = pack_f16(p[2 * c], p[2 * c + 1]);
-                    tmem_st32(s_addr + 32 * ch, pk);   // only this chunk's own, already read, columns
+                        for (int c = 0; c < 16; ++c) pk[16 + c] = pack_f16(p[2 * c], p[2 * c + 1]);
+                        tmem_st32(s_addr + 32 * ch, pk);   // only this chunk's own, already read, columns
+                    } else {
+                        tmem_st16(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_P_READY + half));
-                // ---- phase 2: dS^T = P^T o (z dP^T - D) into the shared-memory dS^T
-                // buffer (free: this warp waited for dQ^T(t - 1), the last reader
-                // of dS^T(t - 1), in its epilogue step of the previous tile)
+                TRACE(EV_C_PDONE, gt);
+                if (pend) {
+                    if (!epilogue()) {
+                        ok = false;
+                        break;
+                    }
+                    pend = false;
+                }
+                // ---- phase 2: dS^T = P^T o (z dP^T - D) into registers, then into the
+                // shared-memory dS^T buffer once the writer has read the staged
+                // dQ^T(t - 1) out of it.
                 if (!wait_warp(sm, B_DP_FULL, gt, a)) {
                     ok = false;
                     break;
                 }
+                TRACE(EV_C_DPFULL, gt);
                 tc_fence_after();
                 const uint32_t dp_addr = tmem + lane_addr + TM_DP + 64 * half;
-                uint8_t *row = sm.base + G_::OFF_DS + half * kColBlk + ln * 128;
+                uint32_t dsk[32];
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     uint32_t raw[32], pp[16];
                     tmem_ld32(dp_addr + 32 * ch, raw);
-                    tmem_ld16(s_addr + 32 * ch + 16, pp);
+                    tmem_ld16(s_addr + 32 * ch + (sep_p ? 16 : 0), pp);
                     const uint32_t zh = (uint32_t)(zb >> (32 * ch));
-                    uint32_t pk[16];
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         const float4 dv = dvec4[8 * ch + c4];
@@ -796,118 +931,130 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 4; ++e)
                                 dp[e] = ((zh >> (4 * c4 + e)) & 1u) ? dp[e] * a.inv_keep : 0.0f;
                         }
-                        const float2 pa = unpack_h2(pp[2 * c4]);
-                        const float2 pb = unpack_h2(pp[2 * c4 + 1]);
-                        pk[2 * c4] = pack2<BF16>(pa.x * (dp[0] - dv.x), pa.y * (dp[1] - dv.y));
-                        pk[2 * c4 + 1] = pack2<BF16>(pb.x * (dp[2] - dv.z), pb.y * (dp[3] - dv.w));
+                        float2 pa, pb;
+                        if (sep_p) {
+                            pa = unpack_h2(pp[2 * c4]);
+                            pb = unpack_h2(pp[2 * c4 + 1]);
+                        } else {
+                            pa = unpack_bf2(pp[2 * c4]);
+                            pb = unpack_bf2(pp[2 * c4 + 1]);
+                        }
+                        dsk[16 * ch + 2 * c4] = pack2<BF16>(pa.x * (dp[0] - dv.x), pa.y * (dp[1] - dv.y));
+                        dsk[16 * ch + 2 * c4 + 1] = pack2<BF16>(pb.x * (dp[2] - dv.z), pb.y * (dp[3] - dv.w));
                     }
+                }
+                if (gt >= 1 && !wait_warp(sm, B_STG_FREE, gt - 1, a)) {
+                    ok = false;
+                    break;
+                }
+                TRACE(EV_C_CHAIN, gt);
+                uint8_t *row = sm.base + G_::OFF_DS + half * kColBlk + ln * 128;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int chunk = 4 * ch + c;
-                        const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        *reinterpret_cast<uint4 *>(row + ((chunk ^ (ln & 7)) << 4)) = v;
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = make_uint4(dsk[4 * c], dsk[4 * c + 1], dsk[4 * c + 2], dsk[4 * c + 3]);
+                    *reinterpret_cast<uint4 *>(row + ((c ^ (ln & 7)) << 4)) = v;
                 }
                 fence_async_smem();
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_DS_READY));
-                // ---- phase 3: dQ^T(t) out of TMEM (thread = feature ln, q rows
-                // 64 half .. + 63 of the tile), then into the accumulator / dQ
-                const int qg = U.sd.qblk0 + qb;
-                const QBlockInfo qi = a.qblk[qg];
-                int *flag = a.flags + (int64_t)qg * a.nq + h;
-                if (!wait_warp(sm, B_DQ_FULL, gt, a)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                uint32_t v[64];
-                tmem_ld32(dp_addr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(dp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                tc_fence_before();
-                mbar_arrive(sm.bar(B_DQ_FREE));
-                // the unit's dK / dV go out before the last tile's dQ chain wait
-                if (t + 1 == U.ntiles && !unit_out(U, false)) {
-                    ok = false;
-                    break;
-                }
-                // dQ chain: position pos of npos contributors (highest kv block first)
-                const int pos = qi.jhi - U.jb, npos = qi.jhi - qi.jlo + 1;
-                if (pos > 0) {
-                    const long long t0 = clock64();
-                    while (ld_acquire_gpu(flag) < kEpiWarps * pos) {
-                        if (*sm.abort_flag()) {
-                            ok = false;
-                            break;
-                        }
-                        if (clock64() - t0 > a.wait_limit_cycles) {
-                            // detail: the awaited position and the (q block, head) counter
-                            set_status(a.status, TND_ERR_DEVICE_TIMEOUT,
-                                       0x80000000u | ((uint32_t)pos << 24) | (uint32_t)(qg * a.nq + h));
-                            *sm.abort_flag() = 1;
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!__all_sync(0xffffffffu, ok)) {
+                TRACE(EV_C_DSDONE, gt);
+                pend = true;
+                pg = gt;
+                pU = U;
+                p_last = t + 1 == U.ntiles;
+            }
+        }
+        if (ok && pend) epilogue();
+    } else {
+        // ================================================================ dQ writer
+        // For each tile, in order: once the compute warps have staged dQ^T,
+        // waits until the (q block, head) counter shows that every earlier
+        // contributor's update is complete, then stores (first contributor)
+        // or adds (later ones) the two staged 64-row halves into the fp32
+        // accumulator with TMA, releases the staging buffers once they have
+        // been read, and advances the counter once the writes are complete.
+        if (lane == 0) {
+            uint32_t ui = 0, gt = 0;
+            bool ok = true;
+            while (ok) {
+                int u;
+                if (!read_unit1(sm, ui, a, u)) break;
+                ++ui;
+                if (u < 0) break;
+                const UnitInfo U = unit_info(a, u);
+                for (int t = 0; t < U.ntiles; ++t, ++gt) {
+                    const int qb = U.qb_lo + t / G, h = U.g * G + t % G;
+                    const int qg = U.sd.qblk0 + qb;
+                    const QBlockInfo qi = a.qblk[qg];
+                    int *flag = a.flags + (int64_t)qg * a.nq + h;
+                    const int pos = qi.jhi - U.jb;
+                    if (!wait_k(sm, B_STG_FULL, gt, a)) {
                         ok = false;
                         break;
                     }
-                }
-                const int64_t qr0 = (int64_t)qb * BR + 64 * half;          // first q row of this warp
-                const int nrow = (int)max((int64_t)0, min((int64_t)64, (int64_t)U.sd.sq - qr0));
-                const int64_t stride = (int64_t)a.nq * HD;
-                const int64_t off0 = ((U.sd.tq + qr0) * a.nq + h) * (int64_t)HD + ln;
-                // (loops fully unrolled: v stays in registers)
-                if (ln < HD) {
-                    float *accp = a.dqacc + off0;
-                    Out *dqp = dQ + off0;
-                    if (npos == 1) {
+                    TRACE(EV_W_STG, gt);
+                    if (pos > 0) {
+                        const long long t0 = clock64();
+                        while (ld_acquire_gpu(flag) < pos) {
+                            if (*sm.abort_flag()) {
+                                ok = false;
+                                break;
+                            }
+                            if (clock64() - t0 > a.wait_limit_cycles) {
+                                // detail: the awaited position and the (q block, head) counter
+                                set_status(a.status, TND_ERR_DEVICE_TIMEOUT,
+                                           0x80000000u | ((uint32_t)pos << 24) | (uint32_t)(qg * a.nq + h));
+                                *sm.abort_flag() = 1;
+                                ok = false;
+                                break;
+                            }
+                            __nanosleep(32);
+                        }
+                        if (!ok) break;
+                        fence_async_global();   // the counter's acquire before the async-proxy adds
+                    }
+                    TRACE(EV_W_CHAIN, gt);
+                    const int z = (int)(U.sd.tq + (int64_t)qb * BR);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c < nrow) Elem<Out>::store(dqp + c * stride, __uint_as_float(v[c]) * a.scale);
-                    } else if (pos == 0) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c < nrow) accp[c * stride] = __uint_as_float(v[c]);
-                    } else if (pos + 1 < npos) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c < nrow) red_add_f32(accp + c * stride, __uint_as_float(v[c]));
-                    } else {
-#pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
-                            float acc[16];
-#pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                acc[c] = (c0 + c < nrow) ? __ldcg(accp + (c0 + c) * stride) : 0.0f;
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                if (c0 + c < nrow)
-                                    Elem<Out>::store(dqp + (c0 + c) * stride,
-                                                     (acc[c] + __uint_as_float(v[c0 + c])) * a.scale);
+                    for (int hs = 0; hs < 2; ++hs) {
+                        const uint8_t *stg = sm.base + (hs == 0 ? G_::OFF_DY + (gt & 1u) * G_::kQTile : G_::OFF_DS);
+                        const int64_t r0 = (int64_t)qb * BR + 64 * hs;
+                        const int rows = (int)max((int64_t)0, min((int64_t)64, (int64_t)U.sd.sq - r0));
+                        if (rows == 64) {
+                            if (pos == 0) tma_store_3d(&tmDQ, stg, 0, h, z + 64 * hs);
+                            else tma_reduce_add_3d(&tmDQ, stg, 0, h, z + 64 * hs);
+                        } else {
+                            // ragged last block of a sequence: only its own rows
+                            for (int r = 0; r < rows; ++r) {
+                                float *dst = a.dqacc + ((U.sd.tq + r0 + r) * a.nq + h) * (int64_t)HD;
+                                if (pos == 0) bulk_s2g(dst, stg + r * HD * 4, HD * 4);
+                                else bulk_reduce_add_f32(dst, stg + r * HD * 4, HD * 4);
                             }
                         }
                     }
-                }
-                if (pos + 1 < npos) {
-                    // publish: each of the 8 compute warps adds 1 to the counter
-                    // once its lanes' updates are ordered before the add (lane
-                    // fences, a warp barrier, then a release by lane 0)
+                    bulk_commit();
+                    TRACE(EV_W_ISSUED, gt);
+                    bulk_wait_read0();
+                    mbar_arrive(sm.bar(B_STG_FREE));
+                    mbar_arrive(sm.bar(B_DY_EMPTY + (gt & 1u)));
+                    TRACE(EV_W_READ, gt);
+                    bulk_wait0();
+                    fence_async_global();
                     fence_acq_rel_gpu();
-                    __syncwarp();
-                    if (lane == 0) {
-                        fence_acq_rel_gpu();
-                        red_add_s32(flag, 1);
-                    }
+                    st_relaxed_gpu(flag, pos + 1);
+                    TRACE(EV_W_WRITTEN, gt);
                 }
             }
+            bulk_wait0();
         }
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
+#ifdef TND_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_span[blockIdx.x][1] = global_ns();
+#endif
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -954,19 +1101,63 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t heads, int 
     return r == CUDA_SUCCESS;
 }
 
+// dQ accumulator [rows, heads, hd] fp32, boxes of hd features x 1 head x 64 rows (no swizzle)
+bool make_acc_map(CUtensorMap *m, const float *ptr, int64_t rows, int64_t heads, int hd)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * 4, (cuuint64_t)(heads * hd * 4)};
+    cuuint32_t box[3] = {(cuuint32_t)hd, 1, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <bool BF16, int HD>
 cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
 {
-    CUtensorMap mq, mk, mv, mdy;
+    CUtensorMap mq, mk, mv, mdy, mdq;
     if (!make_map(&mq, a.q, a.tq, a.nq, HD, BR, BF16) || !make_map(&mk, a.k, a.tkv, a.nkv, HD, BC, BF16) ||
-        !make_map(&mv, a.v, a.tkv, a.nkv, HD, BC, BF16) || !make_map(&mdy, a.dy, a.tq, a.nq, HD, BR, BF16))
+        !make_map(&mv, a.v, a.tkv, a.nkv, HD, BC, BF16) || !make_map(&mdy, a.dy, a.tq, a.nq, HD, BR, BF16) ||
+        !make_acc_map(&mdq, a.dqacc, a.tq, a.nq, HD))
         return cudaErrorInvalidValue;
     const int grid = std::min<int>(a.num_sms, a.n_units);
     constexpr uint32_t smem = Geo<HD>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel<BF16, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    grad_tc_kernel<BF16, HD><<<grid, kThreads, smem, s>>>(a, mq, mk, mv, mdy);
+    grad_tc_kernel<BF16, HD><<<grid, kThreads, smem, s>>>(a, mq, mk, mv, mdy, mdq);
     return cudaGetLastError();
+}
+
+// dQ = scale * accumulator in the output dtype, 4 features per thread; rows
+// of q blocks that no kv block reaches get zeros.
+template <typename Out>
+__global__ void __launch_bounds__(256) dq_finalize_kernel(GradArgs a)
+{
+    const int per_row = a.d / 4;
+    const int64_t total = (int64_t)a.n_qblk * a.nq * kQBlock * per_row;
+    Out *dQ = reinterpret_cast<Out *>(a.dq);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t rowid = e / per_row;                      // (q block * nq + h) * 128 + row
+        const int c4 = (int)(e - rowid * per_row);
+        const int64_t blk = rowid / kQBlock;
+        const int rr = (int)(rowid - blk * kQBlock);
+        const int qg = (int)(blk / a.nq), h = (int)(blk - (int64_t)qg * a.nq);
+        const int2 qr = a.qblk_rows[qg];
+        const SeqDesc sd = a.seqs[qr.x];
+        const int64_t i = (int64_t)qr.y + rr;
+        if (i >= sd.sq) continue;
+        const int64_t off = ((sd.tq + i) * a.nq + h) * (int64_t)a.d + 4 * c4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.qblk[qg].jlo >= 0) v = __ldcs(reinterpret_cast<const float4 *>(a.dqacc + off));
+        uint2 pk;
+        pk.x = pack2<std::is_same<Out, __nv_bfloat16>::value>(v.x * a.scale, v.y * a.scale);
+        pk.y = pack2<std::is_same<Out, __nv_bfloat16>::value>(v.z * a.scale, v.w * a.scale);
+        *reinterpret_cast<uint2 *>(dQ + off) = pk;
+    }
 }
 
 }  // namespace
@@ -982,4 +1173,27 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s)
+{
+    const int64_t total = (int64_t)a.n_qblk * a.nq * kQBlock * (a.d / 4);
+    if (total == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)a.num_sms * 8);
+    if (a.dtype == TND_BF16) dq_finalize_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else dq_finalize_kernel<__half><<<(unsigned)blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace tnd
+
+#ifdef TND_TRACE
+// Diagnostic build only: copies the event log out (and clears it).
+extern "C" int tnd_debug_trace(unsigned long long *events, unsigned int *counts, unsigned long long *spans)
+{
+    using namespace tnd;
+    if (cudaMemcpyFromSymbol(events, g_trace, sizeof(g_trace)) != cudaSuccess) return 1;
+    if (cudaMemcpyFromSymbol(counts, g_trace_n, sizeof(g_trace_n)) != cudaSuccess) return 1;
+    if (cudaMemcpyFromSymbol(spans, g_cta_span, sizeof(g_cta_span)) != cudaSuccess) return 1;
+    static unsigned int zero[kTraceCtas][11] = {};
+    return cudaMemcpyToSymbol(g_trace_n, zero, sizeof(zero)) != cudaSuccess;
+}
+#endif

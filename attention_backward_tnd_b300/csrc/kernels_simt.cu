@@ -156,8 +156,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 // included).  Eight lanes share a row and read dY and O with 16-byte loads
 // when the row length allows it (D * sizeof(T) a multiple of 16); a warp
 // covers four rows per step.  With tc_state it also zeroes the dQ chain
-// counters and the dQ rows of q blocks that no kv block reaches (the
-// tensor-core gradient writes every other dQ row).
+// counters of the tensor-core gradient.
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float dot16(const uint4 &x, const uint4 &y)
@@ -229,19 +228,6 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t nflags = (int64_t)a.n_qblk * a.nq;
     for (int64_t e = tid; e < nflags; e += nthreads) a.flags[e] = 0;
-    // dQ rows of q blocks without contributors (rare): zero, one (q block,
-    // head) per thread
-    const int per_row = a.d * (int)sizeof(T) / 16;
-    for (int64_t e = tid; e < nflags; e += nthreads) {
-        const int qg = (int)(e / a.nq), h = (int)(e - (int64_t)qg * a.nq);
-        if (a.qblk[qg].jlo >= 0) continue;
-        const int2 qr = a.qblk_rows[qg];
-        const SeqDesc sd = a.seqs[qr.x];
-        for (int64_t i = qr.y; i < min((int64_t)qr.y + kQBlock, (int64_t)sd.sq); ++i) {
-            uint4 *dst = reinterpret_cast<uint4 *>((T *)a.dq + ((sd.tq + i) * a.nq + h) * a.d);
-            for (int c = 0; c < per_row; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------

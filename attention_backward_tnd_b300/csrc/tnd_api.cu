@@ -33,9 +33,9 @@ struct ProfEntry {
     cudaEvent_t start, stop;
 };
 const char *kKindNames[] = {"fwd_simt", "grad_prepass", "grad_dkdv_simt", "grad_dq_simt",
-                            "grad_sink_reduce", "grad_tc_main"};
+                            "grad_sink_reduce", "grad_tc_main", "grad_dq_finalize"};
 constexpr int kNumKinds = sizeof(kKindNames) / sizeof(kKindNames[0]);
-enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC };
+enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN };
 std::vector<ProfEntry> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 constexpr size_t kProfCap = 4096;
@@ -741,6 +741,8 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
     if (tc) {
         if (timed(K_TC, s, [&] { return launch_grad_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         HOST_LAP(5);
+        if (timed(K_FIN, s, [&] { return launch_dq_finalize(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+        HOST_LAP(6);
     } else {
         if (timed(K_DKDV, s, [&] { return launch_grad_dkdv_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
         if (timed(K_DQ, s, [&] { return launch_grad_dq_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;

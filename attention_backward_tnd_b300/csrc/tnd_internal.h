@@ -110,7 +110,7 @@ struct GradArgs {
     const GradUnit *units;
     int32_t n_units;
     const QBlockInfo *qblk;   // [n_qblk]
-    int32_t *flags;           // [n_qblk][Nq] dQ chain counters (8 per completed contribution)
+    int32_t *flags;           // [n_qblk][Nq] dQ chain counters (completed contributions)
     float *dqacc;             // [Tq][Nq][D] fp32 partial sums
     int64_t wait_limit_cycles;
     int32_t num_sms;
@@ -137,8 +137,8 @@ struct FwdArgs {
 
 // Kernel launchers (each returns the CUDA error of its launch).
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s);
-// Gradient prepass: the blocked per-row vectors; with tc_state also the dQ
-// chain counters (zeroed) and the dQ rows of q blocks no kv block reaches.
+// Gradient prepass: the blocked per-row vectors; with tc_state also zeroes
+// the dQ chain counters.
 cudaError_t launch_prepass(const GradArgs &a, bool tc_state, cudaStream_t s);
 cudaError_t launch_grad_dkdv_simt(const GradArgs &a, cudaStream_t s);
 cudaError_t launch_grad_dq_simt(const GradArgs &a, cudaStream_t s);
@@ -146,6 +146,9 @@ cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s);
 // Tensor-core gradient (bf16/fp16, D = 64 or 128); false where it does not apply.
 bool grad_tc_supported(int dtype, int d);
 cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s);
+// dQ = scale * accumulated partial sums, in the output dtype; zero for q
+// blocks that no kv block reaches (tensor-core path).
+cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s);
 
 // The gradient call behind tnd_attn_grad.  pinned_upload = false copies the
 // plan from pageable host memory and allocates nothing (the library's pinned
