@@ -22,9 +22,10 @@
 // is fixed, so results are bitwise deterministic.
 //
 // Tiles are 128 kv rows x 128 q rows, so S^T, dP^T and dQ^T are N = 128
-// UMMAs.  TMEM (512 columns): dV, dK accumulators; S^T (then P^T packed in
-// place until dV and dS have read it); dP^T (then, once the compute warps
-// have read it, the tile's dQ^T).  dS^T goes to its own shared-memory
+// UMMAs.  TMEM (512 columns): dV, dK accumulators; S^T (then Pd^T packed
+// in place until dV has read it; the compute warps keep P^T in registers
+// for dS^T); dP^T (then, once the compute warps have read it, the tile's
+// dQ^T).  dS^T goes to its own shared-memory
 // buffer, the A operand of dK and the B operand of dQ^T.  The UMMA issue
 // order per tile t is dV(t), dP^T(t), [dS^T(t) ready] S^T(t+1), dK(t),
 // dQ^T(t): the compute warps' P^T(t+1) overlaps dK(t) and dQ^T(t).
@@ -380,18 +381,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return BF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
-__device__ __forceinline__ float2 unpack_h2(uint32_t w)
-{
-    __half2 h = *reinterpret_cast<__half2 *>(&w);
-    return __half22float2(h);
-}
-
-// two bf16 (low half first) to fp32: exact, by moving the bits up
-__device__ __forceinline__ float2 unpack_bf2(uint32_t w)
-{
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
 template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     grad_tc_kernel(const __grid_constant__ GradArgs a, const __grid_constant__ CUtensorMap tmQ,
@@ -728,9 +717,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ln = quarter * 32 + lane;                 // TMEM lane: kv row (S^T, dP^T, dK, dV) or feature (dQ^T)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const float C = a.scale * kLog2e;
-        // dS uses a separate fp16 copy of P^T: Pd^T is 0 where dropout drops a
-        // key, and a bf16 P^T doubles the rounding error of dS
-        const bool sep_p = true;
         Out *dK = reinterpret_cast<Out *>(a.dk);
         Out *dV = reinterpret_cast<Out *>(a.dv);
         uint32_t ui = 0, ku = 0, gt = 0;
@@ -793,20 +779,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_warp(sm, B_DQ_FULL, pg, a)) return false;
             TRACE(EV_C_DQFULL, pg);
             tc_fence_after();
-            uint32_t v[64];
+            // two 32-column halves, staged one after the other (fewer live
+            // registers: the softmax's P^T is held across this epilogue); the dP
+            // buffer is released once both have been read
             const uint32_t dq_addr = tmem + lane_addr + TM_DP + 64 * half;
-            tmem_ld32(dq_addr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(dq_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            tc_fence_before();
-            mbar_arrive(sm.bar(B_DQ_FREE));
-            TRACE(EV_C_DQFREE, pg);
-            if (p_last && !unit_out(pU, false)) return false;
             float *stg = reinterpret_cast<float *>(
                              sm.base + (half == 0 ? G_::OFF_DY + (pg & 1u) * G_::kQTile : G_::OFF_DS)) + ln;
-            if (ln < HD) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) stg[c * HD] = __uint_as_float(v[c]);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
+                tmem_ld32(dq_addr + 32 * hh, v);
+                if (hh == 1) {
+                    tc_fence_before();
+                    mbar_arrive(sm.bar(B_DQ_FREE));
+                    TRACE(EV_C_DQFREE, pg);
+                }
+                if (ln < HD) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) stg[(32 * hh + c) * HD] = __uint_as_float(v[c]);
+                }
             }
+            if (p_last && !unit_out(pU, false)) return false;
             fence_async_smem();
             mbar_arrive(sm.bar(B_STG_FULL));
             TRACE(EV_C_EPIDONE, pg);
@@ -850,49 +843,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4 *lse4 = reinterpret_cast<const float4 *>(vec) + 16 * half;
                 const float4 *dvec4 = reinterpret_cast<const float4 *>(vec + BR) + 16 * half;
                 const uint64_t zb = a.has_drop ? keep_transpose(kw, lane) : ~0ull;
-                // ---- phase 1: P^T from S^T.  Each 32-column chunk of S^T is replaced
-                // by Pd^T = P^T o z packed in the dtype (16 columns, the dV operand)
-                // and P^T packed as fp16 (16 columns, read back for dS; the next
-                // S^T is issued only after DS_READY, so it survives until then)
+                // ---- phase 1: P^T from S^T, kept in registers (fp32) for dS; each
+                // 32-column chunk of S^T gets Pd^T = P^T o z packed in the dtype in
+                // its first 16 columns (the dV operand)
                 const uint32_t s_addr = tmem + lane_addr + TM_S + 64 * half;
+                float p[64];
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     uint32_t raw[32];
                     tmem_ld32(s_addr + 32 * ch, raw);
-                    float p[32];
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         const float4 l = lse4[8 * ch + c4];
-                        p[4 * c4 + 0] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 0]), C, -l.x));
-                        p[4 * c4 + 1] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 1]), C, -l.y));
-                        p[4 * c4 + 2] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 2]), C, -l.z));
-                        p[4 * c4 + 3] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 3]), C, -l.w));
+                        p[32 * ch + 4 * c4 + 0] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 0]), C, -l.x));
+                        p[32 * ch + 4 * c4 + 1] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 1]), C, -l.y));
+                        p[32 * ch + 4 * c4 + 2] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 2]), C, -l.z));
+                        p[32 * ch + 4 * c4 + 3] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 3]), C, -l.w));
                     }
                     if (!full) {
                         const uint32_t kh = (uint32_t)(keep >> (32 * ch));
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) p[c] = ((kh >> c) & 1u) ? p[c] : 0.0f;
+                        for (int c = 0; c < 32; ++c) p[32 * ch + c] = ((kh >> c) & 1u) ? p[32 * ch + c] : 0.0f;
                     }
-                    uint32_t pk[32];
+                    uint32_t pk[16];
                     if (a.has_drop) {
                         const uint32_t zh = (uint32_t)(zb >> (32 * ch));
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const float z0 = ((zh >> (2 * c)) & 1u) ? a.inv_keep : 0.0f;
                             const float z1 = ((zh >> (2 * c + 1)) & 1u) ? a.inv_keep : 0.0f;
-                            pk[c] = pack2<BF16>(p[2 * c] * z0, p[2 * c + 1] * z1);
+                            pk[c] = pack2<BF16>(p[32 * ch + 2 * c] * z0, p[32 * ch + 2 * c + 1] * z1);
                         }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(p[2 * c], p[2 * c + 1]);
+                        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(p[32 * ch + 2 * c], p[32 * ch + 2 * c + 1]);
                     }
-                    if (sep_p) {
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) pk[16 + c] = pack_f16(p[2 * c], p[2 * c + 1]);
-                        tmem_st32(s_addr + 32 * ch, pk);   // only this chunk's own, already read, columns
-                    } else {
-                        tmem_st16(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                    }
+                    tmem_st16(s_addr + 32 * ch, pk);   // only this chunk's own, already read, columns
                 }
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_P_READY + half));
@@ -904,7 +890,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     pend = false;
                 }
-                // ---- phase 2: dS^T = P^T o (z dP^T - D) into registers, then into the
+                // ---- phase 2: dS^T = P^T o (z dP^T - D) (P^T from registers: Pd^T is 0
+                // where dropout drops a key) into registers, then into the
                 // shared-memory dS^T buffer once the writer has read the staged
                 // dQ^T(t - 1) out of it.
                 if (!wait_warp(sm, B_DP_FULL, gt, a)) {
@@ -917,9 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t dsk[32];
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t raw[32], pp[16];
+                    uint32_t raw[32];
                     tmem_ld32(dp_addr + 32 * ch, raw);
-                    tmem_ld16(s_addr + 32 * ch + (sep_p ? 16 : 0), pp);
                     const uint32_t zh = (uint32_t)(zb >> (32 * ch));
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
@@ -931,16 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 4; ++e)
                                 dp[e] = ((zh >> (4 * c4 + e)) & 1u) ? dp[e] * a.inv_keep : 0.0f;
                         }
-                        float2 pa, pb;
-                        if (sep_p) {
-                            pa = unpack_h2(pp[2 * c4]);
-                            pb = unpack_h2(pp[2 * c4 + 1]);
-                        } else {
-                            pa = unpack_bf2(pp[2 * c4]);
-                            pb = unpack_bf2(pp[2 * c4 + 1]);
-                        }
-                        dsk[16 * ch + 2 * c4] = pack2<BF16>(pa.x * (dp[0] - dv.x), pa.y * (dp[1] - dv.y));
-                        dsk[16 * ch + 2 * c4 + 1] = pack2<BF16>(pb.x * (dp[2] - dv.z), pb.y * (dp[3] - dv.w));
+                        const float *pc = p + 32 * ch + 4 * c4;
+                        dsk[16 * ch + 2 * c4] = pack2<BF16>(pc[0] * (dp[0] - dv.x), pc[1] * (dp[1] - dv.y));
+                        dsk[16 * ch + 2 * c4 + 1] = pack2<BF16>(pc[2] * (dp[2] - dv.z), pc[3] * (dp[3] - dv.w));
                     }
                 }
                 if (gt >= 1 && !wait_warp(sm, B_STG_FREE, gt - 1, a)) {
@@ -1015,8 +994,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     TRACE(EV_W_CHAIN, gt);
                     const int z = (int)(U.sd.tq + (int64_t)qb * BR);
+                    // the half staged in the dS^T buffer first, as its own bulk
+                    // group: the compute warps wait for that buffer to be read
 #pragma unroll
-                    for (int hs = 0; hs < 2; ++hs) {
+                    for (int i = 0; i < 2; ++i) {
+                        const int hs = 1 - i;
                         const uint8_t *stg = sm.base + (hs == 0 ? G_::OFF_DY + (gt & 1u) * G_::kQTile : G_::OFF_DS);
                         const int64_t r0 = (int64_t)qb * BR + 64 * hs;
                         const int rows = (int)max((int64_t)0, min((int64_t)64, (int64_t)U.sd.sq - r0));
@@ -1031,11 +1013,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 else bulk_reduce_add_f32(dst, stg + r * HD * 4, HD * 4);
                             }
                         }
+                        bulk_commit();
                     }
-                    bulk_commit();
                     TRACE(EV_W_ISSUED, gt);
-                    bulk_wait_read0();
+                    bulk_wait_read1();                              // the dS^T-buffer half
                     mbar_arrive(sm.bar(B_STG_FREE));
+                    bulk_wait_read0();                              // the dY-stage half
                     mbar_arrive(sm.bar(B_DY_EMPTY + (gt & 1u)));
                     TRACE(EV_W_READ, gt);
                     bulk_wait0();
