@@ -33,9 +33,9 @@ struct ProfEntry {
     cudaEvent_t start, stop;
 };
 const char *kKindNames[] = {"fwd_simt", "grad_prepass", "grad_dkdv_simt", "grad_dq_simt",
-                            "grad_sink_reduce", "grad_tc_main", "grad_dq_finalize"};
+                            "grad_sink_reduce", "grad_tc_main", "grad_dq_finalize", "fwd_tc"};
 constexpr int kNumKinds = sizeof(kKindNames) / sizeof(kKindNames[0]);
-enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN };
+enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN, K_FWD_TC };
 std::vector<ProfEntry> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 constexpr size_t kProfCap = 4096;
@@ -166,7 +166,8 @@ struct Plan {
     std::vector<int2> q_items, kv_items;
     std::vector<GradUnit> units;
     std::vector<QBlockInfo> qblk;
-    std::vector<int2> qblk_rows;  // (b, first row) of every 64-row q block, in global order
+    std::vector<int2> qblk_rows;  // (b, first row) of every 128-row q block, in global order
+    std::vector<int2> fwd_units;  // tensor-core forward: (q block, head), longest kv range first
     int64_t kept_pairs = 0;       // summed over sequences and query heads
     std::vector<unsigned char> image;  // status words + plan arrays, as copied to the workspace
 };
@@ -258,6 +259,16 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
     // block together.  Under a causal mask the low kv blocks carry the most
     // tiles; interleaving the heads makes the last units handed out similar in
     // size instead of one head's largest blocks, which keeps the tail short.
+    // forward units: every (q block, head), q blocks with the longest kv
+    // range first (heads of a q block together)
+    {
+        std::vector<int> order(pl.qblk.size());
+        for (size_t q = 0; q < order.size(); ++q) order[q] = (int)q;
+        auto span = [&](int q) { return pl.qblk[q].jlo < 0 ? 0 : pl.qblk[q].jhi - pl.qblk[q].jlo + 1; };
+        std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return span(x) > span(y); });
+        for (int q : order)
+            for (int64_t h = 0; h < p.nq; ++h) pl.fwd_units.push_back(make_int2(q, (int)h));
+    }
     std::stable_sort(gw.begin(), gw.end(), [](const GroupWork &x, const GroupWork &y) { return x.work > y.work; });
     for (const GroupWork &w : gw) {
         for (GradUnit u : seq_units[w.b]) {
@@ -274,7 +285,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-    size_t seqs = 0, q_items = 0, kv_items = 0, units = 0, qblk = 0, qblk_rows = 0;  // offsets of the
+    size_t seqs = 0, q_items = 0, kv_items = 0, units = 0, qblk = 0, qblk_rows = 0, fwd_units = 0;  // offsets of the
     size_t plan_end = 0;                                                                // copied plan
     size_t flags = 0, lse2 = 0, drow = 0, sinkrow = 0, dqacc = 0, total = 0;
 };
@@ -294,6 +305,7 @@ void plan_offsets(const Plan &pl, Layout &L, size_t &off)
     L.units = take(pl.units.size() * sizeof(GradUnit));
     L.qblk = take(pl.qblk.size() * sizeof(QBlockInfo));
     L.qblk_rows = take(pl.qblk_rows.size() * sizeof(int2));
+    L.fwd_units = take(pl.fwd_units.size() * sizeof(int2));
     L.plan_end = off;
 }
 
@@ -336,6 +348,7 @@ void build_image(Plan &pl)
     put(L.units, pl.units.data(), pl.units.size() * sizeof(GradUnit));
     put(L.qblk, pl.qblk.data(), pl.qblk.size() * sizeof(QBlockInfo));
     put(L.qblk_rows, pl.qblk_rows.data(), pl.qblk_rows.size() * sizeof(int2));
+    put(L.fwd_units, pl.fwd_units.data(), pl.fwd_units.size() * sizeof(int2));
 }
 
 // Plans depend only on the sequence table, head counts and the mask; calls
@@ -410,6 +423,7 @@ DeviceInfo device_info()
 }
 
 bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
+bool use_fwd_tc(const Problem &p) { return g_opt.grad_path == 0 && fwd_tc_supported(p.dtype, (int)p.d); }
 
 // Pinned host staging of plan uploads.  A copy from pageable host memory may
 // make the runtime wait for the stream before it starts, so a run call would
@@ -614,7 +628,7 @@ tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int
     tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode, has_drop != 0,
                              has_sink != 0, p);
     if (st != TND_OK) return st;
-    auto plp = get_plan(p, false);
+    auto plp = get_plan(p, fwd_tc_supported(p.dtype, (int)p.d));
     *ws_size = layout_for(p, *plp, false, false).total;
     return TND_OK;
 }
@@ -631,7 +645,8 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, (const void *)out, (const void *)smax, (const void *)ssum})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
-    auto plp = get_plan(p, false);
+    const bool tc_layout = fwd_tc_supported(p.dtype, (int)p.d);
+    auto plp = get_plan(p, tc_layout);
     const Plan &pl = *plp;
     const Layout L = layout_for(p, pl, false, false);
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
@@ -640,6 +655,7 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
     if (st != TND_OK) return st;
     FwdArgs a{};
     fill_common(a, p, pl, L, ws);
+    char *w = (char *)ws;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -648,7 +664,21 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
     a.o = out;
     a.smax = smax;
     a.ssum = ssum;
-    if (timed(K_FWD, s, [&] { return launch_fwd_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    a.mask_bytes = (mask_bits_total(p) + 7) / 8;
+    a.qblk = (const QBlockInfo *)(w + L.qblk);
+    a.qblk_rows = (const int2 *)(w + L.qblk_rows);
+    a.fwd_units = (const int2 *)(w + L.fwd_units);
+    a.n_fwd_units = (int32_t)pl.fwd_units.size();
+    {
+        const DeviceInfo di = device_info();
+        a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)di.clock_khz;
+        a.num_sms = di.num_sms;
+    }
+    if (tc_layout && use_fwd_tc(p)) {
+        if (timed(K_FWD_TC, s, [&] { return launch_fwd_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    } else {
+        if (timed(K_FWD, s, [&] { return launch_fwd_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
+    }
     return TND_OK;
 }
 

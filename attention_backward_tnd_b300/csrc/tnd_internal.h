@@ -133,10 +133,21 @@ struct FwdArgs {
     const SeqDesc *seqs;
     const int2 *q_items;
     int32_t n_q_items;
+    // tensor-core forward
+    int64_t mask_bytes;
+    const QBlockInfo *qblk;   // kv block range of every 128-row q block
+    const int2 *qblk_rows;    // (b, first row) per q block
+    const int2 *fwd_units;    // (q block, head), longest kv range first
+    int32_t n_fwd_units;
+    int64_t wait_limit_cycles;
+    int32_t num_sms;
 };
 
 // Kernel launchers (each returns the CUDA error of its launch).
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s);
+// Tensor-core forward (bf16/fp16, D = 64 or 128); false where it does not apply.
+bool fwd_tc_supported(int dtype, int d);
+cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t s);
 // Gradient prepass: the blocked per-row vectors; with tc_state also zeroes
 // the dQ chain counters.
 cudaError_t launch_prepass(const GradArgs &a, bool tc_state, cudaStream_t s);
