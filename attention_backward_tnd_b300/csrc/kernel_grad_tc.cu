@@ -1115,31 +1115,42 @@ cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// dQ = scale * accumulator in the output dtype, 4 features per thread; rows
-// of q blocks that no kv block reaches get zeros.
+// dQ = scale * accumulator in the output dtype, one block per (128-row q
+// block, head), 4 features per thread with all loads of a thread issued
+// first; rows of q blocks that no kv block reaches get zeros.
 template <typename Out>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(GradArgs a)
 {
-    const int per_row = a.d / 4;
-    const int64_t total = (int64_t)a.n_qblk * a.nq * kQBlock * per_row;
+    const int qg = blockIdx.x, h = blockIdx.y;
+    const int2 qr = a.qblk_rows[qg];
+    const SeqDesc sd = a.seqs[qr.x];
+    const bool covered = a.qblk[qg].jlo >= 0;
+    const int rows = min(BR, sd.sq - qr.y);
+    const int per_row = a.d / 4;                    // 16 or 32 float4 per row
+    const int total = rows * per_row;
     Out *dQ = reinterpret_cast<Out *>(a.dq);
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t rowid = e / per_row;                      // (q block * nq + h) * 128 + row
-        const int c4 = (int)(e - rowid * per_row);
-        const int64_t blk = rowid / kQBlock;
-        const int rr = (int)(rowid - blk * kQBlock);
-        const int qg = (int)(blk / a.nq), h = (int)(blk - (int64_t)qg * a.nq);
-        const int2 qr = a.qblk_rows[qg];
-        const SeqDesc sd = a.seqs[qr.x];
-        const int64_t i = (int64_t)qr.y + rr;
-        if (i >= sd.sq) continue;
-        const int64_t off = ((sd.tq + i) * a.nq + h) * (int64_t)a.d + 4 * c4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.qblk[qg].jlo >= 0) v = __ldcs(reinterpret_cast<const float4 *>(a.dqacc + off));
-        uint2 pk;
-        pk.x = pack2<std::is_same<Out, __nv_bfloat16>::value>(v.x * a.scale, v.y * a.scale);
-        pk.y = pack2<std::is_same<Out, __nv_bfloat16>::value>(v.z * a.scale, v.w * a.scale);
-        *reinterpret_cast<uint2 *>(dQ + off) = pk;
+    constexpr int kBatch = 8;
+    for (int e0 = threadIdx.x; e0 < total; e0 += kBatch * 256) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int e = e0 + 256 * k;
+            const int rr = e / per_row, c4 = e - rr * per_row;
+            const int64_t off = ((sd.tq + qr.y + rr) * a.nq + h) * (int64_t)a.d + 4 * c4;
+            v[k] = (covered && e < total) ? __ldcs(reinterpret_cast<const float4 *>(a.dqacc + off))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int e = e0 + 256 * k;
+            if (e >= total) break;
+            const int rr = e / per_row, c4 = e - rr * per_row;
+            const int64_t off = ((sd.tq + qr.y + rr) * a.nq + h) * (int64_t)a.d + 4 * c4;
+            uint2 pk;
+            pk.x = pack2<std::is_same<Out, __nv_bfloat16>::value>(v[k].x * a.scale, v[k].y * a.scale);
+            pk.y = pack2<std::is_same<Out, __nv_bfloat16>::value>(v[k].z * a.scale, v[k].w * a.scale);
+            *reinterpret_cast<uint2 *>(dQ + off) = pk;
+        }
     }
 }
 
@@ -1158,11 +1169,10 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
 
 cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s)
 {
-    const int64_t total = (int64_t)a.n_qblk * a.nq * kQBlock * (a.d / 4);
-    if (total == 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)a.num_sms * 8);
-    if (a.dtype == TND_BF16) dq_finalize_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(a);
-    else dq_finalize_kernel<__half><<<(unsigned)blocks, 256, 0, s>>>(a);
+    if (a.n_qblk == 0) return cudaSuccess;
+    const dim3 grid((unsigned)a.n_qblk, (unsigned)a.nq);
+    if (a.dtype == TND_BF16) dq_finalize_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+    else dq_finalize_kernel<__half><<<grid, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

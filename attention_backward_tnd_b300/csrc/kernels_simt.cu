@@ -153,10 +153,10 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 
 // ---------------------------------------------------------------------------
 // gradient prepass: writes the blocked per-row vectors (padded rows
-// included).  Eight lanes share a row and read dY and O with 16-byte loads
-// when the row length allows it (D * sizeof(T) a multiple of 16); a warp
-// covers four rows per step.  With tc_state it also zeroes the dQ chain
-// counters of the tensor-core gradient.
+// included), one block per (128-row q block, head).  Eight lanes share a
+// row and read dY and O with 16-byte loads when the row length allows it
+// (D * sizeof(T) a multiple of 16, at most 256 bytes).  With tc_state it
+// also zeroes the dQ chain counters of the tensor-core gradient.
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float dot16(const uint4 &x, const uint4 &y)
@@ -172,62 +172,66 @@ __device__ __forceinline__ float dot16(const uint4 &x, const uint4 &y)
 template <typename T>
 __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
 {
-    const int lane = threadIdx.x & 31, sub = lane & 7;
-    const int64_t nrows = (int64_t)a.n_qblk * a.nq * kQBlock;
+    // block (q block qg, head h): 128 rows, 32 groups of 8 lanes, 4 rows per
+    // group with all their loads issued before the sums
+    const int qg = blockIdx.x, h = blockIdx.y;
+    const int lane = threadIdx.x & 31, sub = lane & 7, grp = threadIdx.x >> 3;
+    const int2 qr = a.qblk_rows[qg];
+    const SeqDesc sd = a.seqs[qr.x];
     const T *dY = (const T *)a.dy, *O = (const T *)a.o;
-    const int64_t warps = (int64_t)gridDim.x * 8;
-    const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const bool vec = ((a.d * (int)sizeof(T)) & 15) == 0;
-    const int chunks = a.d * (int)sizeof(T) / 16;          // 16-byte chunks per row
-    for (int64_t w0 = wid * 4; w0 < nrows; w0 += warps * 4) {
-        const int64_t w = w0 + (lane >> 3);                 // this lane's row of the four
-        bool have = w < nrows;
-        int64_t r = 0;
-        int h = 0;
-        bool live_row = false;
-        if (have) {
-            const int64_t blk = w / kQBlock;                // q block * nq + h
-            const int rr = (int)(w - blk * kQBlock);
-            const int qg = (int)(blk / a.nq);
-            h = (int)(blk - (int64_t)qg * a.nq);
-            const int2 qr = a.qblk_rows[qg];
-            const SeqDesc sd = a.seqs[qr.x];
-            const int64_t i = (int64_t)qr.y + rr;
-            live_row = i < sd.sq;
-            r = (sd.tq + i) * a.nq + h;
-        }
-        float dot = 0.0f;
-        if (live_row) {
-            if (vec) {
-                const uint4 *y4 = reinterpret_cast<const uint4 *>(dY + r * a.d);
-                const uint4 *o4 = reinterpret_cast<const uint4 *>(O + r * a.d);
-                for (int c = sub; c < chunks; c += 8) dot += dot16<T>(__ldg(y4 + c), __ldg(o4 + c));
-            } else {
-                for (int c = sub; c < a.d; c += 8) dot += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
+    const bool vec = ((a.d * (int)sizeof(T)) & 15) == 0 && a.d * (int)sizeof(T) <= 256;
+    const int chunks = a.d * (int)sizeof(T) / 16;          // 16-byte chunks per row (at most 16)
+    float dot[4];
+    if (vec) {
+        uint4 y[4][2], o[4][2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t i = (int64_t)qr.y + grp + 32 * k;
+            const int64_t r = (sd.tq + i) * a.nq + h;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = sub + 8 * e;
+                const bool ld = i < sd.sq && c < chunks;
+                y[k][e] = ld ? __ldg(reinterpret_cast<const uint4 *>(dY + r * a.d) + c) : make_uint4(0, 0, 0, 0);
+                o[k][e] = ld ? __ldg(reinterpret_cast<const uint4 *>(O + r * a.d) + c) : make_uint4(0, 0, 0, 0);
             }
         }
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-        if (have && sub == 0) {
-            if (!live_row) {
-                a.drow[w] = 0.0f;
-                a.lse2[w] = INFINITY;
-                if (a.has_sink) a.sinkrow[w] = 0.0f;
-            } else {
-                const float m = a.smax[r * 8], l = a.ssum[r * 8];
-                const bool live = l > 0.0f;
-                a.drow[w] = dot;
-                a.lse2[w] = live ? m * kLog2e + lg2(l) : INFINITY;
-                if (a.has_sink) a.sinkrow[w] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * dot : 0.0f;
-            }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dot[k] = dot16<T>(y[k][0], o[k][0]) + dot16<T>(y[k][1], o[k][1]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t i = (int64_t)qr.y + grp + 32 * k;
+            const int64_t r = (sd.tq + i) * a.nq + h;
+            dot[k] = 0.0f;
+            if (i < sd.sq)
+                for (int c = sub; c < a.d; c += 8) dot[k] += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
         }
     }
-    if (!tc_state) return;
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    const int64_t nflags = (int64_t)a.n_qblk * a.nq;
-    for (int64_t e = tid; e < nflags; e += nthreads) a.flags[e] = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float d = dot[k];
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        const int rr = grp + 32 * k;
+        const int64_t i = (int64_t)qr.y + rr;
+        const int64_t w = ((int64_t)qg * a.nq + h) * kQBlock + rr;   // blocked vector index
+        if (sub != 0) continue;
+        if (i >= sd.sq) {
+            a.drow[w] = 0.0f;
+            a.lse2[w] = INFINITY;
+            if (a.has_sink) a.sinkrow[w] = 0.0f;
+        } else {
+            const int64_t r = (sd.tq + i) * a.nq + h;
+            const float m = a.smax[r * 8], l = a.ssum[r * 8];
+            const bool live = l > 0.0f;
+            a.drow[w] = d;
+            a.lse2[w] = live ? m * kLog2e + lg2(l) : INFINITY;
+            if (a.has_sink) a.sinkrow[w] = live ? -ex2((a.sink[h] - m) * kLog2e) / l * d : 0.0f;
+        }
+    }
+    if (tc_state && threadIdx.x == 0) a.flags[(int64_t)qg * a.nq + h] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -467,11 +471,9 @@ template <typename T, int DMAX> struct DqLaunch {
 template <typename T, int DMAX> struct PrepassLaunch {
     static cudaError_t run(const GradArgs &a, bool tc_state, cudaStream_t s)
     {
-        const int64_t rows = (int64_t)a.n_qblk * a.nq * kQBlock;
-        if (rows == 0) return cudaSuccess;
-        // 8 warps per block, 4 rows per warp step; up to 8 resident blocks per SM
-        const int64_t blocks = std::min<int64_t>((rows + 31) / 32, (int64_t)a.num_sms * 8);
-        prepass_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(a, tc_state ? 1 : 0);
+        if (a.n_qblk == 0) return cudaSuccess;
+        const dim3 grid((unsigned)a.n_qblk, (unsigned)a.nq);
+        prepass_kernel<T><<<grid, 256, 0, s>>>(a, tc_state ? 1 : 0);
         return cudaGetLastError();
     }
 };
