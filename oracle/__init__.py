@@ -49,6 +49,9 @@ class _Problem(ctypes.Structure):
         ("sink", ctypes.POINTER(ctypes.c_double)),
         ("h_lo", ctypes.c_int64), ("h_hi", ctypes.c_int64),
         ("row_lo", ctypes.POINTER(ctypes.c_int64)),
+        ("atten_mask", ctypes.POINTER(ctypes.c_uint8)),
+        ("mask_rows", ctypes.c_int64), ("mask_cols", ctypes.c_int64),
+        ("prefix", ctypes.POINTER(ctypes.c_int64)),
     ]
 
 
@@ -70,6 +73,8 @@ def bind(path: str):
     cdll.ora_keep_bit.restype = ctypes.c_int
     cdll.ora_mask_base.argtypes = [P(_Problem), ctypes.c_int64]
     cdll.ora_mask_base.restype = ctypes.c_int64
+    cdll.ora_keep_at.argtypes = [P(_Problem)] + [ctypes.c_int64] * 5
+    cdll.ora_keep_at.restype = ctypes.c_int
     return cdll
 
 
@@ -101,13 +106,16 @@ class Problem:
 
     ``heads`` = (h_lo, h_hi) restricts the computation to those query heads;
     ``row_lo`` (one int per sequence) skips query rows i < row_lo[b].
+    ``atten_mask`` is the [S1Max, S2Max] attention-mask matrix (nonzero masks)
+    for sparseMode 0 / 1; ``prefix`` the per-sequence prefix N for mode 6.
     """
 
     def __init__(self, cu_q: Sequence[int], cu_kv: Sequence[int], nq: int, nkv: int, d: int,
                  scale: float, keep_prob: float = 1.0, pre_tokens: int = 2147483647,
                  next_tokens: int = 2147483647, sparse_mode: int = 0,
                  drop_mask: Optional[np.ndarray] = None, sink: Optional[np.ndarray] = None,
-                 heads: Optional[Sequence[int]] = None, row_lo: Optional[Sequence[int]] = None):
+                 heads: Optional[Sequence[int]] = None, row_lo: Optional[Sequence[int]] = None,
+                 atten_mask: Optional[np.ndarray] = None, prefix: Optional[Sequence[int]] = None):
         self.cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
         self.cu_kv = np.ascontiguousarray(cu_kv, dtype=np.int64)
         self.nq, self.nkv, self.d = int(nq), int(nkv), int(d)
@@ -115,6 +123,19 @@ class Problem:
         self.drop_mask = None if drop_mask is None else np.ascontiguousarray(drop_mask, dtype=np.uint8)
         self.sink = None if sink is None else np.ascontiguousarray(sink, dtype=np.float64)
         self.row_lo = None if row_lo is None else np.ascontiguousarray(row_lo, dtype=np.int64)
+        self.atten_mask = None if atten_mask is None else np.ascontiguousarray(atten_mask, dtype=np.uint8)
+        self.prefix = None if prefix is None else np.ascontiguousarray(prefix, dtype=np.int64)
+        if sparse_mode == 1 and self.atten_mask is None:
+            raise ValueError("sparseMode 1 needs the attention-mask matrix")
+        if sparse_mode == 6 and (self.prefix is None or self.prefix.size != len(cu_q) - 1):
+            raise ValueError("sparseMode 6 needs one prefix value per sequence")
+        if self.atten_mask is not None:
+            if self.atten_mask.ndim != 2:
+                raise ValueError("the attention-mask matrix is two-dimensional")
+            sq_max = int(np.max(np.diff(np.asarray(cu_q)))) if len(cu_q) > 1 else 0
+            skv_max = int(np.max(np.diff(np.asarray(cu_kv)))) if len(cu_kv) > 1 else 0
+            if self.atten_mask.shape[0] < sq_max or self.atten_mask.shape[1] < skv_max:
+                raise ValueError("the attention-mask matrix must cover the longest sequences")
         h_lo, h_hi = (0, self.nq) if heads is None else heads
         self._c = _Problem(
             len(self.cu_q) - 1,
@@ -126,7 +147,13 @@ class Problem:
             else self.drop_mask.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
             _dptr(self.sink), int(h_lo), int(h_hi),
             ctypes.POINTER(ctypes.c_int64)() if self.row_lo is None
-            else self.row_lo.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+            else self.row_lo.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            ctypes.POINTER(ctypes.c_uint8)() if self.atten_mask is None
+            else self.atten_mask.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+            0 if self.atten_mask is None else self.atten_mask.shape[0],
+            0 if self.atten_mask is None else self.atten_mask.shape[1],
+            ctypes.POINTER(ctypes.c_int64)() if self.prefix is None
+            else self.prefix.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
 
     @property
     def tq(self) -> int:
@@ -150,6 +177,13 @@ def problem_from_workload(wl, drop_mask=None, sink=None, **kw) -> Problem:
     return Problem(wl.cu_q, wl.cu_kv, wl.nq, wl.nkv, wl.d, wl.scale, wl.keep_prob,
                    wl.pre_tokens, wl.next_tokens, wl.sparse_mode, drop_mask,
                    None if sink is None else np.asarray(sink, dtype=np.float64), **kw)
+
+
+def keep_at(p: Problem, b: int, i: int, j: int) -> bool:
+    """The oracle's keep rule for (sequence b, row i, column j), mask and prefix included."""
+    sq = int(p.cu_q[b + 1] - p.cu_q[b])
+    skv = int(p.cu_kv[b + 1] - p.cu_kv[b])
+    return bool(lib().ora_keep_at(ctypes.byref(p._c), b, sq, skv, i, j))
 
 
 def keep(mode: int, pre: int, nxt: int, sq: int, skv: int, i: int, j: int) -> bool:

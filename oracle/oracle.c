@@ -41,8 +41,20 @@
  *     and dropout applied as P*z, d(sum dY*O)/ds_ij = p_ij (z_ij dP_ij - D_i).
  *   - sparseMode 3 keeps j <= i + (Skv - Sq) (lower triangle anchored at the
  *     bottom-right vertex); mode 2 keeps j <= i (top-left vertex); mode 4 keeps
- *     -preTokens <= j - i <= nextTokens; mode 0 (no attention-mask tensor) keeps
- *     everything and ignores preTokens/nextTokens.
+ *     -preTokens <= j - i <= nextTokens; mode 0 without an attention-mask
+ *     tensor keeps everything and ignores preTokens/nextTokens.
+ *   - attenMaskOptional [UnpadGrad, parameters; ScoreV2, parameters: 1 masks,
+ *     0 keeps] is one [S1Max, S2Max] matrix (the longest query and key
+ *     sequence) shared by every sequence and head, indexed by the in-sequence
+ *     row i and column j.  Mode 1 keeps where it is 0; mode 0 with the matrix
+ *     keeps where it is 0 and inside the preTokens/nextTokens band (the
+ *     parameters section: the part between preTokens and nextTokens is
+ *     computed); modes 2, 3, 4 and 6 take the pages' compressed matrices,
+ *     which only restate their index rules, so the matrix is not read there.
+ *   - mode 6 (prefix) keeps j <= i + (Skv - Sq) (the bottom-right lower
+ *     triangle, the upper part of the compressed matrix) or j < N_b, the
+ *     sequence's prefixOptional value (the lower part: the first N_b columns
+ *     kept for every row).
  *   - keep-bit of (b, h, i, j) sits at flat index
  *     base_b + (h*Sq_b + i)*Skv_b + j, base_b = sum_{b'<b} Nq*Sq_b'*Skv_b',
  *     byte = index >> 3, bit = index & 7 (least significant bit first).
@@ -71,6 +83,11 @@ typedef struct ora_problem {
     /* selection: heads [h_lo, h_hi) and rows i >= row_lo[b] (NULL = all rows) */
     int64_t h_lo, h_hi;
     const int64_t *row_lo;
+    /* attenMaskOptional [mask_rows][mask_cols], nonzero masks (NULL = none);
+     * prefixOptional [B] (NULL = none) */
+    const uint8_t *atten_mask;
+    int64_t mask_rows, mask_cols;
+    const int64_t *prefix;
 } ora_problem;
 
 /* sparseMode predicate; [UnpadGrad, parameters: sparseMode]. */
@@ -83,6 +100,23 @@ int ora_keep(int64_t mode, int64_t pre, int64_t next, int64_t sq, int64_t skv,
     case 3: return j <= i + (skv - sq);                /* rightDownCausal        */
     case 4: return (j - i >= -pre) && (j - i <= next); /* band                   */
     default: return 0;
+    }
+}
+
+/* Whether (b, i, j) is kept: the sparseMode rule with the attention-mask
+ * matrix and the prefix where the mode uses them [UnpadGrad, parameters:
+ * sparseMode, attenMaskOptional, prefixOptional]. */
+int ora_keep_at(const ora_problem *p, int64_t b, int64_t sq, int64_t skv, int64_t i, int64_t j)
+{
+    const int64_t mode = p->sparse_mode;
+    const int masked = p->atten_mask != NULL && p->atten_mask[i * p->mask_cols + j] != 0;
+    switch (mode) {
+    case 0:
+        if (p->atten_mask == NULL) return 1;
+        return !masked && (j - i >= -p->pre_tokens) && (j - i <= p->next_tokens);
+    case 1: return !masked;
+    case 6: return j <= i + (skv - sq) || j < p->prefix[b];
+    default: return ora_keep(mode, p->pre_tokens, p->next_tokens, sq, skv, i, j);
     }
 }
 
@@ -131,7 +165,7 @@ static void row_scores(const ora_problem *p, const double *q, const double *k,
     const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
     const double *qi = q + ((tq + i) * p->Nq + h) * D;
     for (int64_t j = 0; j < skv; ++j) {
-        kept[j] = (unsigned char)ora_keep(p->sparse_mode, p->pre_tokens, p->next_tokens, sq, skv, i, j);
+        kept[j] = (unsigned char)ora_keep_at(p, b, sq, skv, i, j);
         s[j] = kept[j] ? p->scale * dot(qi, k + ((tk + j) * p->Nkv + g) * D, D) : 0.0;
     }
 }
@@ -235,7 +269,7 @@ static double grad_ds(const ora_problem *p, const double *q, const double *k, co
     const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
     const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
     *pz_out = 0.0;
-    if (!ora_keep(p->sparse_mode, p->pre_tokens, p->next_tokens, sq, skv, i, j) || !(l > 0.0)) return 0.0;
+    if (!ora_keep_at(p, b, sq, skv, i, j) || !(l > 0.0)) return 0.0;
     const int64_t r = (tq + i) * p->Nq + h;
     const double *kj = k + ((tk + j) * p->Nkv + g) * D, *vj = v + ((tk + j) * p->Nkv + g) * D;
     const double s = p->scale * dot(q + r * D, kj, D);

@@ -13,10 +13,19 @@ import numpy as np
 import torch
 
 
-def mask_matrix(mode: int, pre: int, nxt: int, sq: int, skv: int) -> np.ndarray:
+def mask_matrix(mode: int, pre: int, nxt: int, sq: int, skv: int, atten_mask=None,
+                prefix_n: int = 0) -> np.ndarray:
     """Explicit keep matrix [sq, skv] built from the verbal definitions of
-    sparseMode (aclnnFlashAttentionUnpaddingScoreGrad, parameters section)."""
+    sparseMode, attenMaskOptional and prefixOptional
+    (aclnnFlashAttentionUnpaddingScoreGrad, parameters section)."""
     ones = np.ones((sq, skv), dtype=bool)
+    if mode == 0 and atten_mask is not None:   # the matrix, inside the preTokens/nextTokens band
+        band = np.tril(ones, k=min(nxt, skv + 1)) & np.triu(ones, k=-min(pre, sq + 1))
+        return band & (np.asarray(atten_mask)[:sq, :skv] == 0)
+    if mode == 1:                      # the full attention-mask matrix: nonzero masks
+        return np.asarray(atten_mask)[:sq, :skv] == 0
+    if mode == 6:                      # bottom-right lower triangle, plus the first N columns
+        return np.tril(ones, k=skv - sq) | (np.arange(skv)[None, :] < prefix_n)
     if mode == 0:                      # no attention mask: everything takes part
         return ones
     if mode == 2:                      # lower triangle from the top-left vertex
@@ -38,7 +47,8 @@ def random_bits(rng, shapes, p_keep=0.7):
 
 
 def autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, *, mode=0, pre=2**31 - 1,
-                       nxt=2**31 - 1, bits=None, keep_prob=1.0, sink=None):
+                       nxt=2**31 - 1, bits=None, keep_prob=1.0, sink=None, atten_mask=None,
+                       prefix=None):
     """Textbook attention per (sequence, head) in torch fp64, differentiated by
     autograd.  Returns dict of numpy arrays: out, smax, ssum, dq, dk, dv, dsink."""
     G = nq // nkv
@@ -56,7 +66,8 @@ def autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, *, mode=0, p
         sq, skv = int(cu_q[b + 1]) - tq, int(cu_kv[b + 1]) - tk
         if sq == 0:
             continue
-        keep = torch.tensor(mask_matrix(mode, pre, nxt, sq, skv))
+        keep = torch.tensor(mask_matrix(mode, pre, nxt, sq, skv, atten_mask,
+                                        0 if prefix is None else int(prefix[b])))
         for h in range(nq):
             g = h // G
             qb = Q[tq:tq + sq, h, :]

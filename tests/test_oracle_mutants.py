@@ -29,6 +29,11 @@ MUTANTS = {
     "gqa_interleaved_heads": ("const int64_t G = p->Nq / p->Nkv, g = h / G, D = p->D;",
                               "const int64_t G = p->Nq / p->Nkv, g = h % p->Nkv, D = p->D;"),
     "band_exclusive_edge": ("(j - i >= -pre) && (j - i <= next)", "(j - i > -pre) && (j - i <= next)"),
+    "atten_mask_transposed": ("p->atten_mask[i * p->mask_cols + j]", "p->atten_mask[j * p->mask_cols + i]"),
+    "atten_mask_mode0_without_band": (
+        "return !masked && (j - i >= -p->pre_tokens) && (j - i <= p->next_tokens);", "return !masked;"),
+    "prefix_inclusive": ("j < p->prefix[b]", "j <= p->prefix[b]"),
+    "prefix_top_left_anchor": ("case 6: return j <= i + (skv - sq)", "case 6: return j <= i"),
 }
 
 
@@ -43,6 +48,11 @@ def _pin_suite(ora):
         pins.test_dropout_bit_layout_bruteforce(ora)
         pins.test_ds_row_sums(ora, True)
         pins.test_gqa_equals_repeated_mha(ora)
+        for mode, pre, nxt in [(1, pins.INF, pins.INF), (0, 3, 1)]:
+            pins.test_atten_mask_predicate_matches_explicit_matrix(ora, mode, pre, nxt, 5, 9)
+        pins.test_prefix_predicate_matches_explicit_matrix(ora, 5, 9)
+        for ci in range(len(pins.MASK_CASES)):
+            pins.test_masked_forward_and_grad_match_autograd(ora, ci)
     except AssertionError:
         return False
     return True

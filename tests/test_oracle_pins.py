@@ -91,6 +91,124 @@ def test_mask_mode_equivalences(ora):
 
 
 # --------------------------------------------------------------------------
+# attention-mask matrix (sparseMode 0 / 1) and prefix (sparseMode 6)
+# --------------------------------------------------------------------------
+
+def _keep_grid(ora, p, b):
+    sq = int(p.cu_q[b + 1] - p.cu_q[b])
+    skv = int(p.cu_kv[b + 1] - p.cu_kv[b])
+    return np.array([[ora.keep_at(p, b, i, j) for j in range(skv)] for i in range(sq)],
+                    dtype=bool).reshape(sq, skv)
+
+
+@pytest.mark.parametrize("mode,pre,nxt", [(1, INF, INF), (0, INF, INF), (0, 3, 1), (0, 0, 4)])
+@pytest.mark.parametrize("sq,skv", [(7, 7), (5, 9), (9, 5), (1, 6)])
+def test_atten_mask_predicate_matches_explicit_matrix(ora, mode, pre, nxt, sq, skv):
+    rng = np.random.default_rng(sq * 31 + skv)
+    # the matrix is [S1Max, S2Max]; the second sequence is the longest one
+    amask = (rng.random((sq + 2, skv + 3)) < 0.4).astype(np.uint8) * rng.integers(1, 256, (sq + 2, skv + 3),
+                                                                                 dtype=np.uint8)
+    cu_q, cu_kv = [0, sq, 2 * sq + 2], [0, skv, 2 * skv + 3]
+    p = _problem(ora, cu_q, cu_kv, 1, 1, 4, 1.0, sparse_mode=mode, pre_tokens=pre, next_tokens=nxt,
+                 atten_mask=amask)
+    for b, (a, c) in enumerate([(sq, skv), (sq + 2, skv + 3)]):
+        np.testing.assert_array_equal(_keep_grid(ora, p, b), mask_matrix(mode, pre, nxt, a, c, amask))
+
+
+@pytest.mark.parametrize("sq,skv", [(7, 7), (5, 9), (9, 5), (4, 1)])
+def test_prefix_predicate_matches_explicit_matrix(ora, sq, skv):
+    prefixes = [0, 1, skv // 2, skv]
+    cu_q = np.arange(len(prefixes) + 1) * sq
+    cu_kv = np.arange(len(prefixes) + 1) * skv
+    p = _problem(ora, cu_q, cu_kv, 1, 1, 4, 1.0, sparse_mode=6, prefix=prefixes)
+    for b, n in enumerate(prefixes):
+        np.testing.assert_array_equal(_keep_grid(ora, p, b), mask_matrix(6, INF, INF, sq, skv, prefix_n=n))
+
+
+def test_atten_mask_and_prefix_special_cases(ora):
+    """Degenerate matrices and prefixes reduce to the plain modes."""
+    s = 9
+    cu = [0, s]
+    zero = np.zeros((s, s), np.uint8)
+    upper = np.triu(np.ones((s, s), np.uint8), k=1)
+    plain = {m: _keep_grid(ora, _problem(ora, cu, cu, 1, 1, 4, 1.0, sparse_mode=m), 0) for m in (0, 3)}
+    band = _keep_grid(ora, _problem(ora, cu, cu, 1, 1, 4, 1.0, sparse_mode=4, pre_tokens=2, next_tokens=1), 0)
+    grid = lambda **kw: _keep_grid(ora, _problem(ora, cu, cu, 1, 1, 4, 1.0, **kw), 0)
+    np.testing.assert_array_equal(grid(sparse_mode=1, atten_mask=zero), plain[0])
+    np.testing.assert_array_equal(grid(sparse_mode=1, atten_mask=upper), plain[3])
+    np.testing.assert_array_equal(grid(sparse_mode=0, atten_mask=zero, pre_tokens=2, next_tokens=1), band)
+    np.testing.assert_array_equal(grid(sparse_mode=0, atten_mask=upper, pre_tokens=INF, next_tokens=INF),
+                                  plain[3])
+    np.testing.assert_array_equal(grid(sparse_mode=6, prefix=[0]), plain[3])
+    np.testing.assert_array_equal(grid(sparse_mode=6, prefix=[s]), plain[0])
+    # prefix 3 on a 9 x 9 sequence: the 45 causal pairs plus, in row i, the prefix columns right of i
+    n = int(grid(sparse_mode=6, prefix=[3]).sum())
+    assert n == s * (s + 1) // 2 + sum(max(0, 3 - (i + 1)) for i in range(s))
+
+
+MASK_CASES = [
+    # seqlens_q, seqlens_kv, nq, nkv, mode, pre, nxt, prefix, dropout, sink
+    ([5, 9], [5, 9], 2, 2, 1, INF, INF, None, False, False),
+    ([6, 3], [9, 4], 4, 2, 1, INF, INF, None, True, True),
+    ([7, 8], [7, 8], 2, 1, 0, 3, 2, None, False, True),
+    ([6, 9], [6, 9], 2, 2, 6, INF, INF, [2, 4], False, False),
+    ([5, 4, 7], [8, 4, 7], 2, 1, 6, INF, INF, [0, 4, 3], True, True),
+]
+
+
+def _mask_case(ora, ci):
+    sq, skv, nq, nkv, mode, pre, nxt, prefix, drop, sink = MASK_CASES[ci]
+    d = 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(300 + ci, sq, skv, nq, nkv, d)
+    scale = scale_for(d) * 1.7
+    amask = None
+    if mode in (0, 1):
+        amask = (rng.random((max(sq), max(skv))) < 0.35).astype(np.uint8)
+        amask[0, :] = 1                         # a fully masked row
+    bits, packed, kp = None, None, 1.0
+    if drop:
+        bits, packed = random_bits(rng, [(nq, a, b) for a, b in zip(sq, skv)], 0.75)
+        kp = 0.75
+    snk = rng.standard_normal(nq) if sink else None
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, keep_prob=kp, pre_tokens=pre, next_tokens=nxt,
+                 sparse_mode=mode, drop_mask=packed, sink=snk, atten_mask=amask, prefix=prefix)
+    ref = autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, mode=mode, pre=pre, nxt=nxt,
+                             bits=bits, keep_prob=kp, sink=snk, atten_mask=amask, prefix=prefix)
+    return p, (q, k, v, dy), ref
+
+
+@pytest.mark.parametrize("ci", range(len(MASK_CASES)))
+def test_masked_forward_and_grad_match_autograd(ora, ci):
+    p, (q, k, v, dy), ref = _mask_case(ora, ci)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-12)
+    fin = np.isfinite(ref["smax"])
+    np.testing.assert_array_equal(np.isfinite(smax), fin)
+    np.testing.assert_allclose(smax[fin], ref["smax"][fin], rtol=1e-13, atol=1e-13)
+    dq, dk, dv, dsink = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-11, err_msg=name)
+    if ref["dsink"] is not None:
+        np.testing.assert_allclose(dsink, ref["dsink"], rtol=1e-10, atol=1e-11)
+
+
+def test_masked_grad_matches_central_differences(ora):
+    p, (q, k, v, dy), _ = _mask_case(ora, 1)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, _, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    h, rng = 1e-6, np.random.default_rng(9)
+    for name, arr, g in (("q", q, dq), ("k", k, dk)):
+        for _ in range(10):
+            idx = tuple(rng.integers(0, n) for n in arr.shape)
+            a1, a2 = arr.copy(), arr.copy()
+            a1[idx] += h
+            a2[idx] -= h
+            f = lambda a: float(np.sum(ora.fwd(p, *((a, k, v) if name == "q" else (q, a, v)))[0] * dy))
+            fd = (f(a1) - f(a2)) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
+# --------------------------------------------------------------------------
 # dropout keep-bit layout
 # --------------------------------------------------------------------------
 
