@@ -49,22 +49,23 @@ def lib():
             raise RuntimeError(f"CUDA library {LIB_PATH} is missing; build it with "
                                "attention_backward_tnd_b300.build.build()")
         L = ctypes.CDLL(LIB_PATH)
-        ws_args = [_int, _i64, _i64p, _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _int, _int,
-                   ctypes.POINTER(ctypes.c_uint64)]
+        ws_args = [_int, _i64, _i64p, _i64p, _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _int, _int,
+                   _int, ctypes.POINTER(ctypes.c_uint64)]
         L.tnd_attn_fwd_workspace_size.argtypes = ws_args
         L.tnd_attn_grad_workspace_size.argtypes = ws_args
-        L.tnd_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64, _i64, _i64, _f64,
-                                   _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64, _vp]
-        L.tnd_attn_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64,
-                                    _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _u64, _vp]
+        L.tnd_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64p, _i64, _i64,
+                                   _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64, _vp]
+        L.tnd_attn_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p,
+                                    _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                    _vp, _u64, _vp]
         L.tnd_attn_device_status.argtypes = [_vp, _u64, _vp]
         L.tnd_status_string.argtypes = [_int]
         L.tnd_status_string.restype = ctypes.c_char_p
         L.tnd_attn_set_option.argtypes = [_int, _i64]
         L.tnd_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                             _i64p, _int, ctypes.POINTER(ctypes.c_int), _int]
-        L.tnd_attn_grad_plan.argtypes = [_i64, _i64p, _i64p, _i64, _i64, _i64, _i64, _i64, _i64p, _i64, _i64p,
-                                         _i64p]
+        L.tnd_attn_grad_plan.argtypes = [_i64, _i64p, _i64p, _i64p, _i64, _i64, _i64, _i64, _i64, _int, _i64p,
+                                         _i64, _i64p, _i64p]
         L.tnd_attn_grad_static_ws.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p,
                                               _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp,
                                               _vp, _vp]
@@ -91,43 +92,57 @@ def _p(a: np.ndarray):
     return a.ctypes.data_as(_i64p)
 
 
+def _pre(prefix):
+    """Host prefix array (int64) or None, kept alive by the caller."""
+    return None if prefix is None else _cu(prefix)
+
+
+def _pp(arr):
+    return None if arr is None else _p(arr)
+
+
 # --- one-to-one wrappers of the C entry points --------------------------------------------
 
-def tnd_attn_fwd_workspace_size(dtype, batch, cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value,
-                                keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_sink):
-    cq, ck, out = _cu(cu_q), _cu(cu_kv), ctypes.c_uint64(0)
-    st = lib().tnd_attn_fwd_workspace_size(dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim,
+def tnd_attn_fwd_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value,
+                                keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_atten_mask,
+                                has_sink):
+    cq, ck, pf, out = _cu(cu_q), _cu(cu_kv), _pre(prefix), ctypes.c_uint64(0)
+    st = lib().tnd_attn_fwd_workspace_size(dtype, batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, head_dim,
                                            scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                                           int(has_drop_mask), int(has_sink), ctypes.byref(out))
+                                           int(has_drop_mask), int(has_atten_mask), int(has_sink),
+                                           ctypes.byref(out))
     return st, out.value
 
 
-def tnd_attn_grad_workspace_size(dtype, batch, cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value,
-                                 keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_sink):
-    cq, ck, out = _cu(cu_q), _cu(cu_kv), ctypes.c_uint64(0)
-    st = lib().tnd_attn_grad_workspace_size(dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim,
-                                            scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                                            int(has_drop_mask), int(has_sink), ctypes.byref(out))
+def tnd_attn_grad_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value,
+                                 keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_atten_mask,
+                                 has_sink):
+    cq, ck, pf, out = _cu(cu_q), _cu(cu_kv), _pre(prefix), ctypes.c_uint64(0)
+    st = lib().tnd_attn_grad_workspace_size(dtype, batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num,
+                                            head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                            int(has_drop_mask), int(has_atten_mask), int(has_sink),
+                                            ctypes.byref(out))
     return st, out.value
 
 
-def tnd_attn_fwd(query, key, value, drop_mask, sink, dtype, batch, cu_q, cu_kv, head_num, kv_head_num, head_dim,
-                 scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, attention_out, softmax_max,
-                 softmax_sum, workspace, workspace_size, stream):
-    cq, ck = _cu(cu_q), _cu(cu_kv)
-    return lib().tnd_attn_fwd(query, key, value, drop_mask, sink, dtype, batch, _p(cq), _p(ck), head_num,
-                              kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                              attention_out, softmax_max, softmax_sum, workspace, workspace_size, stream)
+def tnd_attn_fwd(query, key, value, drop_mask, atten_mask, sink, dtype, batch, cu_q, cu_kv, prefix, head_num,
+                 kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, attention_out,
+                 softmax_max, softmax_sum, workspace, workspace_size, stream):
+    cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
+    return lib().tnd_attn_fwd(query, key, value, drop_mask, atten_mask, sink, dtype, batch, _p(cq), _p(ck),
+                              _pp(pf), head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens,
+                              next_tokens, sparse_mode, attention_out, softmax_max, softmax_sum, workspace,
+                              workspace_size, stream)
 
 
-def tnd_attn_grad(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink, dtype, batch,
-                  cu_q, cu_kv, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens,
-                  sparse_mode, dq, dk, dv, dsink, workspace, workspace_size, stream):
-    cq, ck = _cu(cu_q), _cu(cu_kv)
-    return lib().tnd_attn_grad(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink,
-                               dtype, batch, _p(cq), _p(ck), head_num, kv_head_num, head_dim, scale_value,
-                               keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv, dsink, workspace,
-                               workspace_size, stream)
+def tnd_attn_grad(query, key, value, dy, drop_mask, atten_mask, softmax_max, softmax_sum, attention_in, sink, dtype,
+                  batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens,
+                  next_tokens, sparse_mode, dq, dk, dv, dsink, workspace, workspace_size, stream):
+    cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
+    return lib().tnd_attn_grad(query, key, value, dy, drop_mask, atten_mask, softmax_max, softmax_sum,
+                               attention_in, sink, dtype, batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num,
+                               head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv,
+                               dsink, workspace, workspace_size, stream)
 
 
 def tnd_attn_grad_static_ws(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink, dtype,
@@ -174,17 +189,19 @@ def tnd_attn_profile_read(reset: bool = False):
     return {names[i].decode(): (ms[i], n[i]) for i in range(count.value)}
 
 
-def tnd_attn_grad_plan(batch, cu_q, cu_kv, head_num, kv_head_num, pre_tokens, next_tokens, sparse_mode):
+def tnd_attn_grad_plan(batch, cu_q, cu_kv, head_num, kv_head_num, pre_tokens, next_tokens, sparse_mode,
+                       prefix=None, has_atten_mask=False):
     """(status, units int64 [n,5] = (b, g, j, first q block, end q block), kept pairs)."""
-    cq, ck = _cu(cu_q), _cu(cu_kv)
+    cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
     n, kept = ctypes.c_int64(0), ctypes.c_int64(0)
-    st = lib().tnd_attn_grad_plan(batch, _p(cq), _p(ck), head_num, kv_head_num, pre_tokens, next_tokens,
-                                  sparse_mode, None, 0, ctypes.byref(n), ctypes.byref(kept))
+    st = lib().tnd_attn_grad_plan(batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, pre_tokens, next_tokens,
+                                  sparse_mode, int(has_atten_mask), None, 0, ctypes.byref(n), ctypes.byref(kept))
     if st != TND_OK:
         return st, None, None
     units = np.zeros((n.value, 5), dtype=np.int64)
-    st = lib().tnd_attn_grad_plan(batch, _p(cq), _p(ck), head_num, kv_head_num, pre_tokens, next_tokens,
-                                  sparse_mode, _p(units), n.value, ctypes.byref(n), ctypes.byref(kept))
+    st = lib().tnd_attn_grad_plan(batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, pre_tokens, next_tokens,
+                                  sparse_mode, int(has_atten_mask), _p(units), n.value, ctypes.byref(n),
+                                  ctypes.byref(kept))
     return st, units, kept.value
 
 
@@ -199,6 +216,16 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _check_amask(atten_mask, cu_q, cu_kv):
+    """The matrix must be a contiguous one-byte [S1Max, S2Max] tensor (the C ABI takes its pointer only)."""
+    if atten_mask is None:
+        return
+    s1 = int(np.max(np.diff(_cu(cu_q))))
+    s2 = int(np.max(np.diff(_cu(cu_kv))))
+    if tuple(atten_mask.shape) != (s1, s2) or atten_mask.element_size() != 1 or not atten_mask.is_contiguous():
+        raise ValueError(f"atten_mask must be a contiguous uint8/bool tensor of shape ({s1}, {s2})")
+
+
 def _stream():
     import torch
     return torch.cuda.current_stream().cuda_stream
@@ -206,15 +233,18 @@ def _stream():
 
 def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_prob: float = 1.0,
         pre_tokens: int = 2147483647, next_tokens: int = 2147483647, sparse_mode: int = 0, drop_mask=None,
-        sink=None, workspace=None):
-    """Forward on torch CUDA tensors: returns (out, softmax_max, softmax_sum) ([T,N,8] fp32 stats)."""
+        sink=None, workspace=None, atten_mask=None, prefix=None):
+    """Forward on torch CUDA tensors: returns (out, softmax_max, softmax_sum) ([T,N,8] fp32 stats).
+    atten_mask: uint8/bool CUDA tensor [S1Max, S2Max] (nonzero masks); prefix: host ints (sparse_mode 6)."""
     import torch
     tq, nq, d = q.shape
     nkv = k.shape[1]
     batch = len(cu_q) - 1
     dt = dtype_code(q)
-    st, ws_bytes = tnd_attn_fwd_workspace_size(dt, batch, cu_q, cu_kv, nq, nkv, d, scale, keep_prob, pre_tokens,
-                                               next_tokens, sparse_mode, drop_mask is not None, sink is not None)
+    _check_amask(atten_mask, cu_q, cu_kv)
+    st, ws_bytes = tnd_attn_fwd_workspace_size(dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob,
+                                               pre_tokens, next_tokens, sparse_mode, drop_mask is not None,
+                                               atten_mask is not None, sink is not None)
     if st != TND_OK:
         raise TndError(st, "tnd_attn_fwd_workspace_size")
     out = torch.empty_like(q)
@@ -222,19 +252,21 @@ def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_p
     ssum = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
-    st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(drop_mask), _ptr(sink), dt, batch, cu_q,
-                      cu_kv, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens, sparse_mode, out.data_ptr(),
-                      smax.data_ptr(), ssum.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
+    st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(drop_mask), _ptr(atten_mask), _ptr(sink), dt,
+                      batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens,
+                      sparse_mode, out.data_ptr(), smax.data_ptr(), ssum.data_ptr(), workspace.data_ptr(),
+                      workspace.numel(), _stream())
     if st != TND_OK:
         raise TndError(st, "tnd_attn_fwd")
     return out, smax, ssum
 
 
 def grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob=1.0, pre_tokens=2147483647,
-                         next_tokens=2147483647, sparse_mode=0, has_drop=False, has_sink=False) -> int:
-    st, n = tnd_attn_grad_workspace_size(dtype_code(q), len(cu_q) - 1, cu_q, cu_kv, q.shape[1], k.shape[1],
+                         next_tokens=2147483647, sparse_mode=0, has_drop=False, has_sink=False,
+                         has_atten_mask=False, prefix=None) -> int:
+    st, n = tnd_attn_grad_workspace_size(dtype_code(q), len(cu_q) - 1, cu_q, cu_kv, prefix, q.shape[1], k.shape[1],
                                          q.shape[2], scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                                         has_drop, has_sink)
+                                         has_drop, has_atten_mask, has_sink)
     if st != TND_OK:
         raise TndError(st, "tnd_attn_grad_workspace_size")
     return n
@@ -242,27 +274,28 @@ def grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob=1.0, pre_tokens=214
 
 def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_prob=1.0,
          pre_tokens=2147483647, next_tokens=2147483647, sparse_mode=0, drop_mask=None, sink=None,
-         workspace=None, outputs=None):
+         workspace=None, outputs=None, atten_mask=None, prefix=None):
     """Gradient on torch CUDA tensors: returns (dq, dk, dv, dsink or None)."""
     import torch
     tq, nq, d = q.shape
     nkv = k.shape[1]
     batch = len(cu_q) - 1
     dt = dtype_code(q)
+    _check_amask(atten_mask, cu_q, cu_kv)
     if workspace is None:
         n = grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                                 drop_mask is not None, sink is not None)
+                                 drop_mask is not None, sink is not None, atten_mask is not None, prefix)
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     if outputs is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dsink = torch.empty(nq, dtype=torch.float32, device=q.device) if sink is not None else None
     else:
         dq, dk, dv, dsink = outputs
-    st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(drop_mask),
+    st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(drop_mask), _ptr(atten_mask),
                        softmax_max.data_ptr(), softmax_sum.data_ptr(), out.data_ptr(), _ptr(sink), dt, batch, cu_q,
-                       cu_kv, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens, sparse_mode, dq.data_ptr(),
-                       dk.data_ptr(), dv.data_ptr(), _ptr(dsink), workspace.data_ptr(), workspace.numel(),
-                       _stream())
+                       cu_kv, prefix, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _ptr(dsink), workspace.data_ptr(),
+                       workspace.numel(), _stream())
     if st != TND_OK:
         raise TndError(st, "tnd_attn_grad")
     return dq, dk, dv, dsink

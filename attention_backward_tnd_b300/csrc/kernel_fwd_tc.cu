@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t i = U.q0 + row;                     // q row in the sequence
             const bool row_ok = i < U.sd.sq;
             int64_t lo = 1, hi = 0;                           // kept key range of the row
-            if (row_ok) key_range(a.mask, U.sd.sq, U.sd.skv, i, lo, hi);
+            if (row_ok) key_range(a.mask, U.sd.sq, U.sd.skv, U.sd.prefix, i, lo, hi);
             // running state (log2 units): m_use = max in use, m_true = row max
             float m_use = -INFINITY, m_true = -INFINITY, l = 0.0f;
             if (a.has_sink && row_ok) {
@@ -403,14 +403,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t j0 = (int64_t)(U.jlo + t) * BN;
                 uint32_t kw[5], ksh = 0;
                 if (a.has_drop) fetch_keep128(a, U.sd, U.h, i, j0, kw, ksh);
+                // attention-mask matrix bits of the row's 128 columns (all kept without one)
+                uint2 am0 = make_uint2(~0u, ~0u), am1 = am0;
+                if (a.mask.keep_q != nullptr) {
+                    if (row_ok) {
+                        const uint2 *src = reinterpret_cast<const uint2 *>(a.mask.keep_q + i * a.mask.words_q + (j0 >> 6));
+                        am0 = __ldg(src);
+                        am1 = __ldg(src + 1);
+                    } else {
+                        am0 = am1 = make_uint2(0u, 0u);
+                    }
+                }
                 if (!fwait_warp(sm, F_S_FULL + b, g >> 1, a)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * b;
-                // keep mask of the 128 columns: [lo, hi] relative to j0
-                const int64_t clo = max(lo - j0, (int64_t)0), chi = min(hi - j0, (int64_t)BN - 1);
+                // keep bits of the 128 columns: the range [lo, hi] relative to j0,
+                // and the matrix
+                uint32_t km[4];
+                {
+                    const int64_t clo = max(lo - j0, (int64_t)0), chi = min(hi - j0, (int64_t)BN - 1);
+                    const uint32_t amw[4] = {am0.x, am0.y, am1.x, am1.y};
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const int64_t l0 = clo - 32 * ch, h0 = chi - 32 * ch;
+                        km[ch] = (l0 > 31 || h0 < 0 || l0 > h0)
+                                     ? 0u
+                                     : (~0u << (l0 < 0 ? 0 : (int)l0)) & (~0u >> (31 - (h0 > 31 ? 31 : (int)h0)));
+                        km[ch] &= amw[ch];
+                    }
+                }
                 // pass 1: block max over kept columns
                 float bmax = -INFINITY;
 #pragma unroll
@@ -419,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(s_addr + 32 * ch, raw);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const int col = 32 * ch + c;
-                        if (col >= clo && col <= chi) bmax = fmaxf(bmax, __uint_as_float(raw[c]) * C);
+                        if ((km[ch] >> c) & 1u) bmax = fmaxf(bmax, __uint_as_float(raw[c]) * C);
                     }
                 }
                 // lazy rescale: only when the max in use falls more than 2^8 behind
@@ -462,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float p[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const int col = 32 * ch + c;
-                        const bool kept = col >= clo && col <= chi;
+                        const bool kept = (km[ch] >> c) & 1u;
                         p[c] = kept ? ex2(fmaf(__uint_as_float(raw[c]), C, mneg)) : 0.0f;
                         l += p[c];
                     }

@@ -272,8 +272,9 @@ __device__ __forceinline__ bool read_unit1(const Smem &sm, uint32_t ui, const Gr
     return true;
 }
 
-// Columns [c_lo, c_hi] of the 64 q rows starting at q row qc0 that keep kv
-// row jj, as a bit mask.
+// The 64 q rows starting at q row qc0 (a multiple of 64) that keep kv row
+// jj, as a bit mask: the index rule gives a range [c_lo, c_hi] of them, the
+// attention-mask matrix (when there is one) the bits of that row.
 __device__ __forceinline__ uint64_t keep_columns(const GradArgs &a, const SeqDesc &sd, int64_t qc0, int64_t jj)
 {
     if (jj >= sd.skv) return 0ull;
@@ -281,16 +282,18 @@ __device__ __forceinline__ uint64_t keep_columns(const GradArgs &a, const SeqDes
     const int64_t rows = (int64_t)sd.sq - qc0;           // valid rows from qc0 on
     if (rows - 1 < hi) hi = rows - 1;
     const MaskSpec &m = a.mask;
-    if (m.mode == 2) {
+    if (m.mode == kRuleTopLeft) {
         lo = max(lo, jj - qc0);
-    } else if (m.mode == 3) {
+    } else if (m.mode == kRuleCausal || (m.mode == kRulePrefix && jj >= sd.prefix)) {
         lo = max(lo, jj - ((int64_t)sd.skv - sd.sq) - qc0);
-    } else if (m.mode == 4) {
+    } else if (m.mode == kRuleBand) {
         lo = max(lo, jj - m.next - qc0);
         hi = min(hi, jj + m.pre - qc0);
     }
     if (lo > hi) return 0ull;
-    return (~0ull << lo) & (~0ull >> (63 - hi));
+    const uint64_t range = (~0ull << lo) & (~0ull >> (63 - hi));
+    if (m.keep_kv == nullptr) return range;
+    return range & __ldg(m.keep_kv + jj * m.words_kv + (qc0 >> 6));
 }
 
 // Dropout keep-bits of the tile, for one softmax warp: kv rows

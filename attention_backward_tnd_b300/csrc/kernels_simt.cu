@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
         l = 1.0f;
     }
     int64_t lo = 1, hi = 0;
-    if (row_ok) key_range(a.mask, sd.sq, sd.skv, i, lo, hi);
+    if (row_ok) key_range(a.mask, sd.sq, sd.skv, sd.prefix, i, lo, hi);
     int64_t ulo, uhi;
     block_union(lo, hi, ulo, uhi);
 
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 #pragma unroll
             for (int k = 0; k < DP; ++k) s += qreg[k] * Ks[c * DMAX + c4 + 4 * k];
             s = quad_sum(s);
-            if (j >= lo && j <= hi) {
+            if (j >= lo && j <= hi && matrix_keeps(a.mask, i, j)) {
                 const float mn = fmaxf(m, s);
                 const float corr = ex2(m - mn);
                 const float p = ex2(s - mn);
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
         for (int64_t qt = 0; qt < sd.sq; qt += R) {
             // does any row of this q tile keep a key of [j0, j1]?
             int64_t lo = 1, hi = 0;
-            if (qt + lane < sd.sq) key_range(a.mask, sd.sq, sd.skv, qt + lane, lo, hi);
+            if (qt + lane < sd.sq) key_range(a.mask, sd.sq, sd.skv, sd.prefix, qt + lane, lo, hi);
             const bool hit = (lo <= hi) && (hi >= j0) && (lo <= j1);
             if (!__syncthreads_or(hit)) continue;
             load_tile<T, DMAX>(Qs, Q, sd.tq, qt, sd.sq, a.nq, h, D, 1.0f);
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
                 s = quad_sum(s);
                 dp = quad_sum(dp);
                 int64_t rlo = 1, rhi = 0;
-                if (i < sd.sq) key_range(a.mask, sd.sq, sd.skv, i, rlo, rhi);
-                if (row_ok && j >= rlo && j <= rhi) {
+                if (i < sd.sq) key_range(a.mask, sd.sq, sd.skv, sd.prefix, i, rlo, rhi);
+                if (row_ok && j >= rlo && j <= rhi && matrix_keeps(a.mask, i, j)) {
                     const float p = ex2(s - lses[rr]);
                     const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
                     const float pz = p * z;
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
     const float lse = row_ok ? a.lse2[row_vec_index(sd, a.nq, h, i)] : INFINITY;
     const float Di = row_ok ? a.drow[row_vec_index(sd, a.nq, h, i)] : 0.0f;
     int64_t lo = 1, hi = 0;
-    if (row_ok) key_range(a.mask, sd.sq, sd.skv, i, lo, hi);
+    if (row_ok) key_range(a.mask, sd.sq, sd.skv, sd.prefix, i, lo, hi);
     int64_t ulo, uhi;
     block_union(lo, hi, ulo, uhi);
 
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
             }
             s = quad_sum(s);
             dp = quad_sum(dp);
-            if (j >= lo && j <= hi) {
+            if (j >= lo && j <= hi && matrix_keeps(a.mask, i, j)) {
                 const float p = ex2(s - lse);
                 const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
                 const float ds = p * (z * dp - Di);
@@ -432,6 +432,43 @@ cudaError_t dispatch(int dtype, int d, Args &&...args)
     return Launch<float, 256>::run(args...);
 }
 
+// ---------------------------------------------------------------------------
+// attention-mask matrix -> keep bits, for the tensor-core kernels
+// ---------------------------------------------------------------------------
+// One block per 64 x 64 tile of the [rows][cols] byte matrix: the tile is
+// staged in shared memory as keep flags (matrix value 0), then each warp
+// turns tile rows (keep_q: row i, bit j) or tile columns (keep_kv: row j,
+// bit i) into 64-bit words, two ballots per word.  Tiles past the matrix
+// write zero words, so every word of the padded rows is defined.
+__global__ void __launch_bounds__(256) amask_pack_kernel(const uint8_t *amask, int64_t rows, int64_t cols,
+                                                         uint64_t *keep_q, int32_t words_q, uint64_t *keep_kv,
+                                                         int32_t words_kv)
+{
+    __shared__ uint8_t tile[64][65];
+    const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+    for (int e = threadIdx.x; e < 64 * 64; e += blockDim.x) {
+        const int r = e >> 6, c = e & 63;
+        const int64_t gr = r0 + r, gc = c0 + c;
+        tile[r][c] = (gr < rows && gc < cols) ? (uint8_t)(__ldg(amask + gr * cols + gc) == 0) : (uint8_t)0;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (keep_q) {
+        for (int r = warp; r < 64; r += 8) {
+            const uint32_t lo = __ballot_sync(0xffffffffu, tile[r][lane]);
+            const uint32_t hi = __ballot_sync(0xffffffffu, tile[r][32 + lane]);
+            if (lane == 0 && r0 + r < rows) keep_q[(r0 + r) * words_q + blockIdx.x] = ((uint64_t)hi << 32) | lo;
+        }
+    }
+    if (keep_kv) {
+        for (int c = warp; c < 64; c += 8) {
+            const uint32_t lo = __ballot_sync(0xffffffffu, tile[lane][c]);
+            const uint32_t hi = __ballot_sync(0xffffffffu, tile[32 + lane][c]);
+            if (lane == 0 && c0 + c < cols) keep_kv[(c0 + c) * words_kv + blockIdx.y] = ((uint64_t)hi << 32) | lo;
+        }
+    }
+}
+
 template <typename T, int DMAX> struct FwdLaunch {
     static cudaError_t run(const FwdArgs &a, cudaStream_t s)
     {
@@ -487,6 +524,18 @@ cudaError_t launch_grad_dq_simt(const GradArgs &a, cudaStream_t s) { return disp
 cudaError_t launch_prepass(const GradArgs &a, bool tc_state, cudaStream_t s)
 {
     return dispatch<PrepassLaunch>(a.dtype, a.d, a, tc_state, s);
+}
+
+cudaError_t launch_amask_pack(const uint8_t *amask, int64_t rows, int64_t cols, uint64_t *keep_q, int32_t words_q,
+                              uint64_t *keep_kv, int32_t words_kv, cudaStream_t s)
+{
+    // grid: one block per 64 x 64 tile, rows and columns rounded up to 128
+    const int64_t gx = 2 * ((cols + 127) / 128), gy = 2 * ((rows + 127) / 128);
+    if (rows < 1 || cols < 1 || gy > 65535 || gx > INT32_MAX) return cudaErrorInvalidValue;
+    if ((keep_q && words_q != gx) || (keep_kv && words_kv != gy)) return cudaErrorInvalidValue;
+    amask_pack_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(amask, rows, cols, keep_q, words_q, keep_kv,
+                                                                        words_kv);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_sink_reduce(const GradArgs &a, cudaStream_t s)

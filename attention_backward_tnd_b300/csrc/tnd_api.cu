@@ -32,10 +32,10 @@ struct ProfEntry {
     int kind;
     cudaEvent_t start, stop;
 };
-const char *kKindNames[] = {"fwd_simt", "grad_prepass", "grad_dkdv_simt", "grad_dq_simt",
-                            "grad_sink_reduce", "grad_tc_main", "grad_dq_finalize", "fwd_tc"};
+const char *kKindNames[] = {"fwd_simt",         "grad_prepass", "grad_dkdv_simt", "grad_dq_simt", "grad_sink_reduce",
+                            "grad_tc_main",     "grad_dq_finalize", "fwd_tc",     "atten_mask_pack"};
 constexpr int kNumKinds = sizeof(kKindNames) / sizeof(kKindNames[0]);
-enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN, K_FWD_TC };
+enum Kind { K_FWD = 0, K_PREPASS, K_DKDV, K_DQ, K_SINK, K_TC, K_FIN, K_FWD_TC, K_PACK };
 std::vector<ProfEntry> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 constexpr size_t kProfCap = 4096;
@@ -84,21 +84,34 @@ struct Problem {
     double scale = 0, keep = 1;
     int64_t pre = 0, next = 0, mode = 0;
     bool has_drop = false, has_sink = false;
+    bool has_amask = false;            // the attention-mask matrix is read (sparseMode 0 / 1)
+    const int64_t *prefix = nullptr;   // prefixOptional (sparseMode 6)
     int64_t tq = 0, tkv = 0;
+    int64_t s1max = 0, s2max = 0;      // longest query / key sequence: the matrix is [S1Max][S2Max]
 };
 
 constexpr int64_t kMaxTokens = int64_t(1) << 20;  // T in [1, 1M]
 constexpr int64_t kMaxHeads = 256;                // N in [1, 256]
 constexpr int64_t kMaxHeadDim = 768;              // D in [1, 768] (V5 page)
 constexpr int64_t kMaxBatch = 20000;              // B in [1, 20000] (V5 page)
+constexpr int64_t kMaxBatchPrefix = 1024;         // B in [1, 1K] with prefixOptional
+constexpr int64_t kTokenClamp = int64_t(1) << 40; // |preTokens|, |nextTokens| beyond any T act alike
 constexpr int64_t kSimtMaxHeadDim = 256;          // this build's CUDA-core kernels
 
-tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq,
-                    int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next,
-                    int64_t mode, bool has_drop, bool has_sink, Problem &p)
+// Argument checks of the first phase ([UnpadGrad] parameters and constraints:
+// sparseMode, attenMaskOptional, prefixOptional).  Modes 0 (with the matrix)
+// and 1 read the attention-mask matrix; modes 2, 3, 4 and 6 are index rules
+// (the pages' compressed matrices for them restate those rules, so a matrix
+// passed with them is not read); mode 6 reads prefix; 5, 7 and 8 are not
+// implemented.
+tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv, const int64_t *prefix,
+                    int64_t nq, int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next,
+                    int64_t mode, bool has_drop, bool has_amask, bool has_sink, Problem &p)
 {
     if (!cuq || !cukv) return TND_ERR_NULLPTR;
     if (keep < 1.0 && !has_drop) return TND_ERR_NULLPTR;  // dropMask needed when keepProb < 1
+    if (mode == 1 && !has_amask) return TND_ERR_NULLPTR;  // the full matrix is the mask
+    if (mode == 6 && !prefix) return TND_ERR_NULLPTR;
     if (dtype != TND_F16 && dtype != TND_BF16 && dtype != TND_F32) return TND_ERR_INVALID;
     if (batch < 1 || batch > kMaxBatch) return TND_ERR_INVALID;
     if (cuq[0] != 0 || cukv[0] != 0) return TND_ERR_INVALID;
@@ -113,11 +126,20 @@ tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t 
     if (!(keep > 0.0 && keep <= 1.0)) return TND_ERR_INVALID;
     if (!std::isfinite(scale)) return TND_ERR_INVALID;
     if (mode < 0 || mode > 8) return TND_ERR_INVALID;
-    if (mode == 4 && pre + next < 0) return TND_ERR_INVALID;  // band needs an intersection
-    if (mode == 1 || mode >= 5) return TND_ERR_UNSUPPORTED;
+    pre = std::max(-kTokenClamp, std::min(pre, kTokenClamp));
+    next = std::max(-kTokenClamp, std::min(next, kTokenClamp));
+    const bool band = mode == 4 || (mode == 0 && has_amask);
+    if (band && pre + next < 0) return TND_ERR_INVALID;  // band needs an intersection
+    if (mode == 5 || mode >= 7) return TND_ERR_UNSUPPORTED;
     if (mode == 4) {
         for (int64_t b = 0; b < batch; ++b) {
             if (cuq[b + 1] - cuq[b] != cukv[b + 1] - cukv[b]) return TND_ERR_UNSUPPORTED;
+        }
+    }
+    if (mode == 6) {
+        if (batch > kMaxBatchPrefix) return TND_ERR_INVALID;
+        for (int64_t b = 0; b < batch; ++b) {
+            if (prefix[b] < 0 || prefix[b] > cukv[b + 1] - cukv[b]) return TND_ERR_INVALID;
         }
     }
     if (d > kSimtMaxHeadDim) return TND_ERR_UNSUPPORTED;
@@ -135,17 +157,37 @@ tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t 
     p.mode = mode;
     p.has_drop = has_drop && keep < 1.0;
     p.has_sink = has_sink;
+    p.has_amask = has_amask && (mode == 0 || mode == 1);
+    p.prefix = mode == 6 ? prefix : nullptr;
+    for (int64_t b = 0; b < batch; ++b) {
+        p.s1max = std::max(p.s1max, cuq[b + 1] - cuq[b]);
+        p.s2max = std::max(p.s2max, cukv[b + 1] - cukv[b]);
+    }
     return TND_OK;
 }
 
+// The index rule of the problem's sparseMode (the matrix pointers are filled
+// in by the run calls).
 MaskSpec mask_of(const Problem &p)
 {
-    MaskSpec m;
-    m.mode = (int32_t)p.mode;
+    MaskSpec m{};
+    switch (p.mode) {
+    case 0: m.mode = p.has_amask ? kRuleBand : kRuleAll; break;
+    case 1: m.mode = kRuleAll; break;
+    case 2: m.mode = kRuleTopLeft; break;
+    case 3: m.mode = kRuleCausal; break;
+    case 4: m.mode = kRuleBand; break;
+    default: m.mode = kRulePrefix; break;
+    }
     m.pre = p.pre;
     m.next = p.next;
     return m;
 }
+
+// 64-bit words per row of the packed matrix: rows of keep_q cover S2Max
+// columns, rows of keep_kv S1Max rows, rounded up to 128 bits.
+int32_t words_q_of(const Problem &p) { return (int32_t)(2 * ((p.s2max + 127) / 128)); }
+int32_t words_kv_of(const Problem &p) { return (int32_t)(2 * ((p.s1max + 127) / 128)); }
 
 int64_t mask_bits_total(const Problem &p)
 {
@@ -173,14 +215,14 @@ struct Plan {
 };
 
 // Union of the kept key ranges of query rows [r0, r1) (empty: lo > hi).
-void rows_union(const MaskSpec &m, int64_t sq, int64_t skv, int64_t r0, int64_t r1, int64_t &ulo,
-                int64_t &uhi)
+void rows_union(const MaskSpec &m, int64_t sq, int64_t skv, int64_t prefix_n, int64_t r0, int64_t r1,
+                int64_t &ulo, int64_t &uhi)
 {
     ulo = INT64_MAX;
     uhi = INT64_MIN;
     for (int64_t i = r0; i < r1; ++i) {
         int64_t lo, hi;
-        key_range(m, sq, skv, i, lo, hi);
+        key_range(m, sq, skv, prefix_n, i, lo, hi);
         if (lo > hi) continue;
         ulo = std::min(ulo, lo);
         uhi = std::max(uhi, hi);
@@ -209,6 +251,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         sd.mask_base = base;
         sd.qblk0 = (int32_t)qblk0;
         sd.nqblk = (int32_t)((sq + kQBlock - 1) / kQBlock);
+        sd.prefix = p.prefix ? (int32_t)p.prefix[b] : 0;
         base += p.nq * sq * skv;
         qblk0 += sd.nqblk;
         for (int64_t r = 0; r < sq; r += kSimtRows) pl.q_items.push_back(make_int2((int)b, (int)r));
@@ -216,7 +259,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         for (int64_t r = 0; r < sq; r += kQBlock) pl.qblk_rows.push_back(make_int2((int)b, (int)r));
         for (int64_t i = 0; i < sq; ++i) {
             int64_t lo, hi;
-            key_range(m, sq, skv, i, lo, hi);
+            key_range(m, sq, skv, sd.prefix, i, lo, hi);
             if (hi >= lo) pl.kept_pairs += (hi - lo + 1) * p.nq;
         }
         if (!with_units) continue;
@@ -224,7 +267,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         std::vector<int32_t> ilo(nkb, INT32_MAX), ihi(nkb, -1);
         for (int64_t qb = 0; qb < sd.nqblk; ++qb) {
             int64_t ulo, uhi;
-            rows_union(m, sq, skv, qb * kQBlock, std::min<int64_t>(sq, (qb + 1) * kQBlock), ulo, uhi);
+            rows_union(m, sq, skv, sd.prefix, qb * kQBlock, std::min<int64_t>(sq, (qb + 1) * kQBlock), ulo, uhi);
             QBlockInfo qi;
             if (ulo > uhi) {
                 qi.jlo = qi.jhi = -1;
@@ -287,7 +330,7 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
 struct Layout {
     size_t seqs = 0, q_items = 0, kv_items = 0, units = 0, qblk = 0, qblk_rows = 0, fwd_units = 0;  // offsets of the
     size_t plan_end = 0;                                                                // copied plan
-    size_t flags = 0, lse2 = 0, drow = 0, sinkrow = 0, dqacc = 0, total = 0;
+    size_t flags = 0, lse2 = 0, drow = 0, sinkrow = 0, dqacc = 0, keep_bits = 0, total = 0;
 };
 
 // Offsets of the copied plan (status words first); the rest of the layout
@@ -327,6 +370,11 @@ Layout layout_for(const Problem &p, const Plan &pl, bool grad, bool tc)
         L.sinkrow = take(p.has_sink ? vec * sizeof(float) : 0);
         L.dqacc = take(tc ? (size_t)p.tq * (size_t)p.nq * (size_t)p.d * sizeof(float) : 0);
     }
+    // packed attention-mask matrix for the tensor-core kernels (forward:
+    // rows of q, gradient: rows of kv)
+    if (tc && p.has_amask)
+        L.keep_bits = take(grad ? (size_t)p.s2max * words_kv_of(p) * sizeof(uint64_t)
+                                : (size_t)p.s1max * words_q_of(p) * sizeof(uint64_t));
     L.total = off;
     return L;
 }
@@ -356,12 +404,13 @@ void build_image(Plan &pl)
 // plan instead of rebuilding it.  Small LRU, shared by all threads.
 struct PlanKey {
     int64_t batch, nq, nkv, mode, pre, next;
-    bool with_units;
-    std::vector<int64_t> cuq, cukv;
+    bool with_units, has_amask;
+    std::vector<int64_t> cuq, cukv, prefix;
     bool operator==(const PlanKey &o) const
     {
         return batch == o.batch && nq == o.nq && nkv == o.nkv && mode == o.mode && pre == o.pre && next == o.next &&
-               with_units == o.with_units && cuq == o.cuq && cukv == o.cukv;
+               with_units == o.with_units && has_amask == o.has_amask && cuq == o.cuq && cukv == o.cukv &&
+               prefix == o.prefix;
     }
 };
 constexpr size_t kPlanCacheSize = 8;
@@ -370,8 +419,9 @@ std::mutex g_plan_mu;
 
 std::shared_ptr<const Plan> get_plan(const Problem &p, bool with_units)
 {
-    PlanKey key{p.batch, p.nq, p.nkv, p.mode, p.pre, p.next, with_units,
-                std::vector<int64_t>(p.cuq, p.cuq + p.batch + 1), std::vector<int64_t>(p.cukv, p.cukv + p.batch + 1)};
+    PlanKey key{p.batch, p.nq, p.nkv, p.mode, p.pre, p.next, with_units, p.has_amask,
+                std::vector<int64_t>(p.cuq, p.cuq + p.batch + 1), std::vector<int64_t>(p.cukv, p.cukv + p.batch + 1),
+                p.prefix ? std::vector<int64_t>(p.prefix, p.prefix + p.batch) : std::vector<int64_t>()};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         for (size_t i = g_plan_cache.size(); i-- > 0;) {
@@ -620,35 +670,38 @@ tnd_status tnd_attn_profile_read(const char **names, double *total_ms, int64_t *
 }
 
 tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                                       int64_t nq, int64_t nkv, int64_t d, double scale, double keep, int64_t pre,
-                                       int64_t next, int64_t mode, int has_drop, int has_sink, uint64_t *ws_size)
+                                       const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale,
+                                       double keep, int64_t pre, int64_t next, int64_t mode, int has_drop,
+                                       int has_amask, int has_sink, uint64_t *ws_size)
 {
     if (!ws_size) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode, has_drop != 0,
-                             has_sink != 0, p);
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+                             has_drop != 0, has_amask != 0, has_sink != 0, p);
     if (st != TND_OK) return st;
-    auto plp = get_plan(p, fwd_tc_supported(p.dtype, (int)p.d));
-    *ws_size = layout_for(p, *plp, false, false).total;
+    const bool tc_layout = fwd_tc_supported(p.dtype, (int)p.d);
+    auto plp = get_plan(p, tc_layout);
+    *ws_size = layout_for(p, *plp, false, tc_layout).total;
     return TND_OK;
 }
 
-tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask, const float *sink,
-                        tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq,
-                        int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode,
-                        void *out, float *smax, float *ssum, void *ws, uint64_t ws_size, void *stream)
+tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask,
+                        const uint8_t *atten_mask, const float *sink, tnd_dtype dtype, int64_t batch,
+                        const int64_t *cuq, const int64_t *cukv, const int64_t *prefix, int64_t nq, int64_t nkv,
+                        int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *out,
+                        float *smax, float *ssum, void *ws, uint64_t ws_size, void *stream)
 {
     if (!q || !k || !v || !out || !smax || !ssum) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode,
-                             drop_mask != nullptr, sink != nullptr, p);
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+                             drop_mask != nullptr, atten_mask != nullptr, sink != nullptr, p);
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, (const void *)out, (const void *)smax, (const void *)ssum})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
     const bool tc_layout = fwd_tc_supported(p.dtype, (int)p.d);
     auto plp = get_plan(p, tc_layout);
     const Plan &pl = *plp;
-    const Layout L = layout_for(p, pl, false, false);
+    const Layout L = layout_for(p, pl, false, tc_layout);
     if (!ws || ws_size < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TND_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     st = upload_plan(pl, ws, s);
@@ -674,7 +727,21 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
         a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)di.clock_khz;
         a.num_sms = di.num_sms;
     }
-    if (tc_layout && use_fwd_tc(p)) {
+    const bool tc = tc_layout && use_fwd_tc(p);
+    if (p.has_amask) {
+        a.mask.amask = atten_mask;
+        a.mask.amask_cols = p.s2max;
+        if (tc) {
+            a.mask.keep_q = (const uint64_t *)(w + L.keep_bits);
+            a.mask.words_q = words_q_of(p);
+            if (timed(K_PACK, s, [&] {
+                    return launch_amask_pack(atten_mask, p.s1max, p.s2max, (uint64_t *)(w + L.keep_bits),
+                                             a.mask.words_q, nullptr, 0, s);
+                }) != cudaSuccess)
+                return TND_ERR_CUDA;
+        }
+    }
+    if (tc) {
         if (timed(K_FWD_TC, s, [&] { return launch_fwd_tc(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
     } else {
         if (timed(K_FWD, s, [&] { return launch_fwd_simt(a, s); }) != cudaSuccess) return TND_ERR_CUDA;
@@ -683,13 +750,14 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
 }
 
 tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                                        int64_t nq, int64_t nkv, int64_t d, double scale, double keep, int64_t pre,
-                                        int64_t next, int64_t mode, int has_drop, int has_sink, uint64_t *ws_size)
+                                        const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale,
+                                        double keep, int64_t pre, int64_t next, int64_t mode, int has_drop,
+                                        int has_amask, int has_sink, uint64_t *ws_size)
 {
     if (!ws_size) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode, has_drop != 0,
-                             has_sink != 0, p);
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+                             has_drop != 0, has_amask != 0, has_sink != 0, p);
     if (st != TND_OK) return st;
     const bool tc = grad_tc_supported(p.dtype, (int)p.d);
     auto plp = get_plan(p, tc);
@@ -702,18 +770,19 @@ tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const in
 namespace tnd {
 
 tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                    const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
-                    int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv, int64_t d,
-                    double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv,
-                    float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload)
+                    const uint8_t *atten_mask, const float *smax, const float *ssum, const void *o,
+                    const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
+                    const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale, double keep,
+                    int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv, float *dsink, void *ws,
+                    uint64_t ws_size, void *stream, bool pinned_upload)
 {
     if (!q || !k || !v || !dy || !smax || !ssum || !o || !dq || !dk || !dv) return TND_ERR_NULLPTR;
     if (sink && !dsink) return TND_ERR_NULLPTR;
     HostClock hc;
     (void)hc;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, nq, nkv, d, scale, keep, pre, next, mode,
-                             drop_mask != nullptr, sink != nullptr, p);
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+                             drop_mask != nullptr, atten_mask != nullptr, sink != nullptr, p);
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, dy, (const void *)smax, (const void *)ssum, o, (const void *)dq,
                             (const void *)dk, (const void *)dv})
@@ -765,6 +834,19 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
         a.num_sms = di.num_sms;
         a.test_flags = g_opt.test_skip_load ? 1 : 0;
     }
+    if (p.has_amask) {
+        a.mask.amask = atten_mask;
+        a.mask.amask_cols = p.s2max;
+        if (tc) {
+            a.mask.keep_kv = (const uint64_t *)(w + L.keep_bits);
+            a.mask.words_kv = words_kv_of(p);
+            if (timed(K_PACK, s, [&] {
+                    return launch_amask_pack(atten_mask, p.s1max, p.s2max, nullptr, 0, (uint64_t *)(w + L.keep_bits),
+                                             a.mask.words_kv, s);
+                }) != cudaSuccess)
+                return TND_ERR_CUDA;
+        }
+    }
     HOST_LAP(3);
     if (timed(K_PREPASS, s, [&] { return launch_prepass(a, tc, s); }) != cudaSuccess) return TND_ERR_CUDA;
     HOST_LAP(4);
@@ -788,13 +870,14 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
 extern "C" {
 
 tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                         const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
-                         int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv,
-                         int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq,
-                         void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream)
+                         const uint8_t *atten_mask, const float *smax, const float *ssum, const void *o,
+                         const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
+                         const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale, double keep,
+                         int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv, float *dsink,
+                         void *ws, uint64_t ws_size, void *stream)
 {
-    return grad_run(q, k, v, dy, drop_mask, smax, ssum, o, sink, dtype, batch, cuq, cukv, nq, nkv, d, scale, keep,
-                    pre, next, mode, dq, dk, dv, dsink, ws, ws_size, stream, true);
+    return grad_run(q, k, v, dy, drop_mask, atten_mask, smax, ssum, o, sink, dtype, batch, cuq, cukv, prefix, nq,
+                    nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, ws_size, stream, true);
 }
 
 tnd_status tnd_attn_device_status(const void *ws, uint64_t ws_size, void *stream)
@@ -810,13 +893,14 @@ tnd_status tnd_attn_device_status(const void *ws, uint64_t ws_size, void *stream
     return TND_ERR_DEVICE_CHECK;
 }
 
-tnd_status tnd_attn_grad_plan(int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv,
-                              int64_t pre, int64_t next, int64_t mode, int64_t *units, int64_t capacity,
-                              int64_t *n_units, int64_t *kept_pairs)
+tnd_status tnd_attn_grad_plan(int64_t batch, const int64_t *cuq, const int64_t *cukv, const int64_t *prefix,
+                              int64_t nq, int64_t nkv, int64_t pre, int64_t next, int64_t mode, int has_amask,
+                              int64_t *units, int64_t capacity, int64_t *n_units, int64_t *kept_pairs)
 {
     if (!n_units || !kept_pairs) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(TND_BF16, batch, cuq, cukv, nq, nkv, 128, 1.0, 1.0, pre, next, mode, false, false, p);
+    tnd_status st = validate(TND_BF16, batch, cuq, cukv, prefix, nq, nkv, 128, 1.0, 1.0, pre, next, mode, false,
+                             has_amask != 0, false, p);
     if (st != TND_OK) return st;
     Plan pl;
     build_plan(p, true, pl);

@@ -28,35 +28,65 @@ struct SeqDesc {
     int32_t sq;         // query rows
     int32_t skv;        // key/value rows
     int64_t mask_base;  // flat keep-bit index of (h=0, i=0, j=0)
-    int32_t qblk0;      // global index of its first 64-row q block
-    int32_t nqblk;      // number of 64-row q blocks
+    int32_t qblk0;      // global index of its first 128-row q block
+    int32_t nqblk;      // number of 128-row q blocks
+    int32_t prefix;     // prefixOptional N_b (sparseMode 6; 0 otherwise)
+    int32_t pad;
 };
 
-// Mask description (sparseMode 0/2/3/4 computed from indices).
+// Index rules of the masks, after mapping the pages' sparseMode (and the
+// attention-mask matrix) onto them.
+enum MaskRule : int32_t {
+    kRuleAll = 0,      // every (i, j)
+    kRuleTopLeft = 2,  // j <= i
+    kRuleCausal = 3,   // j <= i + Skv - Sq
+    kRuleBand = 4,     // -pre <= j - i <= next
+    kRulePrefix = 6,   // j <= i + Skv - Sq or j < N_b
+};
+
+// Mask description: an index rule, plus (sparseMode 0 with a matrix, and 1)
+// the attention-mask matrix, which further drops the (i, j) it marks.
 struct MaskSpec {
-    int32_t mode;
+    int32_t mode;              // MaskRule
     int64_t pre;
     int64_t next;
+    const uint8_t *amask;      // [S1Max][S2Max] bytes, nonzero masks (NULL = none)
+    int64_t amask_cols;        // S2Max
+    const uint64_t *keep_q;    // packed keep bits of the matrix, row i: bit j (forward)
+    const uint64_t *keep_kv;   // transposed, row j: bit i (gradient)
+    int32_t words_q;           // 64-bit words per row of keep_q (even)
+    int32_t words_kv;          // 64-bit words per row of keep_kv (even)
 };
 
-// Key range [lo, hi] kept for query row i (empty when lo > hi).  Rows of
-// every supported mode keep one contiguous range whose ends never decrease
-// with i, which the schedules rely on.
-__host__ __device__ inline void key_range(const MaskSpec &m, int64_t sq, int64_t skv, int64_t i,
-                                          int64_t &lo, int64_t &hi)
+// Key range [lo, hi] of the index rule for query row i (empty when lo > hi);
+// prefix_n is the sequence's N_b.  Rows of every rule keep one contiguous
+// range whose ends never decrease with i, which the schedules rely on (the
+// prefix rule's two parts both start at column 0).
+__host__ __device__ inline void key_range(const MaskSpec &m, int64_t sq, int64_t skv, int64_t prefix_n,
+                                          int64_t i, int64_t &lo, int64_t &hi)
 {
     lo = 0;
     hi = skv - 1;
-    if (m.mode == 2) {
+    if (m.mode == kRuleTopLeft) {
         hi = hi < i ? hi : i;
-    } else if (m.mode == 3) {
+    } else if (m.mode == kRuleCausal) {
         const int64_t e = i + skv - sq;
         hi = hi < e ? hi : e;
-    } else if (m.mode == 4) {
+    } else if (m.mode == kRuleBand) {
         const int64_t a = i - m.pre, e = i + m.next;
         lo = lo > a ? lo : a;
         hi = hi < e ? hi : e;
+    } else if (m.mode == kRulePrefix) {
+        int64_t e = i + skv - sq;
+        e = e > prefix_n - 1 ? e : prefix_n - 1;
+        hi = hi < e ? hi : e;
     }
+}
+
+// Whether the attention-mask matrix keeps in-sequence (i, j) (true without one).
+__host__ __device__ inline bool matrix_keeps(const MaskSpec &m, int64_t i, int64_t j)
+{
+    return m.amask == nullptr || m.amask[i * m.amask_cols + j] == 0;
 }
 
 // Work unit of the tensor-core gradient: kv block j of kv head g of
@@ -144,6 +174,11 @@ struct FwdArgs {
 };
 
 // Kernel launchers (each returns the CUDA error of its launch).
+// Packs the [rows][cols] attention-mask bytes into keep bits: keep_q (row i,
+// bit j) and / or keep_kv (row j, bit i), whichever is non-NULL; bits past
+// the matrix are 0.
+cudaError_t launch_amask_pack(const uint8_t *amask, int64_t rows, int64_t cols, uint64_t *keep_q, int32_t words_q,
+                              uint64_t *keep_kv, int32_t words_kv, cudaStream_t s);
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t s);
 // Tensor-core forward (bf16/fp16, D = 64 or 128); false where it does not apply.
 bool fwd_tc_supported(int dtype, int d);
@@ -165,8 +200,9 @@ cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s);
 // plan from pageable host memory and allocates nothing (the library's pinned
 // staging slots are allocated on first use).
 tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                    const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
-                    int64_t batch, const int64_t *cuq, const int64_t *cukv, int64_t nq, int64_t nkv, int64_t d,
+                    const uint8_t *atten_mask, const float *smax, const float *ssum, const void *o,
+                    const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
+                    const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d,
                     double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv,
                     float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload);
 

@@ -39,15 +39,30 @@
  * actualSeqQLen / actualSeqKvLen ([UnpadGrad] parameters: the S of each
  * batch entry).  A sequence may be empty.
  *
- * sparse_mode ([UnpadGrad] parameters, sparseMode), computed, never read
- * from a mask tensor:
- *   0  no mask; pre_tokens / next_tokens ignored
+ * sparse_mode ([UnpadGrad] parameters, sparseMode; i, j are the row and
+ * column within sequence b):
+ *   0  without atten_mask: no mask, pre_tokens / next_tokens ignored;
+ *      with atten_mask: keep where the matrix is 0 and
+ *      -pre_tokens <= j - i <= next_tokens (pre_tokens + next_tokens >= 0)
+ *   1  keep where the matrix is 0 (atten_mask required)
  *   2  lower triangle from the top-left vertex:      keep j <= i
  *   3  lower triangle from the bottom-right vertex:  keep j <= i + Skv - Sq
  *   4  band: keep -pre_tokens <= j - i <= next_tokens (needs Sq_b == Skv_b
  *      for every sequence and pre_tokens + next_tokens >= 0)
- *   1, 5, 6, 7, 8 (explicit mask tensors, prefix, external split) return
- *   TND_ERR_UNSUPPORTED.
+ *   6  prefix: keep j <= i + Skv - Sq or j < prefix[b] (prefix required;
+ *      batch <= 1024; 0 <= prefix[b] <= Skv_b)
+ *   5, 7, 8 (padded full matrix, external split) return TND_ERR_UNSUPPORTED.
+ *   Modes 2, 3, 4 and 6 are computed from indices: the pages' compressed
+ *   matrices for them only restate these rules, so an atten_mask passed with
+ *   them is not read.
+ * atten_mask ([UnpadGrad] parameters, attenMaskOptional): device uint8 (or
+ *   bool) [S1Max, S2Max] row-major, S1Max = max_b Sq_b, S2Max = max_b Skv_b;
+ *   one matrix for every sequence and head, indexed by (i, j); nonzero
+ *   masks, 0 keeps.  Read only by modes 0 and 1.
+ * prefix ([UnpadGrad] parameters, prefixOptional): HOST array of batch int64
+ *   values N_b, read only by mode 6 (NULL otherwise).
+ * A row that keeps no key (and has no sink) gets max = -inf, sum = 0 and a
+ * zero output row; its gradient rows are zero.
  * GQA: Nq % Nkv == 0; query head h uses key/value head h / (Nq/Nkv).
  *
  * Two phases, as on the pages ([UnpadGrad] function prototype section): a
@@ -89,54 +104,61 @@ typedef enum tnd_dtype { TND_F16 = 0, TND_BF16 = 1, TND_F32 = 2 } tnd_dtype;
  * Forward workspace size ([UnpadGrad]/[ScoreV2] function prototype: first
  * phase).  Checks all shape / scalar arguments ([UnpadGrad] and
  * [UnpadGradV5] constraints: T in [1, 1M], N in [1, 256], D in [1, 768],
- * B in [1, 20000], keep_prob in (0, 1], headNum == Nq, Nq % Nkv == 0).
- * has_drop_mask / has_sink say whether the run call will pass those inputs.
- * Writes the byte count to *workspace_size.
+ * B in [1, 20000], keep_prob in (0, 1], headNum == Nq, Nq % Nkv == 0) and
+ * the sparse_mode rules above.  has_drop_mask / has_atten_mask / has_sink
+ * say whether the run call will pass those inputs; prefix is the host
+ * prefix array (mode 6).  Writes the byte count to *workspace_size.
  */
 tnd_status tnd_attn_fwd_workspace_size(
     tnd_dtype dtype, int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
-    int64_t head_num, int64_t kv_head_num, int64_t head_dim, double scale_value,
-    double keep_prob, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
-    int has_drop_mask, int has_sink, uint64_t *workspace_size);
+    const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
+    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode, int has_drop_mask, int has_atten_mask, int has_sink,
+    uint64_t *workspace_size);
 
 /*
  * Forward ([ScoreV2] function description and parameters): writes
  * attention_out [Tq,Nq,D] (dtype), softmax_max and softmax_sum [Tq,Nq,8]
- * (fp32).  drop_mask and sink may be NULL (see conventions).
+ * (fp32).  drop_mask, atten_mask, sink and prefix may be NULL where the
+ * conventions above allow it.
  */
 tnd_status tnd_attn_fwd(
     const void *query, const void *key, const void *value, const uint8_t *drop_mask,
-    const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cu_seqlens_q,
-    const int64_t *cu_seqlens_kv, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
-    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
-    int64_t sparse_mode, void *attention_out, float *softmax_max, float *softmax_sum,
-    void *workspace, uint64_t workspace_size, void *stream);
+    const uint8_t *atten_mask, const float *sink, tnd_dtype dtype, int64_t batch,
+    const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, const int64_t *prefix,
+    int64_t head_num, int64_t kv_head_num, int64_t head_dim, double scale_value,
+    double keep_prob, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
+    void *attention_out, float *softmax_max, float *softmax_sum, void *workspace,
+    uint64_t workspace_size, void *stream);
 
 /* Gradient workspace size (first phase of [UnpadGrad]); same arguments and
  * checks as the forward's. */
 tnd_status tnd_attn_grad_workspace_size(
     tnd_dtype dtype, int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
-    int64_t head_num, int64_t kv_head_num, int64_t head_dim, double scale_value,
-    double keep_prob, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
-    int has_drop_mask, int has_sink, uint64_t *workspace_size);
+    const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
+    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode, int has_drop_mask, int has_atten_mask, int has_sink,
+    uint64_t *workspace_size);
 
 /*
  * Score-gradient ([UnpadGrad] second phase; inputs and outputs as in its
  * parameters section, plus sinkInOptional / dSink of [UnpadGradV5]).
  * Inputs: query, key, value, dy; softmax_max, softmax_sum and attention_in
- * as written by tnd_attn_fwd; drop_mask (NULL when keep_prob == 1); sink
- * (NULL = no sink).  Outputs: dq [Tq,Nq,D], dk and dv [Tkv,Nkv,D] (dtype;
- * dk and dv are summed over the Nq/Nkv query heads of each kv head), dsink
- * [Nq] fp32 (required when sink is given, ignored otherwise).
+ * as written by tnd_attn_fwd; drop_mask (NULL when keep_prob == 1);
+ * atten_mask and prefix as for the forward (the same ones it was given);
+ * sink (NULL = no sink).  Outputs: dq [Tq,Nq,D], dk and dv [Tkv,Nkv,D]
+ * (dtype; dk and dv are summed over the Nq/Nkv query heads of each kv
+ * head), dsink [Nq] fp32 (required when sink is given, ignored otherwise).
  */
 tnd_status tnd_attn_grad(
     const void *query, const void *key, const void *value, const void *dy,
-    const uint8_t *drop_mask, const float *softmax_max, const float *softmax_sum,
-    const void *attention_in, const float *sink, tnd_dtype dtype, int64_t batch,
-    const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, int64_t head_num,
-    int64_t kv_head_num, int64_t head_dim, double scale_value, double keep_prob,
-    int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode, void *dq, void *dk, void *dv,
-    float *dsink, void *workspace, uint64_t workspace_size, void *stream);
+    const uint8_t *drop_mask, const uint8_t *atten_mask, const float *softmax_max,
+    const float *softmax_sum, const void *attention_in, const float *sink, tnd_dtype dtype,
+    int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
+    const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
+    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode, void *dq, void *dk, void *dv, float *dsink, void *workspace,
+    uint64_t workspace_size, void *stream);
 
 /*
  * Waits for `stream`, then reports the device-side status of the last
@@ -188,14 +210,17 @@ tnd_status tnd_attn_profile_read(const char **names, double *total_ms, int64_t *
  * work).  For the problem described by the arguments writes up to
  * `capacity` work units as 5 int64 each (sequence b, kv head g, kv block j,
  * first q block, end q block) in the order the tensor-core kernel takes
- * them, the unit count to *n_units and the number of kept (q-row, kv-row)
- * pairs summed over sequences and query heads to *kept_pairs.  Blocks are
- * 128 kv rows and 128 q rows.
+ * them, the unit count to *n_units and the number of (q-row, kv-row)
+ * pairs the index rule keeps, summed over sequences and query heads, to
+ * *kept_pairs (the attention-mask matrix is not seen here: with one, the
+ * count is of the pairs its band admits).  Blocks are 128 kv rows and 128
+ * q rows.
  */
 tnd_status tnd_attn_grad_plan(
-    int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, int64_t head_num,
-    int64_t kv_head_num, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
-    int64_t *units, int64_t capacity, int64_t *n_units, int64_t *kept_pairs);
+    int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
+    const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t pre_tokens,
+    int64_t next_tokens, int64_t sparse_mode, int has_atten_mask, int64_t *units,
+    int64_t capacity, int64_t *n_units, int64_t *kept_pairs);
 
 /*
  * Gradient without a caller-provided workspace.  The pages have no
@@ -204,7 +229,8 @@ tnd_status tnd_attn_grad_plan(
  * For callers that cannot allocate device memory, for instance a plug-in
  * that only receives buffers from its host framework's allocator, or a
  * process that reserved all device memory at start-up.  Arguments and
- * results are those of tnd_attn_grad without `workspace` / `workspace_size`;
+ * results are those of tnd_attn_grad without `workspace` / `workspace_size`,
+ * `atten_mask` and `prefix` (so sparse_mode 1 and 6 return TND_ERR_NULLPTR);
  * the caller still passes every input and output.
  *
  * The workspace is a fixed device array inside this library of

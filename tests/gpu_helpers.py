@@ -25,6 +25,7 @@ def upload(inp: workloads.Inputs):
     dev = {n: to_device(getattr(inp, n), wl.dtype) for n in ("q", "k", "v", "dy")}
     dev["sink"] = None if inp.sink is None else torch.from_numpy(inp.sink).cuda()
     dev["mask"] = None if inp.mask is None else torch.from_numpy(inp.mask).cuda()
+    dev["amask"] = None if inp.amask is None else torch.from_numpy(inp.amask).cuda()
     return dev
 
 
@@ -34,15 +35,19 @@ def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0):
     dev = dev or upload(inp)
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, grad_path) == tnd.TND_OK
     try:
+        amask = dev.get("amask")
         out, smax, ssum = tnd.fwd(dev["q"], dev["k"], dev["v"], wl.cu_q, wl.cu_kv, wl.scale, wl.keep_prob,
-                                  wl.pre_tokens, wl.next_tokens, wl.sparse_mode, dev["mask"], dev["sink"])
+                                  wl.pre_tokens, wl.next_tokens, wl.sparse_mode, dev["mask"], dev["sink"],
+                                  atten_mask=amask, prefix=wl.prefix)
         ws_bytes = tnd.grad_workspace_bytes(dev["q"], dev["k"], wl.cu_q, wl.cu_kv, wl.scale, wl.keep_prob,
                                             wl.pre_tokens, wl.next_tokens, wl.sparse_mode,
-                                            dev["mask"] is not None, dev["sink"] is not None)
+                                            dev["mask"] is not None, dev["sink"] is not None,
+                                            amask is not None, wl.prefix)
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
         dq, dk, dv, dsink = tnd.grad(dev["q"], dev["k"], dev["v"], dev["dy"], out, smax, ssum, wl.cu_q,
                                      wl.cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens, wl.next_tokens,
-                                     wl.sparse_mode, dev["mask"], dev["sink"], workspace=ws)
+                                     wl.sparse_mode, dev["mask"], dev["sink"], workspace=ws,
+                                     atten_mask=amask, prefix=wl.prefix)
         torch.cuda.synchronize()
         st = tnd.device_status(ws)
         assert st == tnd.TND_OK, f"device status {st}: {tnd.tnd_status_string(st)}"
@@ -56,7 +61,8 @@ def host64(t: torch.Tensor) -> np.ndarray:
 
 
 def oracle_problem(inp: workloads.Inputs, **kw) -> oracle.Problem:
-    return oracle.problem_from_workload(inp.wl, drop_mask=inp.mask, sink=inp.sink, **kw)
+    return oracle.problem_from_workload(inp.wl, drop_mask=inp.mask, sink=inp.sink, atten_mask=inp.amask,
+                                        prefix=inp.wl.prefix, **kw)
 
 
 def oracle_reference(inp: workloads.Inputs, **kw):
@@ -99,8 +105,8 @@ def fp32_error_bound(inp: workloads.Inputs, ref: dict) -> dict:
         if sq == 0 or skv == 0:
             continue
         q0, k0 = wl.cu_q[b], wl.cu_kv[b]
-        keep = np.array([[oracle.keep(wl.sparse_mode, wl.pre_tokens, wl.next_tokens, sq, skv, i, j)
-                          for j in range(skv)] for i in range(sq)], dtype=bool)
+        keep = np.array([[oracle.keep_at(p, b, i, j) for j in range(skv)] for i in range(sq)],
+                        dtype=bool).reshape(sq, skv)
         nk = keep.sum(axis=1) + (1 if inp.sink is not None else 0)
         base = p.mask_base(b)
         for h in range(wl.nq):
@@ -161,8 +167,8 @@ def plain_fp32_eval(inp: workloads.Inputs) -> dict:
     for b in range(wl.batch):
         sq, skv = wl.seqlens_q[b], wl.seqlens_kv[b]
         q0, k0 = wl.cu_q[b], wl.cu_kv[b]
-        keep = torch.tensor([[oracle.keep(wl.sparse_mode, wl.pre_tokens, wl.next_tokens, sq, skv, i, j)
-                              for j in range(skv)] for i in range(sq)])
+        keep = torch.tensor(np.array([[oracle.keep_at(p, b, i, j) for j in range(skv)] for i in range(sq)],
+                                     dtype=bool).reshape(sq, skv))
         base = p.mask_base(b)
         for h in range(wl.nq):
             kv = h // g
@@ -173,9 +179,10 @@ def plain_fp32_eval(inp: workloads.Inputs) -> dict:
             m = S.max(dim=1).values
             if inp.sink is not None:
                 m = torch.maximum(m, torch.tensor(float(inp.sink[h])))
+            m = torch.where(torch.isfinite(m), m, torch.zeros_like(m))   # rows that keep nothing
             E = torch.exp(S - m[:, None])
             l = E.sum(dim=1) + (torch.exp(torch.tensor(float(inp.sink[h])) - m) if inp.sink is not None else 0)
-            P = E / l[:, None]
+            P = E / torch.where(l > 0, l, torch.ones_like(l))[:, None]
             if inp.mask is not None:
                 idx = base + (h * sq + np.arange(sq))[:, None] * skv + np.arange(skv)[None, :]
                 Z = torch.from_numpy(((inp.mask[idx >> 3] >> (idx & 7)) & 1) / wl.keep_prob).float()

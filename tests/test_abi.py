@@ -43,9 +43,9 @@ def test_status_strings():
 
 
 def ws(dtype=tnd.TND_BF16, batch=2, cu_q=(0, 5, 9), cu_kv=(0, 5, 9), nq=4, nkv=2, d=128, scale=0.1, keep=1.0,
-       pre=INF, nxt=INF, mode=3, drop=False, sink=False):
-    return tnd.tnd_attn_grad_workspace_size(dtype, batch, list(cu_q), list(cu_kv), nq, nkv, d, scale, keep, pre,
-                                            nxt, mode, drop, sink)
+       pre=INF, nxt=INF, mode=3, drop=False, sink=False, amask=False, prefix=None):
+    return tnd.tnd_attn_grad_workspace_size(dtype, batch, list(cu_q), list(cu_kv), prefix, nq, nkv, d, scale, keep,
+                                            pre, nxt, mode, drop, amask, sink)
 
 
 def test_workspace_size_accepts_valid_problems():
@@ -53,8 +53,14 @@ def test_workspace_size_accepts_valid_problems():
     assert st == tnd.TND_OK and n > 0
     st2, n2 = ws(cu_q=(0, 500, 900), cu_kv=(0, 500, 900))
     assert st2 == tnd.TND_OK and n2 > n
-    assert tnd.tnd_attn_fwd_workspace_size(tnd.TND_F32, 2, [0, 5, 9], [0, 5, 9], 4, 2, 64, 0.1, 1.0, INF, INF, 0,
-                                           False, False)[0] == tnd.TND_OK
+    assert tnd.tnd_attn_fwd_workspace_size(tnd.TND_F32, 2, [0, 5, 9], [0, 5, 9], None, 4, 2, 64, 0.1, 1.0, INF,
+                                           INF, 0, False, False, False)[0] == tnd.TND_OK
+    # the packed matrix of the tensor-core kernels takes workspace
+    assert ws(mode=1, amask=True)[1] > ws(mode=0)[1]
+    assert ws(mode=6, prefix=[2, 4])[0] == tnd.TND_OK
+    assert ws(mode=0, amask=True, pre=2, nxt=0)[0] == tnd.TND_OK
+    assert ws(mode=0, amask=True, cu_kv=(0, 7, 9))[0] == tnd.TND_OK       # matrix with Sq != Skv
+    assert ws(mode=3, amask=True)[1] == ws(mode=3)[1]                     # not read by index rules
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -75,9 +81,14 @@ def test_workspace_size_accepts_valid_problems():
     (dict(scale=float("nan")), tnd.TND_ERR_INVALID),
     (dict(mode=9), tnd.TND_ERR_INVALID),
     (dict(mode=4, pre=-3, nxt=1), tnd.TND_ERR_INVALID),           # empty band
-    (dict(mode=1), tnd.TND_ERR_UNSUPPORTED),
+    (dict(mode=1), tnd.TND_ERR_NULLPTR),                          # the matrix is the mask
+    (dict(mode=6), tnd.TND_ERR_NULLPTR),                          # prefix needed
+    (dict(mode=6, prefix=[2, 5]), tnd.TND_ERR_INVALID),           # prefix > Skv
+    (dict(mode=6, prefix=[-1, 0]), tnd.TND_ERR_INVALID),
+    (dict(mode=6, batch=1025, cu_q=tuple(range(1026)), cu_kv=tuple(range(1026)), prefix=[0] * 1025),
+     tnd.TND_ERR_INVALID),                                        # B > 1K with prefix
+    (dict(mode=0, amask=True, pre=-3, nxt=1), tnd.TND_ERR_INVALID),  # empty band with the matrix
     (dict(mode=5), tnd.TND_ERR_UNSUPPORTED),
-    (dict(mode=6), tnd.TND_ERR_UNSUPPORTED),
     (dict(mode=7), tnd.TND_ERR_UNSUPPORTED),
     (dict(mode=8), tnd.TND_ERR_UNSUPPORTED),
     (dict(mode=4, pre=3, nxt=0, cu_kv=(0, 6, 9)), tnd.TND_ERR_UNSUPPORTED),  # band with Sq != Skv
@@ -89,16 +100,17 @@ def test_workspace_size_rejects(kw, expect):
 
 def test_null_workspace_size_pointer_and_seqlens():
     L = tnd.lib()
-    assert L.tnd_attn_grad_workspace_size(1, 1, None, None, 1, 1, 128, 0.1, 1.0, 0, 0, 0, 0, 0, None) == \
+    assert L.tnd_attn_grad_workspace_size(1, 1, None, None, None, 1, 1, 128, 0.1, 1.0, 0, 0, 0, 0, 0, 0, None) == \
         tnd.TND_ERR_NULLPTR
 
 
 def _grad_call(**over):
     """tnd_attn_grad with fake aligned device addresses; only arguments that
     fail validation are used, so nothing is ever dereferenced."""
-    args = dict(query=4096, key=4096, value=4096, dy=4096, drop_mask=None, softmax_max=4096, softmax_sum=4096,
-                attention_in=4096, sink=None, dtype=tnd.TND_BF16, batch=1, cu_q=[0, 8], cu_kv=[0, 8], head_num=2,
-                kv_head_num=1, head_dim=128, scale_value=0.1, keep_prob=1.0, pre_tokens=INF, next_tokens=INF,
+    args = dict(query=4096, key=4096, value=4096, dy=4096, drop_mask=None, atten_mask=None, softmax_max=4096,
+                softmax_sum=4096, attention_in=4096, sink=None, dtype=tnd.TND_BF16, batch=1, cu_q=[0, 8],
+                cu_kv=[0, 8], prefix=None, head_num=2, kv_head_num=1, head_dim=128, scale_value=0.1,
+                keep_prob=1.0, pre_tokens=INF, next_tokens=INF,
                 sparse_mode=3, dq=4096, dk=4096, dv=4096, dsink=None, workspace=None, workspace_size=0, stream=None)
     args.update(over)
     return tnd.tnd_attn_grad(*args.values())
@@ -111,6 +123,9 @@ def _grad_call(**over):
     (dict(dv=None), tnd.TND_ERR_NULLPTR),
     (dict(sink=4096, dsink=None), tnd.TND_ERR_NULLPTR),
     (dict(keep_prob=0.9), tnd.TND_ERR_NULLPTR),
+    (dict(sparse_mode=1), tnd.TND_ERR_NULLPTR),                  # no attention-mask matrix
+    (dict(sparse_mode=6), tnd.TND_ERR_NULLPTR),                  # no prefix
+    (dict(sparse_mode=6, prefix=[9]), tnd.TND_ERR_INVALID),
     (dict(head_num=3, kv_head_num=2), tnd.TND_ERR_INVALID),
     (dict(query=4098), tnd.TND_ERR_INVALID),                     # misaligned
     (dict(workspace=None, workspace_size=0), tnd.TND_ERR_WORKSPACE),
@@ -134,22 +149,24 @@ def test_set_option_checks_values():
 # host-side gradient plan
 # ---------------------------------------------------------------------------
 
-def _keep(mode, pre, nxt, sq, skv, i, j):
+def _keep(mode, pre, nxt, sq, skv, i, j, prefix_n=0):
     if mode == 0:
         return True
     if mode == 2:
         return j <= i
     if mode == 3:
         return j <= i + skv - sq
+    if mode == 6:
+        return j <= i + skv - sq or j < prefix_n
     return -pre <= j - i <= nxt
 
 
-def _tiles(mode, pre, nxt, sq, skv):
+def _tiles(mode, pre, nxt, sq, skv, prefix_n=0):
     """Brute force: set of (q block, kv block) with a kept pair, and kept pairs."""
     tiles, kept = set(), 0
     for i in range(sq):
         for j in range(skv):
-            if _keep(mode, pre, nxt, sq, skv, i, j):
+            if _keep(mode, pre, nxt, sq, skv, i, j, prefix_n):
                 tiles.add((i // 128, j // 128))
                 kept += 1
     return tiles, kept
@@ -162,21 +179,29 @@ PLANS = [
     ([700, 257], [700, 257], 2, 1, 4, 30, 150),
     ([130, 65], [500, 7], 2, 2, 0, INF, INF),
     ([260, 90], [130, 300], 2, 1, 2, INF, INF),
+    ([300, 129, 200], [300, 400, 100], 2, 1, 6, INF, INF, [170, 390, 0]),
+    ([500, 60], [200, 500], 4, 2, 6, INF, INF, [200, 1]),
 ]
+
+
+def _plan_case(case):
+    sq, skv, nq, nkv, mode, pre, nxt = PLANS[case][:7]
+    prefix = PLANS[case][7] if len(PLANS[case]) > 7 else None
+    return sq, skv, nq, nkv, mode, pre, nxt, prefix
 
 
 @pytest.mark.parametrize("case", range(len(PLANS)))
 def test_plan_covers_every_kept_tile_once_in_chain_order(case):
-    sq, skv, nq, nkv, mode, pre, nxt = PLANS[case]
+    sq, skv, nq, nkv, mode, pre, nxt, prefix = _plan_case(case)
     cu_q = np.concatenate([[0], np.cumsum(sq)])
     cu_kv = np.concatenate([[0], np.cumsum(skv)])
-    st, units, kept = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode)
+    st, units, kept = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode, prefix=prefix)
     assert st == tnd.TND_OK
     seen = {}
     order = {}
     total_kept = 0
     for b in range(len(sq)):
-        tiles, k = _tiles(mode, pre, nxt, sq[b], skv[b])
+        tiles, k = _tiles(mode, pre, nxt, sq[b], skv[b], 0 if prefix is None else prefix[b])
         total_kept += k * nq
         for g in range(nkv):
             for (qb, j) in tiles:
@@ -203,10 +228,10 @@ def test_plan_covers_every_kept_tile_once_in_chain_order(case):
 def test_plan_hands_out_kv_heads_of_a_block_together(case):
     # units of one sequence come kv block by kv block (descending), every kv
     # head of a block in a row; sequences with more tiles come first
-    sq, skv, nq, nkv, mode, pre, nxt = PLANS[case]
+    sq, skv, nq, nkv, mode, pre, nxt, prefix = _plan_case(case)
     cu_q = np.concatenate([[0], np.cumsum(sq)])
     cu_kv = np.concatenate([[0], np.cumsum(skv)])
-    st, units, _ = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode)
+    st, units, _ = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode, prefix=prefix)
     assert st == tnd.TND_OK
     groups = [units[i:i + nkv] for i in range(0, len(units), nkv)]
     for grp in groups:

@@ -37,13 +37,28 @@ SMALL = {
     "fp32_band_dropout_sink_d128": ("f32", [140, 65], None, 2, 2, 128, 4, 30, 5, 0.75, True),
     "fp16_d96_full": ("f16", [45, 70], None, 3, 1, 96, 0, INF, INF, 1.0, False),
     "single_token": ("bf16", [1], None, 1, 1, 128, 0, INF, INF, 1.0, False),
+    # attention-mask matrix (sparseMode 1, and 0 with the preTokens/nextTokens band) and prefix (6);
+    # the last field holds the matrix density / the prefix values
+    "amask_mode1_bf16": ("bf16", [200, 129, 1], None, 4, 2, 128, 1, INF, INF, 1.0, False, dict(amask=0.3)),
+    "amask_mode1_sq_ne_skv_dropout_sink": ("bf16", [100, 37], [150, 260], 2, 1, 128, 1, INF, INF, 0.8, True,
+                                           dict(amask=0.5)),
+    "amask_mode0_band_fp16_d64": ("f16", [150, 90], None, 2, 2, 64, 0, 64, 16, 1.0, False, dict(amask=0.2)),
+    "amask_mode1_fp32_d64": ("f32", [90, 33], None, 2, 1, 64, 1, INF, INF, 1.0, False, dict(amask=0.3)),
+    "prefix_bf16": ("bf16", [300, 129], [300, 200], 4, 2, 128, 6, INF, INF, 1.0, False,
+                    dict(prefix=[150, 60])),
+    "prefix_sq_gt_skv_sink_fp16": ("f16", [200, 64], [70, 64], 2, 2, 128, 6, INF, INF, 1.0, True,
+                                   dict(prefix=[0, 64])),
+    "prefix_fp32_d64_dropout": ("f32", [70, 40], [70, 90], 2, 1, 64, 6, INF, INF, 0.75, False,
+                                dict(prefix=[10, 90])),
 }
 
 
 def _small(name, seed=777):
-    dt, sq, skv, nq, nkv, d, mode, pre, nxt, keep, sink = SMALL[name]
+    dt, sq, skv, nq, nkv, d, mode, pre, nxt, keep, sink = SMALL[name][:11]
+    extra = SMALL[name][11] if len(SMALL[name]) > 11 else {}
     wl = workloads.custom(name, dt, sq, sq if skv is None else skv, nq, nkv, d, keep_prob=keep,
-                          pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, has_sink=sink, seed=seed)
+                          pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, has_sink=sink, seed=seed,
+                          amask_density=extra.get("amask", 0.0), prefix=extra.get("prefix"))
     return workloads.make_inputs(wl)
 
 

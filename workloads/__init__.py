@@ -28,6 +28,12 @@ compared against round(p_keep * 65536)), packed 8 bits per byte, least
 significant bit first, over the flattened (sequence, q-head, q-row, kv-row)
 index.  Sequence lengths of the varlen case are uniform integers in
 [256, 2048].
+
+Attention-mask matrices (sparseMode 0 / 1 cases): uint8 [S1Max, S2Max], each
+element 1 (masked) with probability ``amask_density`` (uniform 16-bit integer
+against round(density * 65536)); every row i with i % 97 == 5 is fully
+masked, so rows that keep no key occur.  Prefix values (sparseMode 6) are
+given with the workload.
 """
 
 from __future__ import annotations
@@ -39,7 +45,7 @@ from typing import Dict, List, Optional
 import numpy as np
 
 # stream ids of the independent tensors drawn for one workload
-_STREAM = {"seqlens": 1, "q": 2, "k": 3, "v": 4, "dy": 5, "sink": 6, "mask": 7}
+_STREAM = {"seqlens": 1, "q": 2, "k": 3, "v": 4, "dy": 5, "sink": 6, "mask": 7, "amask": 8}
 
 BASE_SEED = 20261202
 
@@ -62,6 +68,8 @@ class Workload:
     sparse_mode: int = 0
     has_sink: bool = False
     seed: int = BASE_SEED
+    amask_density: float = 0.0             # > 0: an attention-mask matrix is drawn
+    prefix: Optional[List[int]] = None     # prefixOptional (sparseMode 6)
 
     @property
     def batch(self) -> int:
@@ -95,6 +103,8 @@ class Workload:
             "scale": self.scale, "keep_prob": self.keep_prob,
             "pre_tokens": self.pre_tokens, "next_tokens": self.next_tokens,
             "sparse_mode": self.sparse_mode, "sink": self.has_sink, "seed": self.seed,
+            **({"atten_mask_density": self.amask_density} if self.amask_density > 0 else {}),
+            **({"prefix": list(self.prefix)} if self.prefix is not None else {}),
         }
 
 
@@ -218,6 +228,7 @@ class Inputs:
     dy64: np.ndarray
     sink: Optional[np.ndarray]          # float32 [Nq] or None
     mask: Optional[np.ndarray]          # uint8 packed keep-bits or None
+    amask: Optional[np.ndarray] = None  # uint8 [S1Max, S2Max] attention-mask matrix (nonzero masks) or None
 
 
 def make_inputs(wl: Workload, with_fp64: bool = True) -> Inputs:
@@ -232,16 +243,30 @@ def make_inputs(wl: Workload, with_fp64: bool = True) -> Inputs:
     mask = None
     if wl.keep_prob < 1.0:
         mask = dropout_mask(wl.seed, wl.mask_bits(), wl.keep_prob)
+    amask = None
+    if wl.amask_density > 0:
+        amask = atten_mask_matrix(wl.seed, max(wl.seqlens_q), max(wl.seqlens_kv), wl.amask_density)
     if not with_fp64:
         q64 = k64 = v64 = dy64 = None
-    return Inputs(wl, q, k, v, dy, q64, k64, v64, dy64, sink, mask)
+    return Inputs(wl, q, k, v, dy, q64, k64, v64, dy64, sink, mask, amask)
+
+
+def atten_mask_matrix(seed: int, rows: int, cols: int, density: float) -> np.ndarray:
+    """uint8 [rows, cols]: 1 (masked) with probability ``density``; rows i with
+    i % 97 == 5 fully masked."""
+    thresh = np.uint16(min(65535, int(round(density * 65536.0))))
+    u = _rng(seed, "amask").integers(0, 65536, size=(rows, cols), dtype=np.uint16)
+    out = (u < thresh).astype(np.uint8)
+    out[5::97, :] = 1
+    return out
 
 
 def custom(name: str, dtype: str, seqlens_q, seqlens_kv, nq: int, nkv: int, d: int, *,
            scale: Optional[float] = None, keep_prob: float = 1.0, pre_tokens: int = 2147483647,
            next_tokens: int = 2147483647, sparse_mode: int = 0, has_sink: bool = False,
-           seed: int = BASE_SEED) -> Workload:
+           seed: int = BASE_SEED, amask_density: float = 0.0, prefix=None) -> Workload:
     """A workload with explicit shapes (used for edge cases and small parity runs)."""
     return Workload(name, dtype, list(seqlens_q), list(seqlens_kv), nq, nkv, d,
                     1.0 / math.sqrt(d) if scale is None else scale, keep_prob, pre_tokens,
-                    next_tokens, sparse_mode, has_sink, seed)
+                    next_tokens, sparse_mode, has_sink, seed, amask_density,
+                    None if prefix is None else list(prefix))
