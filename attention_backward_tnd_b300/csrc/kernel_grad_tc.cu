@@ -14,7 +14,8 @@
 // dK_j (x scale) and dV_j leave TMEM once per unit.  The dQ tile of every
 // (q block, head) is combined across its contributing kv blocks in a fixed
 // order, highest kv block first: the compute warps stage each tile's dQ^T in
-// shared memory, and a writer warp stores it into an fp32 accumulator with
+// shared memory (in the tile's own Q and dY stages, whose UMMA readers are
+// done by then), and a writer warp stores it into an fp32 accumulator with
 // TMA (first contributor) or adds it with TMA bulk reduce-adds (later ones),
 // each only after its predecessor's counter says that update is complete.
 // dq_finalize_kernel then writes dQ = scale * accumulator in the output
@@ -27,19 +28,21 @@
 // for dS^T); dP^T (then, once the compute warps have read it, the tile's
 // dQ^T).  dS^T goes to its own shared-memory
 // buffer, the A operand of dK and the B operand of dQ^T.  The UMMA issue
-// order per tile t is dV(t), dP^T(t), [dS^T(t) ready] S^T(t+1), dK(t),
-// dQ^T(t): the compute warps' P^T(t+1) overlaps dK(t) and dQ^T(t).
+// order per tile t is [P^T(t) ready] dV(t), [dS^T(t) ready] dK(t), dQ^T(t),
+// S^T(t+1), [dQ^T(t) read out] dP^T(t+1); the compute warps take P^T(t),
+// dS^T(t), then the epilogue of t (dQ^T out of TMEM), so S^T(t+1) runs
+// under that epilogue and dP^T(t+1) under P^T(t+1).
 //
 // Warp roles (352 threads, one CTA per SM, persistent over work units taken
 // in plan order from a counter):
 //   warp 0      TMA producer: K, V per unit; Q (+ lse2 / D vectors) and dY
 //               per tile (two stages each)
-//   warp 1      TMEM allocator and single-thread UMMA issuer
+//   warp 1      TMEM allocator and UMMA issuer (the warp runs the issue code
+//               together; one elected lane issues)
 //   warps 2-9   compute warps, two per TMEM lane quarter, each on 64 of the
-//               tile's 128 q columns.  Per tile: P^T (thread = kv row), the
-//               epilogue of the previous tile (dQ^T out of TMEM, thread =
-//               feature, into shared-memory staging; dK, dV at unit end),
-//               then dS^T
+//               tile's 128 q columns.  Per tile: P^T (thread = kv row),
+//               dS^T, then the tile's epilogue (dQ^T out of TMEM, thread =
+//               feature, into shared-memory staging; dK, dV at unit end)
 //   warp 10     dQ writer: chain order, TMA store / reduce-add of the staged
 //               tile, counter release
 // Every wait is bounded; on expiry the kernel records TND_ERR_DEVICE_TIMEOUT
@@ -102,7 +105,8 @@ enum : int {
     B_V_FULL = 2,      //      count 1 + tx
     B_V_EMPTY = 3,     //      count 1 (commit after the unit's last dP^T)
     B_Q_FULL = 4,      // [2]  count 1 + tx (Q tile + lse2 / D vectors, stage t % 2)
-    B_Q_EMPTY = 6,     // [2]  count 1 (commit after dK)
+    B_Q_EMPTY = 6,     // [2]  count 2 (commit after dK; the writer, once the dQ^T staged
+                       //      in this stage has been read)
     B_DY_FULL = 8,     // [2]  count 1 + tx
     B_DY_EMPTY = 10,   // [2]  count 2 (commit after dV and dP^T; the writer, once the dQ^T
                        //      staged in this stage has been read)
@@ -118,8 +122,7 @@ enum : int {
     B_UNIT_FULL = 22,  // [2]  count 1
     B_UNIT_EMPTY = 24, // [2]  count 10 (MMA + 8 compute warps + writer)
     B_DRAIN = 26,      //      count 1 (commit)
-    B_STG_FULL = 27,   //      count 256 (dQ^T staged)
-    B_STG_FREE = 28,   //      count 1 (the writer's TMA has read the staging)
+    B_STG_FULL = 27,   // [2]  count 256 (dQ^T of a tile of stage t % 2 staged)
 };
 
 // misc words
@@ -188,8 +191,8 @@ __device__ __forceinline__ bool wait_k(const Smem &sm, int bar, uint32_t k, cons
     return true;
 }
 
-// Single-thread polling variant for the UMMA issuer: mbarrier.test_wait does
-// not suspend the thread, so it reacts to the phase flip without a resume delay.
+// Non-suspending phase test: mbarrier.test_wait reacts to the phase flip
+// without the resume delay of a suspended try_wait.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -202,16 +205,23 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool wait_poll(const Smem &sm, int bar, uint32_t k, const GradArgs &a)
+
+// Polling variant for a whole converged warp (the UMMA issuer): every lane
+// tests the phase and the warp leaves together, as soon as any lane has seen
+// it complete (the barrier cannot move a further phase before this warp acts).
+__device__ __forceinline__ bool wait_uni(const Smem &sm, int bar, uint32_t k, const GradArgs &a)
 {
     uint64_t *b = sm.bar(bar);
     const uint32_t parity = k & 1u;
     const long long t0 = clock64();
-    while (!mbar_test_wait(b, parity)) {
-        if (*sm.abort_flag()) return false;
-        if (clock64() - t0 > a.wait_limit_cycles) {
-            set_status(a.status, TND_ERR_DEVICE_TIMEOUT, (k << 12) | ((threadIdx.x >> 5) << 6) | (uint32_t)bar);
-            *sm.abort_flag() = 1;
+    while (!__any_sync(0xffffffffu, mbar_test_wait(b, parity))) {
+        if (__any_sync(0xffffffffu, *sm.abort_flag() != 0)) return false;
+        if (__any_sync(0xffffffffu, clock64() - t0 > a.wait_limit_cycles)) {
+            if ((threadIdx.x & 31) == 0) {
+                set_status(a.status, TND_ERR_DEVICE_TIMEOUT, (k << 12) | ((threadIdx.x >> 5) << 6) | (uint32_t)bar);
+                *sm.abort_flag() = 1;
+            }
+            __syncwarp();
             return false;
         }
     }
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(sm.bar(B_V_EMPTY), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(sm.bar(B_Q_FULL + i), 1);
-            mbar_init(sm.bar(B_Q_EMPTY + i), 1);
+            mbar_init(sm.bar(B_Q_EMPTY + i), 2);
             mbar_init(sm.bar(B_DY_FULL + i), 1);
             mbar_init(sm.bar(B_DY_EMPTY + i), 2);
             mbar_init(sm.bar(B_P_READY + i), 128);
@@ -430,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(sm.bar(B_ACC_FREE), kComputeThreads);
         mbar_init(sm.bar(B_DRAIN), 1);
         mbar_init(sm.bar(B_STG_FULL), kComputeThreads);
-        mbar_init(sm.bar(B_STG_FREE), 1);
+        mbar_init(sm.bar(B_STG_FULL + 1), kComputeThreads);
         *sm.abort_flag() = 0;
         fence_mbar_init();
     }
@@ -550,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
+        {
             const uint32_t idS = instr_desc_f16(BF16, 128, BR, false, false);     // S^T, dP^T
             const uint32_t idKV = instr_desc_f16(BF16, 128, HD, false, true);     // dV (A in TMEM), dK
             const uint32_t idQ = instr_desc_f16(BF16, 128, BR, true, true);       // dQ^T
@@ -571,23 +581,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             // S^T(t) = K Q(t)^T into the S buffer: dV(t - 1) has read Pd^T(t - 1)
             // (PV_DONE) and the compute warps have read P^T(t - 1) (their
-            // DS_READY(t - 1), awaited before every S^T but a unit's first)
+            // DS_READY(t - 1), awaited before)
             auto issue_s = [&](uint32_t g, bool first) -> bool {
                 const uint32_t s = g & 1u;
-                if (!wait_poll(sm, B_Q_FULL + s, g >> 1, a)) return false;
+                if (!wait_uni(sm, B_Q_FULL + s, g >> 1, a)) return false;
                 TRACE(EV_W_QFULL, g);
-                if (g >= 1 && !wait_poll(sm, B_PV_DONE, g - 1, a)) return false;
+                if (g >= 1 && !wait_uni(sm, B_PV_DONE, g - 1, a)) return false;
                 TRACE(EV_W_PVDONE, g);
-                if (first && !wait_poll(sm, B_K_FULL, ku, a)) return false;
+                if (first && !wait_uni(sm, B_K_FULL, ku, a)) return false;
                 TRACE(EV_W_KFULL, g);
                 tc_fence_after();
                 const uint64_t dq = desc_at(dQ_k0, s * G_::kQTile);
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     const uint32_t off = (kk >> 2) * kColBlk + (kk & 3) * 32;
-                    mma_ss(tmem + TM_S, desc_at(dK_k, off), desc_at(dq, off), idS, kk > 0);
+                    mma_ss_elect(tmem + TM_S, desc_at(dK_k, off), desc_at(dq, off), idS, kk > 0);
                 }
-                mma_commit(sm.bar(B_S_FULL));
+                mma_commit_elect(sm.bar(B_S_FULL));
                 TRACE(EV_I_S, g);
                 return true;
             };
@@ -595,29 +605,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             // read dQ^T(t - 1) out of it
             auto issue_dp = [&](uint32_t g, bool first) -> bool {
                 const uint32_t s = g & 1u;
-                if (!wait_poll(sm, B_DY_FULL + s, g >> 1, a)) return false;
+                if (!wait_uni(sm, B_DY_FULL + s, g >> 1, a)) return false;
                 TRACE(EV_W_DYFULL, g);
-                if (g >= 1 && !wait_poll(sm, B_DQ_FREE, g - 1, a)) return false;
+                if (g >= 1 && !wait_uni(sm, B_DQ_FREE, g - 1, a)) return false;
                 TRACE(EV_W_DQFREE, g);
-                if (first && !wait_poll(sm, B_V_FULL, ku, a)) return false;
+                if (first && !wait_uni(sm, B_V_FULL, ku, a)) return false;
                 TRACE(EV_W_VFULL, g);
                 tc_fence_after();
                 const uint64_t dy = desc_at(dY_k0, s * G_::kQTile);
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     const uint32_t off = (kk >> 2) * kColBlk + (kk & 3) * 32;
-                    mma_ss(tmem + TM_DP, desc_at(dV_k, off), desc_at(dy, off), idS, kk > 0);
+                    mma_ss_elect(tmem + TM_DP, desc_at(dV_k, off), desc_at(dy, off), idS, kk > 0);
                 }
-                mma_commit(sm.bar(B_DP_FULL));
+                mma_commit_elect(sm.bar(B_DP_FULL));
                 TRACE(EV_I_DP, g);
                 return true;
             };
-            // Per tile t: dV(t); dP^T(t) (a unit's first tile: before the loop);
-            // then, once dS^T(t) is ready, S^T(t + 1), dK(t), dQ^T(t).  The
-            // compute warps' P^T(t + 1) thus overlaps dK(t) and dQ^T(t).
+            // Per tile t: dV(t) once P^T(t) is in; dK(t) and dQ^T(t) once dS^T(t)
+            // is; then S^T(t + 1) and, once the epilogue has read dQ^T(t) out of
+            // the dP buffer, dP^T(t + 1).  A unit's first S^T / dP^T come before
+            // its loop.
             while (ok) {
                 int u;
-                if (!read_unit1(sm, ui, a, u)) break;
+                if (!read_unit(sm, ui, a, u)) break;
                 ++ui;
                 if (u < 0) break;
                 const UnitInfo U = unit_info(a, u);
@@ -628,22 +639,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (uint32_t g = g0; g < g_end; ++g) {
                     const uint32_t s = g & 1u;
                     const bool first = g == g0;
-                    if (first && ku >= 1 && !wait_poll(sm, B_ACC_FREE, ku - 1, a)) {
+                    if (first && ku >= 1 && !wait_uni(sm, B_ACC_FREE, ku - 1, a)) {
                         ok = false;
                         break;
                     }
                     TRACE(EV_W_ACCFREE, g);
                     // dV += Pd^T dY(t): A = Pd^T (TMEM, packed), B = dY MN-major (N = HD);
-                    // the two K halves follow the two softmax halves.  dV(t) comes before
-                    // dP^T(t) (a unit's first tile aside), so it waits for dY(t) itself.
-                    if (!first && !wait_poll(sm, B_DY_FULL + s, g >> 1, a)) {
-                        ok = false;
-                        break;
-                    }
+                    // the two K halves follow the two softmax halves.  dY(t) is in:
+                    // dP^T(t) was issued after its DY_FULL.
                     const uint64_t dym = desc_at(dY_m0, s * G_::kQTile);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        if (!wait_poll(sm, B_P_READY + hf, g, a)) {
+                        if (!wait_uni(sm, B_P_READY + hf, g, a)) {
                             ok = false;
                             break;
                         }
@@ -652,49 +659,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kq = 0; kq < 4; ++kq) {
                             const int kk = 4 * hf + kq;
-                            mma_ts(tmem + 0, tmem + TM_S + pk_col(kk), desc_at(dym, kk * 2048), idKV,
-                                   (!first || kk > 0));
+                            mma_ts_elect(tmem + 0, tmem + TM_S + pk_col(kk), desc_at(dym, kk * 2048), idKV,
+                                         (!first || kk > 0));
                         }
                     }
                     if (!ok) break;
-                    mma_commit(sm.bar(B_PV_DONE));
+                    mma_commit_elect(sm.bar(B_PV_DONE));
+                    mma_commit_elect(sm.bar(B_DY_EMPTY + s));      // dP^T(t) and dV(t) issued: dY(t)'s readers
+                    if (g + 1 == g_end) mma_commit_elect(sm.bar(B_V_EMPTY));   // the unit's last dP^T issued
                     TRACE(EV_I_DV, g);
-                    if (!first && !issue_dp(g, false)) {
-                        ok = false;
-                        break;
-                    }
-                    mma_commit(sm.bar(B_DY_EMPTY + s));      // dP^T(t) and dV(t) issued: dY(t)'s readers
-                    if (g + 1 == g_end) mma_commit(sm.bar(B_V_EMPTY));   // the unit's last dP^T issued
-                    if (!wait_poll(sm, B_DS_READY, g, a)) {
+                    if (!wait_uni(sm, B_DS_READY, g, a)) {
                         ok = false;
                         break;
                     }
                     TRACE(EV_W_DS, g);
                     tc_fence_after();
-                    if (g + 1 < g_end && !issue_s(g + 1, false)) {
-                        ok = false;
-                        break;
-                    }
                     // dK += dS^T Q(t): A = dS^T smem K-major, B = Q MN-major
                     const uint64_t dqm = desc_at(dQ_m0, s * G_::kQTile);
 #pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kColBlk + (kk & 3) * 32;
-                        mma_ss(tmem + HD, desc_at(dS_k, off), desc_at(dqm, kk * 2048), idKV, (!first || kk > 0));
+                        mma_ss_elect(tmem + HD, desc_at(dS_k, off), desc_at(dqm, kk * 2048), idKV, (!first || kk > 0));
                     }
-                    mma_commit(sm.bar(B_Q_EMPTY + s));
+                    mma_commit_elect(sm.bar(B_Q_EMPTY + s));
                     TRACE(EV_I_DK, g);
                     // dQ^T = K^T dS^T into the dP buffer (the compute warps have read
                     // dP^T(t)): A = K MN-major (M = 128 features), B = dS^T MN-major
 #pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
-                        mma_ss(tmem + TM_DP, desc_at(dK_m, kk * 2048), desc_at(dS_m, kk * 2048), idQ, kk > 0);
+                        mma_ss_elect(tmem + TM_DP, desc_at(dK_m, kk * 2048), desc_at(dS_m, kk * 2048), idQ, kk > 0);
                     }
-                    mma_commit(sm.bar(B_DQ_FULL));
+                    mma_commit_elect(sm.bar(B_DQ_FULL));
                     TRACE(EV_I_DQ, g);
                     if (g + 1 == g_end) {
-                        mma_commit(sm.bar(B_ACC_FULL));
-                        mma_commit(sm.bar(B_K_EMPTY));
+                        mma_commit_elect(sm.bar(B_ACC_FULL));
+                        mma_commit_elect(sm.bar(B_K_EMPTY));
+                    } else if (!issue_s(g + 1, false) || !issue_dp(g + 1, false)) {
+                        ok = false;
+                        break;
                     }
                 }
                 if (!ok) break;
@@ -702,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ku;
             }
             // every issued UMMA must finish before TMEM is released
-            mma_commit(sm.bar(B_DRAIN));
+            mma_commit_elect(sm.bar(B_DRAIN));
             const long long t0 = clock64();
             while (!mbar_try_wait(sm.bar(B_DRAIN), 0) && clock64() - t0 < a.wait_limit_cycles) {
             }
@@ -713,8 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Two warps per TMEM lane quarter: warps 2-5 take q columns 0-63 of
         // the tile, warps 6-9 columns 64-127 (the same split serves dQ^T,
         // whose TMEM columns are q rows, and dK / dV, whose columns are
-        // features).  Per tile t: P^T(t); the epilogue of tile t - 1 (before
-        // P^T(t) when t starts a unit); dS^T(t).
+        // features).  Per tile t: P^T(t); dS^T(t); the epilogue of tile t.
         const int quarter = warp & 3;
         const int half = (warp - kComputeWarp0) >> 2;
         const int ln = quarter * 32 + lane;                 // TMEM lane: kv row (S^T, dP^T, dK, dV) or feature (dQ^T)
@@ -768,44 +769,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ku;
             return true;
         };
-        // Epilogue of tile pg (the previous tile): dQ^T out of TMEM (thread =
-        // feature ln, q rows 64 half .. + 63), the dP buffer released, the
-        // unit's dK / dV out if pg ended its unit, then dQ^T staged as fp32
-        // [64 q rows][HD] for the writer warp: rows 0-63 of the tile in the
-        // dY stage of tile pg (its readers are done), rows 64-127 in the dS^T
-        // buffer (dK(pg) and dQ^T(pg) have read it).
-        bool pend = false;
-        uint32_t pg = 0;
-        UnitInfo pU;
-        bool p_last = false;
-        auto epilogue = [&]() -> bool {
-            if (!wait_warp(sm, B_DQ_FULL, pg, a)) return false;
-            TRACE(EV_C_DQFULL, pg);
+        // Epilogue of tile g: dQ^T out of TMEM (thread = feature ln, q rows
+        // 64 half .. + 63), the dP buffer released, the unit's dK / dV out if
+        // g ends its unit, then dQ^T staged as fp32 [64 q rows][HD] for the
+        // writer warp: rows 0-63 of the tile in its dY stage, rows 64-127 in
+        // its Q stage.  DQ_FULL(g) follows dV(g), dP^T(g), dK(g) and dQ^T(g):
+        // every reader of both stages and of the dS^T buffer is done.
+        auto epilogue = [&](uint32_t g, const UnitInfo &U, bool last) -> bool {
+            if (!wait_warp(sm, B_DQ_FULL, g, a)) return false;
+            TRACE(EV_C_DQFULL, g);
             tc_fence_after();
-            // two 32-column halves, staged one after the other (fewer live
-            // registers: the softmax's P^T is held across this epilogue); the dP
-            // buffer is released once both have been read
+            // both 32-column halves loaded together; the dP buffer is released
+            // as soon as they are in registers
+            const uint32_t s = g & 1u;
             const uint32_t dq_addr = tmem + lane_addr + TM_DP + 64 * half;
-            float *stg = reinterpret_cast<float *>(
-                             sm.base + (half == 0 ? G_::OFF_DY + (pg & 1u) * G_::kQTile : G_::OFF_DS)) + ln;
+            float *stg = reinterpret_cast<float *>(sm.base + (half == 0 ? G_::OFF_DY : G_::OFF_Q) + s * G_::kQTile) + ln;
+            uint32_t v0[32], v1[32];
+            tmem_ld32_async(dq_addr, v0);
+            tmem_ld32_async(dq_addr + 32, v1);
+            tmem_wait_ld32(v0);
+            tmem_wait_ld32(v1);
+            tc_fence_before();
+            mbar_arrive(sm.bar(B_DQ_FREE));
+            TRACE(EV_C_DQFREE, g);
+            if (ln < HD) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t v[32];
-                tmem_ld32(dq_addr + 32 * hh, v);
-                if (hh == 1) {
-                    tc_fence_before();
-                    mbar_arrive(sm.bar(B_DQ_FREE));
-                    TRACE(EV_C_DQFREE, pg);
-                }
-                if (ln < HD) {
+                for (int c = 0; c < 32; ++c) stg[c * HD] = __uint_as_float(v0[c]);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) stg[(32 * hh + c) * HD] = __uint_as_float(v[c]);
-                }
+                for (int c = 0; c < 32; ++c) stg[(32 + c) * HD] = __uint_as_float(v1[c]);
             }
-            if (p_last && !unit_out(pU, false)) return false;
+            if (last && !unit_out(U, false)) return false;
             fence_async_smem();
-            mbar_arrive(sm.bar(B_STG_FULL));
-            TRACE(EV_C_EPIDONE, pg);
+            mbar_arrive(sm.bar(B_STG_FULL + s));
+            TRACE(EV_C_EPIDONE, g);
             return true;
         };
         while (ok) {
@@ -827,15 +823,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = __all_sync(0xffffffffu, keep == ~0ull);
                 KeepWin kw;
                 if (a.has_drop) keep_fetch(a, U.sd, h, qc0, (int64_t)U.jb * BC + quarter * 32, lane, kw);
-                // a unit's first S^T is issued after its first dP^T, which needs
-                // the previous tile's dQ^T read out: that epilogue goes first
-                if (t == 0 && pend) {
-                    if (!epilogue()) {
-                        ok = false;
-                        break;
-                    }
-                    pend = false;
-                }
                 if (!wait_warp(sm, B_Q_FULL + s, gt >> 1, a) || !wait_warp(sm, B_S_FULL, gt, a)) {
                     ok = false;
                     break;
@@ -886,17 +873,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_P_READY + half));
                 TRACE(EV_C_PDONE, gt);
-                if (pend) {
-                    if (!epilogue()) {
-                        ok = false;
-                        break;
-                    }
-                    pend = false;
-                }
                 // ---- phase 2: dS^T = P^T o (z dP^T - D) (P^T from registers: Pd^T is 0
                 // where dropout drops a key) into registers, then into the
-                // shared-memory dS^T buffer once the writer has read the staged
-                // dQ^T(t - 1) out of it.
+                // shared-memory dS^T buffer (dK(t - 1) and dQ^T(t - 1) have read it:
+                // the epilogue of t - 1 waited for DQ_FULL(t - 1)).
                 if (!wait_warp(sm, B_DP_FULL, gt, a)) {
                     ok = false;
                     break;
@@ -925,11 +905,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dsk[16 * ch + 2 * c4 + 1] = pack2<BF16>(pc[2] * (dp[2] - dv.z), pc[3] * (dp[3] - dv.w));
                     }
                 }
-                if (gt >= 1 && !wait_warp(sm, B_STG_FREE, gt - 1, a)) {
-                    ok = false;
-                    break;
-                }
-                TRACE(EV_C_CHAIN, gt);
                 uint8_t *row = sm.base + G_::OFF_DS + half * kColBlk + ln * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -940,21 +915,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(sm.bar(B_DS_READY));
                 TRACE(EV_C_DSDONE, gt);
-                pend = true;
-                pg = gt;
-                pU = U;
-                p_last = t + 1 == U.ntiles;
+                if (!epilogue(gt, U, t + 1 == U.ntiles)) {
+                    ok = false;
+                    break;
+                }
             }
         }
-        if (ok && pend) epilogue();
     } else {
         // ================================================================ dQ writer
         // For each tile, in order: once the compute warps have staged dQ^T,
         // waits until the (q block, head) counter shows that every earlier
         // contributor's update is complete, then stores (first contributor)
         // or adds (later ones) the two staged 64-row halves into the fp32
-        // accumulator with TMA, releases the staging buffers once they have
-        // been read, and advances the counter once the writes are complete.
+        // accumulator with TMA, releases the tile's Q and dY stages to the
+        // producer as each half has been read, and advances the counter once
+        // the writes are complete.
         if (lane == 0) {
             uint32_t ui = 0, gt = 0;
             bool ok = true;
@@ -970,7 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const QBlockInfo qi = a.qblk[qg];
                     int *flag = a.flags + (int64_t)qg * a.nq + h;
                     const int pos = qi.jhi - U.jb;
-                    if (!wait_k(sm, B_STG_FULL, gt, a)) {
+                    const uint32_t s = gt & 1u;
+                    if (!wait_k(sm, B_STG_FULL + s, gt >> 1, a)) {
                         ok = false;
                         break;
                     }
@@ -997,12 +973,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     TRACE(EV_W_CHAIN, gt);
                     const int z = (int)(U.sd.tq + (int64_t)qb * BR);
-                    // the half staged in the dS^T buffer first, as its own bulk
-                    // group: the compute warps wait for that buffer to be read
+                    // the half staged in the Q stage first, as its own bulk group:
+                    // the next Q load (needed sooner than the next dY) waits for it
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         const int hs = 1 - i;
-                        const uint8_t *stg = sm.base + (hs == 0 ? G_::OFF_DY + (gt & 1u) * G_::kQTile : G_::OFF_DS);
+                        const uint8_t *stg = sm.base + (hs == 0 ? G_::OFF_DY : G_::OFF_Q) + s * G_::kQTile;
                         const int64_t r0 = (int64_t)qb * BR + 64 * hs;
                         const int rows = (int)max((int64_t)0, min((int64_t)64, (int64_t)U.sd.sq - r0));
                         if (rows == 64) {
@@ -1019,10 +995,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit();
                     }
                     TRACE(EV_W_ISSUED, gt);
-                    bulk_wait_read1();                              // the dS^T-buffer half
-                    mbar_arrive(sm.bar(B_STG_FREE));
+                    bulk_wait_read1();                              // the Q-stage half
+                    mbar_arrive(sm.bar(B_Q_EMPTY + s));
                     bulk_wait_read0();                              // the dY-stage half
-                    mbar_arrive(sm.bar(B_DY_EMPTY + (gt & 1u)));
+                    mbar_arrive(sm.bar(B_DY_EMPTY + s));
                     TRACE(EV_W_READ, gt);
                     bulk_wait0();
                     fence_async_global();
@@ -1119,12 +1095,13 @@ cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
 }
 
 // dQ = scale * accumulator in the output dtype, one block per (128-row q
-// block, head), 4 features per thread with all loads of a thread issued
-// first; rows of q blocks that no kv block reaches get zeros.
+// block, head) with heads in x (blocks running together cover neighbouring
+// pieces of the same rows), 4 features per thread with all loads of a
+// thread issued first; rows of q blocks that no kv block reaches get zeros.
 template <typename Out>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(GradArgs a)
 {
-    const int qg = blockIdx.x, h = blockIdx.y;
+    const int h = blockIdx.x, qg = blockIdx.y;   // heads of a q block side by side: adjacent rows
     const int2 qr = a.qblk_rows[qg];
     const SeqDesc sd = a.seqs[qr.x];
     const bool covered = a.qblk[qg].jlo >= 0;
@@ -1173,7 +1150,7 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
 cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s)
 {
     if (a.n_qblk == 0) return cudaSuccess;
-    const dim3 grid((unsigned)a.n_qblk, (unsigned)a.nq);
+    const dim3 grid((unsigned)a.nq, (unsigned)a.n_qblk);
     if (a.dtype == TND_BF16) dq_finalize_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
     else dq_finalize_kernel<__half><<<grid, 256, 0, s>>>(a);
     return cudaGetLastError();

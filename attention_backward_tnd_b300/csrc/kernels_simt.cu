@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 
 // ---------------------------------------------------------------------------
 // gradient prepass: writes the blocked per-row vectors (padded rows
-// included), one block per (128-row q block, head).  Eight lanes share a
+// included), one block per (128-row q block, head), heads in x so that
+// blocks running together read neighbouring pieces of the same rows (q
+// blocks, at most 1M / 128 + B, fit y).  Eight lanes share a
 // row and read dY and O with 16-byte loads when the row length allows it
 // (D * sizeof(T) a multiple of 16, at most 256 bytes).  With tc_state it
 // also zeroes the dQ chain counters of the tensor-core gradient.
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
 {
     // block (q block qg, head h): 128 rows, 32 groups of 8 lanes, 4 rows per
     // group with all their loads issued before the sums
-    const int qg = blockIdx.x, h = blockIdx.y;
+    const int h = blockIdx.x, qg = blockIdx.y;   // heads of a q block side by side: adjacent rows
     const int lane = threadIdx.x & 31, sub = lane & 7, grp = threadIdx.x >> 3;
     const int2 qr = a.qblk_rows[qg];
     const SeqDesc sd = a.seqs[qr.x];
@@ -509,7 +511,7 @@ template <typename T, int DMAX> struct PrepassLaunch {
     static cudaError_t run(const GradArgs &a, bool tc_state, cudaStream_t s)
     {
         if (a.n_qblk == 0) return cudaSuccess;
-        const dim3 grid((unsigned)a.n_qblk, (unsigned)a.nq);
+        const dim3 grid((unsigned)a.nq, (unsigned)a.n_qblk);
         prepass_kernel<T><<<grid, 256, 0, s>>>(a, tc_state ? 1 : 0);
         return cudaGetLastError();
     }
