@@ -131,18 +131,20 @@ constexpr uint32_t MISC_TMEM = 0, MISC_RING = 1, MISC_ABORT = 3;
 #ifdef TND_TRACE
 // Diagnostic build only: a clock-stamped event log of the first kTraceCtas
 // CTAs, one ring per warp (lane 0 records): {clock64, (event << 24) | tile}.
+// The event count lives in a register of the recording thread (`n`), so an
+// event costs two fire-and-forget stores and no global round trip.
 constexpr int kTraceCtas = 2, kTraceLen = 8192;
 __device__ unsigned long long g_trace[kTraceCtas][11][kTraceLen][2];
 __device__ unsigned int g_trace_n[kTraceCtas][11];
 __device__ unsigned long long g_cta_span[1024][2];
-__device__ __forceinline__ void trace(uint32_t ev, uint32_t k)
+__device__ __forceinline__ void trace(uint32_t &n, uint32_t ev, uint32_t k)
 {
     if ((threadIdx.x & 31) != 0 || blockIdx.x >= kTraceCtas) return;
     const int w = threadIdx.x >> 5;
-    const unsigned i = g_trace_n[blockIdx.x][w]++;
+    const unsigned i = n++;
     if (i < (unsigned)kTraceLen) {
-        g_trace[blockIdx.x][w][i][0] = (unsigned long long)clock64();
-        g_trace[blockIdx.x][w][i][1] = ((unsigned long long)ev << 24) | (k & 0xffffffu);
+        ulonglong2 rec = make_ulonglong2((unsigned long long)clock64(), ((unsigned long long)ev << 24) | (k & 0xffffffu));
+        *reinterpret_cast<ulonglong2 *>(&g_trace[blockIdx.x][w][i][0]) = rec;
     }
 }
 __device__ __forceinline__ unsigned long long global_ns()
@@ -151,7 +153,7 @@ __device__ __forceinline__ unsigned long long global_ns()
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-#define TRACE(ev, k) trace((ev), (k))
+#define TRACE(ev, k) trace(trace_n, (ev), (k))
 #else
 #define TRACE(ev, k) ((void)0)
 #endif
@@ -394,7 +396,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return BF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
-template <bool BF16, int HD>
+// DROP = false: the kernel carries no dropout code, which keeps the compute
+// warps' loop small; DROP = true applies the keep-bits when the call has them.
+template <bool BF16, int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     grad_tc_kernel(const __grid_constant__ GradArgs a, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -461,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm.misc() + MISC_TMEM);
 #ifdef TND_TRACE
     if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_span[blockIdx.x][0] = global_ns();
+    uint32_t trace_n = 0;
 #endif
     uint32_t drain_arm[6] = {0, 0, 0, 0, 0, 0};   // producer: phases armed per load barrier
 
@@ -822,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t keep = keep_columns(a, U.sd, qc0, jj);
                 const bool full = __all_sync(0xffffffffu, keep == ~0ull);
                 KeepWin kw;
-                if (a.has_drop) keep_fetch(a, U.sd, h, qc0, (int64_t)U.jb * BC + quarter * 32, lane, kw);
+                if (DROP && a.has_drop) keep_fetch(a, U.sd, h, qc0, (int64_t)U.jb * BC + quarter * 32, lane, kw);
                 if (!wait_warp(sm, B_Q_FULL + s, gt >> 1, a) || !wait_warp(sm, B_S_FULL, gt, a)) {
                     ok = false;
                     break;
@@ -832,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *vec = reinterpret_cast<const float *>(sm.base + G_::OFF_VEC + s * G_::kVecBytes);
                 const float4 *lse4 = reinterpret_cast<const float4 *>(vec) + 16 * half;
                 const float4 *dvec4 = reinterpret_cast<const float4 *>(vec + BR) + 16 * half;
-                const uint64_t zb = a.has_drop ? keep_transpose(kw, lane) : ~0ull;
+                const uint64_t zb = (DROP && a.has_drop) ? keep_transpose(kw, lane) : ~0ull;
                 // ---- phase 1: P^T from S^T, kept in registers (fp32) for dS; each
                 // 32-column chunk of S^T gets Pd^T = P^T o z packed in the dtype in
                 // its first 16 columns (the dV operand)
@@ -856,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 32; ++c) p[32 * ch + c] = ((kh >> c) & 1u) ? p[32 * ch + c] : 0.0f;
                     }
                     uint32_t pk[16];
-                    if (a.has_drop) {
+                    if (DROP && a.has_drop) {
                         const uint32_t zh = (uint32_t)(zb >> (32 * ch));
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
@@ -895,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float4 dv = dvec4[8 * ch + c4];
                         float dp[4] = {__uint_as_float(raw[4 * c4]), __uint_as_float(raw[4 * c4 + 1]),
                                        __uint_as_float(raw[4 * c4 + 2]), __uint_as_float(raw[4 * c4 + 3])};
-                        if (a.has_drop) {
+                        if (DROP && a.has_drop) {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 dp[e] = ((zh >> (4 * c4 + e)) & 1u) ? dp[e] * a.inv_keep : 0.0f;
@@ -1016,6 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 #ifdef TND_TRACE
     if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_span[blockIdx.x][1] = global_ns();
+    if ((threadIdx.x & 31) == 0 && blockIdx.x < kTraceCtas) g_trace_n[blockIdx.x][threadIdx.x >> 5] = trace_n;
 #endif
     if (warp == 1) {
         tc_fence_after();
@@ -1078,7 +1084,7 @@ bool make_acc_map(CUtensorMap *m, const float *ptr, int64_t rows, int64_t heads,
     return r == CUDA_SUCCESS;
 }
 
-template <bool BF16, int HD>
+template <bool BF16, int HD, bool DROP>
 cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
 {
     CUtensorMap mq, mk, mv, mdy, mdq;
@@ -1088,9 +1094,10 @@ cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
         return cudaErrorInvalidValue;
     const int grid = std::min<int>(a.num_sms, a.n_units);
     constexpr uint32_t smem = Geo<HD>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel<BF16, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(grad_tc_kernel<BF16, HD, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    grad_tc_kernel<BF16, HD><<<grid, kThreads, smem, s>>>(a, mq, mk, mv, mdy, mdq);
+    grad_tc_kernel<BF16, HD, DROP><<<grid, kThreads, smem, s>>>(a, mq, mk, mv, mdy, mdq);
     return cudaGetLastError();
 }
 
@@ -1142,8 +1149,15 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
 {
     if (a.n_units == 0) return cudaSuccess;
     const bool bf16 = a.dtype == TND_BF16;
-    if (a.d == 128) return bf16 ? launch_hd<true, 128>(a, s) : launch_hd<false, 128>(a, s);
-    if (a.d == 64) return bf16 ? launch_hd<true, 64>(a, s) : launch_hd<false, 64>(a, s);
+    const bool drop = a.has_drop != 0;
+    if (a.d == 128) {
+        if (bf16) return drop ? launch_hd<true, 128, true>(a, s) : launch_hd<true, 128, false>(a, s);
+        return drop ? launch_hd<false, 128, true>(a, s) : launch_hd<false, 128, false>(a, s);
+    }
+    if (a.d == 64) {
+        if (bf16) return drop ? launch_hd<true, 64, true>(a, s) : launch_hd<true, 64, false>(a, s);
+        return drop ? launch_hd<false, 64, true>(a, s) : launch_hd<false, 64, false>(a, s);
+    }
     return cudaErrorInvalidValue;
 }
 
