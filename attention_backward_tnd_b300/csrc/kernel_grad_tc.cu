@@ -1103,40 +1103,40 @@ cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
 
 // dQ = scale * accumulator in the output dtype, one block per (128-row q
 // block, head) with heads in x (blocks running together cover neighbouring
-// pieces of the same rows), 4 features per thread with all loads of a
-// thread issued first; rows of q blocks that no kv block reaches get zeros.
-template <typename Out>
-__global__ void __launch_bounds__(256) dq_finalize_kernel(GradArgs a)
+// pieces of the same rows); rows of q blocks that no kv block reaches get
+// zeros.  Thread t takes float4 column t % (HD / 4) of every (256 / (HD / 4))-th
+// row, four rows' loads in flight before their stores, eight blocks per SM.
+template <typename Out, int HD>
+__global__ void __launch_bounds__(256, 8) dq_finalize_kernel(GradArgs a)
 {
-    const int h = blockIdx.x, qg = blockIdx.y;   // heads of a q block side by side: adjacent rows
+    constexpr int kF4 = HD / 4;                 // float4 per row
+    constexpr int kRowStep = 256 / kF4;         // rows per pass of the block
+    constexpr int kBatch = 4;
+    const int h = blockIdx.x, qg = blockIdx.y;
     const int2 qr = a.qblk_rows[qg];
     const SeqDesc sd = a.seqs[qr.x];
     const bool covered = a.qblk[qg].jlo >= 0;
     const int rows = min(BR, sd.sq - qr.y);
-    const int per_row = a.d / 4;                    // 16 or 32 float4 per row
-    const int total = rows * per_row;
+    const int c4 = threadIdx.x % kF4, r0 = threadIdx.x / kF4;
+    const int64_t stride = (int64_t)a.nq * HD;                  // elements between consecutive rows
+    const int64_t base = ((sd.tq + qr.y + r0) * a.nq + h) * (int64_t)HD + 4 * c4;
     Out *dQ = reinterpret_cast<Out *>(a.dq);
-    constexpr int kBatch = 8;
-    for (int e0 = threadIdx.x; e0 < total; e0 += kBatch * 256) {
+    for (int rb = 0; rb < BR; rb += kBatch * kRowStep) {
         float4 v[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-            const int e = e0 + 256 * k;
-            const int rr = e / per_row, c4 = e - rr * per_row;
-            const int64_t off = ((sd.tq + qr.y + rr) * a.nq + h) * (int64_t)a.d + 4 * c4;
-            v[k] = (covered && e < total) ? __ldcs(reinterpret_cast<const float4 *>(a.dqacc + off))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int r = r0 + rb + k * kRowStep;
+            v[k] = (covered && r < rows) ? __ldcs(reinterpret_cast<const float4 *>(a.dqacc + base + (rb + k * kRowStep) * stride))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-            const int e = e0 + 256 * k;
-            if (e >= total) break;
-            const int rr = e / per_row, c4 = e - rr * per_row;
-            const int64_t off = ((sd.tq + qr.y + rr) * a.nq + h) * (int64_t)a.d + 4 * c4;
+            const int r = r0 + rb + k * kRowStep;
+            if (r >= rows) break;
             uint2 pk;
             pk.x = pack2<std::is_same<Out, __nv_bfloat16>::value>(v[k].x * a.scale, v[k].y * a.scale);
             pk.y = pack2<std::is_same<Out, __nv_bfloat16>::value>(v[k].z * a.scale, v[k].w * a.scale);
-            *reinterpret_cast<uint2 *>(dQ + off) = pk;
+            *reinterpret_cast<uint2 *>(dQ + base + (rb + k * kRowStep) * stride) = pk;
         }
     }
 }
@@ -1165,8 +1165,14 @@ cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s)
 {
     if (a.n_qblk == 0) return cudaSuccess;
     const dim3 grid((unsigned)a.nq, (unsigned)a.n_qblk);
-    if (a.dtype == TND_BF16) dq_finalize_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
-    else dq_finalize_kernel<__half><<<grid, 256, 0, s>>>(a);
+    const bool bf16 = a.dtype == TND_BF16;
+    if (a.d == 128) {
+        if (bf16) dq_finalize_kernel<__nv_bfloat16, 128><<<grid, 256, 0, s>>>(a);
+        else dq_finalize_kernel<__half, 128><<<grid, 256, 0, s>>>(a);
+    } else {
+        if (bf16) dq_finalize_kernel<__nv_bfloat16, 64><<<grid, 256, 0, s>>>(a);
+        else dq_finalize_kernel<__half, 64><<<grid, 256, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 

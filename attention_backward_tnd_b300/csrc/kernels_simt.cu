@@ -183,6 +183,17 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
     const T *dY = (const T *)a.dy, *O = (const T *)a.o;
     const bool vec = ((a.d * (int)sizeof(T)) & 15) == 0 && a.d * (int)sizeof(T) <= 256;
     const int chunks = a.d * (int)sizeof(T) / 16;          // 16-byte chunks per row (at most 16)
+    // the forward's max and sum of the group's rows, requested with dY and O
+    // (one lane per row reads them)
+    float mv[4], lv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t i = (int64_t)qr.y + grp + 32 * k;
+        const int64_t r = (sd.tq + i) * a.nq + h;
+        const bool rd = sub == 0 && i < sd.sq;
+        mv[k] = rd ? __ldg(a.smax + r * 8) : 0.0f;
+        lv[k] = rd ? __ldg(a.ssum + r * 8) : 0.0f;
+    }
     float dot[4];
     if (vec) {
         uint4 y[4][2], o[4][2];
@@ -225,8 +236,7 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
             a.lse2[w] = INFINITY;
             if (a.has_sink) a.sinkrow[w] = 0.0f;
         } else {
-            const int64_t r = (sd.tq + i) * a.nq + h;
-            const float m = a.smax[r * 8], l = a.ssum[r * 8];
+            const float m = mv[k], l = lv[k];
             const bool live = l > 0.0f;
             a.drow[w] = d;
             a.lse2[w] = live ? m * kLog2e + lg2(l) : INFINITY;
