@@ -463,6 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm.misc() + MISC_TMEM);
+    // launched as a programmatic dependent of the prepass: the set-up above
+    // overlaps its tail; its vectors and counters are read only from here on
+    griddep_wait();
 #ifdef TND_TRACE
     if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_span[blockIdx.x][0] = global_ns();
     uint32_t trace_n = 0;
@@ -1023,6 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && blockIdx.x < 1024) g_cta_span[blockIdx.x][1] = global_ns();
     if ((threadIdx.x & 31) == 0 && blockIdx.x < kTraceCtas) g_trace_n[blockIdx.x][threadIdx.x >> 5] = trace_n;
 #endif
+    griddep_launch_dependents();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -1097,8 +1101,8 @@ cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
     cudaError_t e =
         cudaFuncSetAttribute(grad_tc_kernel<BF16, HD, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    grad_tc_kernel<BF16, HD, DROP><<<grid, kThreads, smem, s>>>(a, mq, mk, mv, mdy, mdq);
-    return cudaGetLastError();
+    return launch_dependent(grad_tc_kernel<BF16, HD, DROP>, dim3(grid), dim3(kThreads), smem, s, a, mq, mk, mv, mdy,
+                            mdq);
 }
 
 // dQ = scale * accumulator in the output dtype, one block per (128-row q
@@ -1113,6 +1117,7 @@ __global__ void __launch_bounds__(256, 8) dq_finalize_kernel(GradArgs a)
     constexpr int kRowStep = 256 / kF4;         // rows per pass of the block
     constexpr int kBatch = 4;
     const int h = blockIdx.x, qg = blockIdx.y;
+    griddep_wait();   // programmatic dependent of the gradient kernel
     const int2 qr = a.qblk_rows[qg];
     const SeqDesc sd = a.seqs[qr.x];
     const bool covered = a.qblk[qg].jlo >= 0;
@@ -1166,14 +1171,11 @@ cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s)
     if (a.n_qblk == 0) return cudaSuccess;
     const dim3 grid((unsigned)a.nq, (unsigned)a.n_qblk);
     const bool bf16 = a.dtype == TND_BF16;
-    if (a.d == 128) {
-        if (bf16) dq_finalize_kernel<__nv_bfloat16, 128><<<grid, 256, 0, s>>>(a);
-        else dq_finalize_kernel<__half, 128><<<grid, 256, 0, s>>>(a);
-    } else {
-        if (bf16) dq_finalize_kernel<__nv_bfloat16, 64><<<grid, 256, 0, s>>>(a);
-        else dq_finalize_kernel<__half, 64><<<grid, 256, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.d == 128)
+        return bf16 ? launch_dependent(dq_finalize_kernel<__nv_bfloat16, 128>, grid, dim3(256), 0, s, a)
+                    : launch_dependent(dq_finalize_kernel<__half, 128>, grid, dim3(256), 0, s, a);
+    return bf16 ? launch_dependent(dq_finalize_kernel<__nv_bfloat16, 64>, grid, dim3(256), 0, s, a)
+                : launch_dependent(dq_finalize_kernel<__half, 64>, grid, dim3(256), 0, s, a);
 }
 
 }  // namespace tnd

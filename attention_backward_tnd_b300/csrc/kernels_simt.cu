@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
         }
     }
     if (tc_state && threadIdx.x == 0) a.flags[(int64_t)qg * a.nq + h] = 0;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the gradient kernel may be scheduled
 }
 
 // ---------------------------------------------------------------------------

@@ -352,6 +352,12 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int *p)
 // makes an earlier relaxed read act as an acquire for what follows
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled (it still waits for this grid in griddep_wait), and wait for the
+// previous kernel's completion and memory.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void st_relaxed_gpu(int *p, int v)
 {
     asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "../../include/tnd_attn.h"
 
@@ -172,6 +173,26 @@ struct FwdArgs {
     int64_t wait_limit_cycles;
     int32_t num_sms;
 };
+
+// Launches `kernel` as a programmatic dependent of the previous kernel on
+// stream s: it may be scheduled before that kernel finishes and must call
+// griddepcontrol.wait before reading what that kernel wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernel launchers (each returns the CUDA error of its launch).
 // Packs the [rows][cols] attention-mask bytes into keep bits: keep_q (row i,
