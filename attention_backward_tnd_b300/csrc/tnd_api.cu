@@ -214,6 +214,9 @@ struct Plan {
     std::vector<unsigned char> image;  // status words + plan arrays, as copied to the workspace
 };
 
+// L2 share (bytes) for the q-side tiles of the gradient units that run together.
+constexpr int64_t kL2GroupBytes = int64_t(48) << 20;
+
 // Union of the kept key ranges of query rows [r0, r1) (empty: lo > hi).
 void rows_union(const MaskSpec &m, int64_t sq, int64_t skv, int64_t prefix_n, int64_t r0, int64_t r1,
                 int64_t &ulo, int64_t &uhi)
@@ -296,12 +299,6 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         gw.push_back({work, (int32_t)b});
     }
     if (!with_units) return;
-    // Sequences with the most work first; within a sequence, kv blocks in
-    // descending order (every kv head's chain is dispatched in chain order, so
-    // no unit ever waits on one not yet handed out) with all kv heads of a
-    // block together.  Under a causal mask the low kv blocks carry the most
-    // tiles; interleaving the heads makes the last units handed out similar in
-    // size instead of one head's largest blocks, which keeps the tail short.
     // forward units: every (q block, head), q blocks with the longest kv
     // range first (heads of a q block together)
     {
@@ -312,16 +309,30 @@ void build_plan(const Problem &p, bool with_units, Plan &pl)
         for (int q : order)
             for (int64_t h = 0; h < p.nq; ++h) pl.fwd_units.push_back(make_int2(q, (int)h));
     }
+    // Gradient units: sequences with the most work first.  Within a
+    // sequence the kv heads go in groups, and a group's kv blocks in
+    // descending order (every kv head's chain is dispatched in chain order,
+    // so no unit ever waits on one not yet handed out) with the group's heads
+    // of a block together: under a causal mask the low kv blocks carry the
+    // most tiles, and interleaving heads makes the last units of a group
+    // similar in size.  A group holds as many kv heads as keep the q-side
+    // tiles its units sweep (Q, dY and the fp32 dQ accumulator of every q
+    // block of the group's query heads) within kL2GroupBytes, so the units
+    // running together re-read those tiles from L2 rather than from HBM.
     std::stable_sort(gw.begin(), gw.end(), [](const GroupWork &x, const GroupWork &y) { return x.work > y.work; });
+    const int64_t tile_bytes = (int64_t)kQBlock * p.d * (2 + 2 + 4);   // Q, dY (16-bit) and fp32 dQ rows
     for (const GroupWork &w : gw) {
-        for (GradUnit u : seq_units[w.b]) {
-            for (int64_t g = 0; g < p.nkv; ++g) {
-                u.g = (int32_t)g;
-                pl.units.push_back(u);
+        const int64_t per_head = G * (int64_t)pl.seqs[w.b].nqblk * tile_bytes;
+        const int64_t hg = std::max<int64_t>(1, std::min<int64_t>(p.nkv, kL2GroupBytes / std::max<int64_t>(1, per_head)));
+        for (int64_t g0 = 0; g0 < p.nkv; g0 += hg) {
+            for (GradUnit u : seq_units[w.b]) {
+                for (int64_t g = g0; g < std::min(p.nkv, g0 + hg); ++g) {
+                    u.g = (int32_t)g;
+                    pl.units.push_back(u);
+                }
             }
         }
     }
-    (void)G;
 }
 
 // ---------------------------------------------------------------------------
@@ -403,12 +414,13 @@ void build_image(Plan &pl)
 // that repeat a problem (every training step of a fixed batch) reuse the
 // plan instead of rebuilding it.  Small LRU, shared by all threads.
 struct PlanKey {
-    int64_t batch, nq, nkv, mode, pre, next;
+    int64_t batch, nq, nkv, d, mode, pre, next;
     bool with_units, has_amask;
     std::vector<int64_t> cuq, cukv, prefix;
     bool operator==(const PlanKey &o) const
     {
-        return batch == o.batch && nq == o.nq && nkv == o.nkv && mode == o.mode && pre == o.pre && next == o.next &&
+        return batch == o.batch && nq == o.nq && nkv == o.nkv && d == o.d && mode == o.mode && pre == o.pre &&
+               next == o.next &&
                with_units == o.with_units && has_amask == o.has_amask && cuq == o.cuq && cukv == o.cukv &&
                prefix == o.prefix;
     }
@@ -419,7 +431,7 @@ std::mutex g_plan_mu;
 
 std::shared_ptr<const Plan> get_plan(const Problem &p, bool with_units)
 {
-    PlanKey key{p.batch, p.nq, p.nkv, p.mode, p.pre, p.next, with_units, p.has_amask,
+    PlanKey key{p.batch, p.nq, p.nkv, p.d, p.mode, p.pre, p.next, with_units, p.has_amask,
                 std::vector<int64_t>(p.cuq, p.cuq + p.batch + 1), std::vector<int64_t>(p.cukv, p.cukv + p.batch + 1),
                 p.prefix ? std::vector<int64_t>(p.prefix, p.prefix + p.batch) : std::vector<int64_t>()};
     {

@@ -224,28 +224,55 @@ def test_plan_covers_every_kept_tile_once_in_chain_order(case):
         assert js == sorted(js, reverse=True), (b, g, qb, js)
 
 
-@pytest.mark.parametrize("case", range(len(PLANS)))
-def test_plan_hands_out_kv_heads_of_a_block_together(case):
-    # units of one sequence come kv block by kv block (descending), every kv
-    # head of a block in a row; sequences with more tiles come first
-    sq, skv, nq, nkv, mode, pre, nxt, prefix = _plan_case(case)
+L2_GROUP_BYTES = 48 << 20       # q-side bytes the units of one head group may sweep (tnd_api.cu)
+
+
+def _check_unit_order(sq, skv, nq, nkv, mode, pre, nxt, prefix, d=128):
+    # per sequence (more tiles first): kv heads in groups sized to the L2
+    # share; within a group, kv block by kv block (descending), the group's
+    # heads of a block in a row
     cu_q = np.concatenate([[0], np.cumsum(sq)])
     cu_kv = np.concatenate([[0], np.cumsum(skv)])
     st, units, _ = tnd.tnd_attn_grad_plan(len(sq), cu_q, cu_kv, nq, nkv, pre, nxt, mode, prefix=prefix)
     assert st == tnd.TND_OK
-    groups = [units[i:i + nkv] for i in range(0, len(units), nkv)]
-    for grp in groups:
-        assert len(set(grp[:, 0])) == 1 and len(set(grp[:, 2])) == 1, grp
-        assert list(grp[:, 1]) == list(range(nkv)), grp
-    seq_order = []
-    for grp in groups:
-        b, j = int(grp[0, 0]), int(grp[0, 2])
-        if not seq_order or seq_order[-1][0] != b:
-            seq_order.append((b, []))
-        seq_order[-1][1].append(j)
-    assert len({b for b, _ in seq_order}) == len(seq_order), "a sequence's units are split"
-    for b, js in seq_order:
-        assert js == sorted(js, reverse=True), (b, js)
-    work = {b: sum(int(u[4] - u[3]) + 1 for u in units if u[0] == b and u[1] == 0) for b, _ in seq_order}
-    ws = [work[b] for b, _ in seq_order]
+    seqs = []
+    for u in units:
+        if not seqs or seqs[-1][0] != int(u[0]):
+            seqs.append((int(u[0]), []))
+        seqs[-1][1].append(u)
+    assert len({b for b, _ in seqs}) == len(seqs), "a sequence's units are split"
+    for b, us in seqs:
+        nqblk = (sq[b] + 127) // 128
+        per_head = (nq // nkv) * nqblk * 128 * d * 8
+        hg = max(1, min(nkv, L2_GROUP_BYTES // max(1, per_head)))
+        pos = 0
+        for g0 in range(0, nkv, hg):
+            heads = list(range(g0, min(nkv, g0 + hg)))
+            n_blocks = (skv[b] + 127) // 128
+            expect_js = list(range(n_blocks - 1, -1, -1))
+            chunk = us[pos:pos + n_blocks * len(heads)]
+            pos += n_blocks * len(heads)
+            assert [int(u[2]) for u in chunk[::len(heads)]] == expect_js, (b, g0)
+            for i in range(0, len(chunk), len(heads)):
+                assert [int(u[1]) for u in chunk[i:i + len(heads)]] == heads, (b, g0, i)
+                assert len({int(u[2]) for u in chunk[i:i + len(heads)]}) == 1
+        assert pos == len(us)
+    work = {b: sum(int(u[4] - u[3]) + 1 for u in us if u[1] == 0) for b, us in seqs}
+    ws = [work[b] for b, _ in seqs]
     assert ws == sorted(ws, reverse=True), ws
+    return seqs
+
+
+@pytest.mark.parametrize("case", range(len(PLANS)))
+def test_plan_hands_out_kv_heads_of_a_block_together(case):
+    _check_unit_order(*_plan_case(case))
+
+
+def test_plan_groups_kv_heads_of_long_sequences():
+    # 8192 q rows, 32 query heads on 8 kv heads: one kv head's q-side tiles
+    # (4 heads x 64 q blocks x 128 KB = 32 MB) fit the L2 share, two do not
+    seqs = _check_unit_order([8192, 1000], [8192, 1000], 32, 8, 3, INF, INF, None)
+    long_units = seqs[0][1]
+    assert [int(u[1]) for u in long_units[:64]] == [0] * 64
+    # the short sequence keeps all its heads together
+    assert [int(u[1]) for u in seqs[1][1][:8]] == list(range(8))
