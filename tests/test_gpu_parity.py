@@ -202,6 +202,20 @@ def test_long_causal_sink_dsink_matches_oracle():
     assert "dsink" in res
 
 
+@pytest.mark.parametrize("mode,extra", [(1, dict(amask_density=0.3)), (0, dict(amask_density=0.2)),
+                                        (6, dict(prefix=[700, 300, 0]))],
+                         ids=["atten_mask_mode1", "atten_mask_mode0_band", "prefix_mode6"])
+def test_masked_modes_several_blocks_match_oracle(mode, extra):
+    """The attention-mask matrix and the prefix over many 128-row blocks (ragged
+    tails, fully masked rows, GQA), compared in full with the oracle."""
+    pre, nxt = (300, 64) if mode == 0 else (INF, INF)
+    wl = workloads.custom(f"masked_{mode}", "bf16", [1500, 700, 333], [1500, 900, 333], 4, 2, 128,
+                          pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, seed=911 + mode, **extra)
+    inp = workloads.make_inputs(wl)
+    got = gh.run_library(inp)
+    gh.compare_all(inp, got, gh.oracle_reference(inp))
+
+
 def test_grad_call_returns_before_earlier_stream_work_finishes():
     """The run call only enqueues: with a long kernel queued ahead of it on
     the same stream, tnd_attn_grad returns while that kernel still runs."""
