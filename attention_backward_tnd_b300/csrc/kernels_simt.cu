@@ -433,16 +433,19 @@ cudaError_t dispatch(int dtype, int d, Args &&...args)
     if (dtype == TND_BF16) {
         if (d <= 64) return Launch<__nv_bfloat16, 64>::run(args...);
         if (d <= 128) return Launch<__nv_bfloat16, 128>::run(args...);
-        return Launch<__nv_bfloat16, 256>::run(args...);
+        if (d <= 256) return Launch<__nv_bfloat16, 256>::run(args...);
+        return Launch<__nv_bfloat16, 768>::run(args...);
     }
     if (dtype == TND_F16) {
         if (d <= 64) return Launch<__half, 64>::run(args...);
         if (d <= 128) return Launch<__half, 128>::run(args...);
-        return Launch<__half, 256>::run(args...);
+        if (d <= 256) return Launch<__half, 256>::run(args...);
+        return Launch<__half, 768>::run(args...);
     }
     if (d <= 64) return Launch<float, 64>::run(args...);
     if (d <= 128) return Launch<float, 128>::run(args...);
-    return Launch<float, 256>::run(args...);
+    if (d <= 256) return Launch<float, 256>::run(args...);
+    return Launch<float, 768>::run(args...);
 }
 
 // ---------------------------------------------------------------------------

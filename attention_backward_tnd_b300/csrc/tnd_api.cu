@@ -96,7 +96,7 @@ constexpr int64_t kMaxHeadDim = 768;              // D in [1, 768] (V5 page)
 constexpr int64_t kMaxBatch = 20000;              // B in [1, 20000] (V5 page)
 constexpr int64_t kMaxBatchPrefix = 1024;         // B in [1, 1K] with prefixOptional
 constexpr int64_t kTokenClamp = int64_t(1) << 40; // |preTokens|, |nextTokens| beyond any T act alike
-constexpr int64_t kSimtMaxHeadDim = 256;          // this build's CUDA-core kernels
+constexpr int64_t kSimtMaxHeadDim = 768;          // the CUDA-core kernels (instances up to D = 64, 128, 256, 768)
 
 // Argument checks of the first phase ([UnpadGrad] parameters and constraints:
 // sparseMode, attenMaskOptional, prefixOptional).  Modes 0 (with the matrix)

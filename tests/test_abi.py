@@ -92,7 +92,7 @@ def test_workspace_size_accepts_valid_problems():
     (dict(mode=7), tnd.TND_ERR_UNSUPPORTED),
     (dict(mode=8), tnd.TND_ERR_UNSUPPORTED),
     (dict(mode=4, pre=3, nxt=0, cu_kv=(0, 6, 9)), tnd.TND_ERR_UNSUPPORTED),  # band with Sq != Skv
-    (dict(d=512), tnd.TND_ERR_UNSUPPORTED),
+    (dict(d=769), tnd.TND_ERR_INVALID),                           # D > 768
 ])
 def test_workspace_size_rejects(kw, expect):
     assert ws(**kw)[0] == expect

@@ -37,6 +37,9 @@ SMALL = {
     "fp32_band_dropout_sink_d128": ("f32", [140, 65], None, 2, 2, 128, 4, 30, 5, 0.75, True),
     "fp16_d96_full": ("f16", [45, 70], None, 3, 1, 96, 0, INF, INF, 1.0, False),
     "single_token": ("bf16", [1], None, 1, 1, 128, 0, INF, INF, 1.0, False),
+    # head dims past 256 (CUDA-core kernels, D up to 768 on the pages)
+    "bf16_d512_causal_gqa": ("bf16", [40, 70], None, 2, 1, 512, 3, INF, INF, 1.0, False),
+    "fp32_d768_band_dropout_sink": ("f32", [33, 20], None, 2, 2, 768, 4, 9, 3, 0.8, True),
     # attention-mask matrix (sparseMode 1, and 0 with the preTokens/nextTokens band) and prefix (6);
     # the last field holds the matrix density / the prefix values
     "amask_mode1_bf16": ("bf16", [200, 129, 1], None, 4, 2, 128, 1, INF, INF, 1.0, False, dict(amask=0.3)),
