@@ -52,6 +52,8 @@ class _Problem(ctypes.Structure):
         ("atten_mask", ctypes.POINTER(ctypes.c_uint8)),
         ("mask_rows", ctypes.c_int64), ("mask_cols", ctypes.c_int64),
         ("prefix", ctypes.POINTER(ctypes.c_int64)),
+        ("pse", ctypes.POINTER(ctypes.c_double)),
+        ("pse_batch", ctypes.c_int64), ("pse_cols", ctypes.c_int64), ("pse_type", ctypes.c_int64),
     ]
 
 
@@ -75,6 +77,8 @@ def bind(path: str):
     cdll.ora_mask_base.restype = ctypes.c_int64
     cdll.ora_keep_at.argtypes = [P(_Problem)] + [ctypes.c_int64] * 5
     cdll.ora_keep_at.restype = ctypes.c_int
+    cdll.ora_pse_at.argtypes = [P(_Problem)] + [ctypes.c_int64] * 5
+    cdll.ora_pse_at.restype = ctypes.c_double
     return cdll
 
 
@@ -115,7 +119,8 @@ class Problem:
                  next_tokens: int = 2147483647, sparse_mode: int = 0,
                  drop_mask: Optional[np.ndarray] = None, sink: Optional[np.ndarray] = None,
                  heads: Optional[Sequence[int]] = None, row_lo: Optional[Sequence[int]] = None,
-                 atten_mask: Optional[np.ndarray] = None, prefix: Optional[Sequence[int]] = None):
+                 atten_mask: Optional[np.ndarray] = None, prefix: Optional[Sequence[int]] = None,
+                 pse: Optional[np.ndarray] = None, pse_type: int = 1):
         self.cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
         self.cu_kv = np.ascontiguousarray(cu_kv, dtype=np.int64)
         self.nq, self.nkv, self.d = int(nq), int(nkv), int(d)
@@ -125,6 +130,15 @@ class Problem:
         self.row_lo = None if row_lo is None else np.ascontiguousarray(row_lo, dtype=np.int64)
         self.atten_mask = None if atten_mask is None else np.ascontiguousarray(atten_mask, dtype=np.uint8)
         self.prefix = None if prefix is None else np.ascontiguousarray(prefix, dtype=np.int64)
+        self.pse = None if pse is None else np.ascontiguousarray(pse, dtype=np.float64)
+        if self.pse is not None:
+            nb = len(cu_q) - 1
+            if self.pse.ndim != 4 or self.pse.shape[0] not in (1, nb) or self.pse.shape[1] != nq or \
+                    self.pse.shape[2] != 1024:
+                raise ValueError("pse is [B or 1, Nq, 1024, S]")
+            skv_max = int(np.max(np.diff(np.asarray(cu_kv)))) if nb else 0
+            if self.pse.shape[3] < skv_max:
+                raise ValueError("pse must cover the longest key sequence")
         if sparse_mode == 1 and self.atten_mask is None:
             raise ValueError("sparseMode 1 needs the attention-mask matrix")
         if sparse_mode == 6 and (self.prefix is None or self.prefix.size != len(cu_q) - 1):
@@ -153,7 +167,12 @@ class Problem:
             0 if self.atten_mask is None else self.atten_mask.shape[0],
             0 if self.atten_mask is None else self.atten_mask.shape[1],
             ctypes.POINTER(ctypes.c_int64)() if self.prefix is None
-            else self.prefix.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+            else self.prefix.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            ctypes.POINTER(ctypes.c_double)() if self.pse is None
+            else self.pse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            0 if self.pse is None else self.pse.shape[0],
+            0 if self.pse is None else self.pse.shape[3],
+            int(pse_type))
 
     @property
     def tq(self) -> int:
@@ -177,6 +196,12 @@ def problem_from_workload(wl, drop_mask=None, sink=None, **kw) -> Problem:
     return Problem(wl.cu_q, wl.cu_kv, wl.nq, wl.nkv, wl.d, wl.scale, wl.keep_prob,
                    wl.pre_tokens, wl.next_tokens, wl.sparse_mode, drop_mask,
                    None if sink is None else np.asarray(sink, dtype=np.float64), **kw)
+
+
+def pse_at(p: Problem, b: int, h: int, i: int, j: int) -> float:
+    """The oracle's pse value of (sequence b, head h, row i, column j)."""
+    sq = int(p.cu_q[b + 1] - p.cu_q[b])
+    return float(lib().ora_pse_at(ctypes.byref(p._c), b, h, sq, i, j))
 
 
 def keep_at(p: Problem, b: int, i: int, j: int) -> bool:

@@ -15,6 +15,10 @@
  *   s_ij  = scale * <Q_i, K_j>                                [UnpadGrad, function
  *           description: S = Mask((QK^T + pse)/sqrt(d)); scaleValue stands for
  *           1/sqrt(d), parameters section]
+ *           with a pse: scale * (<Q_i, K_j> + pse_ij) (pseType 1, the grad
+ *           page's formula) or scale * <Q_i, K_j> + pse_ij (pseType 0)
+ *           [ScoreV2, parameters: pseType 0 multiplies then adds, 1 adds then
+ *           multiplies]
  *   kept_ij from sparseMode / preTokens / nextTokens          [UnpadGrad, parameters:
  *           sparseMode]
  *   m_i   = max over kept s_ij (and the sink logit if given)  [UnpadGradV5, function
@@ -60,6 +64,16 @@
  *     byte = index >> 3, bit = index & 7 (least significant bit first).
  *   - a row with no kept key and no sink has m = -inf, l = 0, O = 0 and
  *     contributes nothing to the gradient.
+ *   - pseShiftOptional [UnpadGrad, parameters: shape [B,N,H,S] or [1,N,H,S],
+ *     H = 1024; alibi needs a lower triangle and Sq = Skv; UnpadGradV5,
+ *     constraints: alibi_compress = ori_pse[:, :, -1024:, :]] holds, per
+ *     sequence (or for all, when its first dimension is 1) and query head,
+ *     the last 1024 rows of the [Sq, Skv] bias: row i of the sequence is
+ *     stored row i - (Sq - 1024) (so a sequence shorter than 1024 sits at the
+ *     bottom of the 1024 rows), and a row above the stored ones (i < Sq - 1024)
+ *     is read along its diagonal from stored row 0, column j + (Sq - 1024 - i),
+ *     which reproduces a bias that depends only on i - j (alibi).  dpseOut is
+ *     a reserved output on the pages and is not computed.
  *
  * Everything is plain fp64 loops over rows; the selection fields of
  * ora_problem (head range, first row per sequence) only narrow loop bounds so
@@ -88,6 +102,9 @@ typedef struct ora_problem {
     const uint8_t *atten_mask;
     int64_t mask_rows, mask_cols;
     const int64_t *prefix;
+    /* pseShiftOptional [pse_batch][Nq][1024][pse_cols] (NULL = none) and pseType */
+    const double *pse;
+    int64_t pse_batch, pse_cols, pse_type;
 } ora_problem;
 
 /* sparseMode predicate; [UnpadGrad, parameters: sparseMode]. */
@@ -118,6 +135,28 @@ int ora_keep_at(const ora_problem *p, int64_t b, int64_t sq, int64_t skv, int64_
     case 6: return j <= i + (skv - sq) || j < p->prefix[b];
     default: return ora_keep(mode, p->pre_tokens, p->next_tokens, sq, skv, i, j);
     }
+}
+
+/* pse of (b, h, i, j) from the stored last 1024 rows of the sequence's bias
+ * [UnpadGrad, parameters: pseShiftOptional; UnpadGradV5, constraints: alibi
+ * compression]; rows above the stored ones along their diagonal. */
+double ora_pse_at(const ora_problem *p, int64_t b, int64_t h, int64_t sq, int64_t i, int64_t j)
+{
+    const int64_t bb = p->pse_batch == 1 ? 0 : b;
+    int64_t r = i - (sq - 1024), c = j;
+    if (r < 0) {
+        c = j - r;
+        r = 0;
+    }
+    return p->pse[((bb * p->Nq + h) * 1024 + r) * p->pse_cols + c];
+}
+
+/* the logit s_ij from <Q_i, K_j> [UnpadGrad: (QK^T + pse)/sqrt(d); ScoreV2: pseType] */
+static double logit(const ora_problem *p, double qk, int64_t b, int64_t h, int64_t sq, int64_t i, int64_t j)
+{
+    if (p->pse == NULL) return p->scale * qk;
+    const double pse = ora_pse_at(p, b, h, sq, i, j);
+    return p->pse_type == 1 ? p->scale * (qk + pse) : p->scale * qk + pse;
 }
 
 /* first flat keep-bit index of sequence b */
@@ -166,7 +205,7 @@ static void row_scores(const ora_problem *p, const double *q, const double *k,
     const double *qi = q + ((tq + i) * p->Nq + h) * D;
     for (int64_t j = 0; j < skv; ++j) {
         kept[j] = (unsigned char)ora_keep_at(p, b, sq, skv, i, j);
-        s[j] = kept[j] ? p->scale * dot(qi, k + ((tk + j) * p->Nkv + g) * D, D) : 0.0;
+        s[j] = kept[j] ? logit(p, dot(qi, k + ((tk + j) * p->Nkv + g) * D, D), b, h, sq, i, j) : 0.0;
     }
 }
 
@@ -272,7 +311,7 @@ static double grad_ds(const ora_problem *p, const double *q, const double *k, co
     if (!ora_keep_at(p, b, sq, skv, i, j) || !(l > 0.0)) return 0.0;
     const int64_t r = (tq + i) * p->Nq + h;
     const double *kj = k + ((tk + j) * p->Nkv + g) * D, *vj = v + ((tk + j) * p->Nkv + g) * D;
-    const double s = p->scale * dot(q + r * D, kj, D);
+    const double s = logit(p, dot(q + r * D, kj, D), b, h, sq, i, j);
     const double pij = exp(s - m) / l;
     const double z = drop_z(p, base, h, i, j, sq, skv);
     const double dP = dot(dy + r * D, vj, D);

@@ -48,7 +48,7 @@ def random_bits(rng, shapes, p_keep=0.7):
 
 def autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, *, mode=0, pre=2**31 - 1,
                        nxt=2**31 - 1, bits=None, keep_prob=1.0, sink=None, atten_mask=None,
-                       prefix=None):
+                       prefix=None, bias=None, pse_type=1):
     """Textbook attention per (sequence, head) in torch fp64, differentiated by
     autograd.  Returns dict of numpy arrays: out, smax, ssum, dq, dk, dv, dsink."""
     G = nq // nkv
@@ -73,7 +73,11 @@ def autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, *, mode=0, p
             qb = Q[tq:tq + sq, h, :]
             kb = K[tk:tk + skv, g, :]
             vb = V[tk:tk + skv, g, :]
-            logits = scale * qb @ kb.T
+            if bias is None:
+                logits = scale * qb @ kb.T
+            else:   # bias[b]: explicit [Nq, Sq, Skv] pse matrix of the sequence
+                pse = torch.tensor(bias[b][h], dtype=torch.float64)
+                logits = scale * (qb @ kb.T + pse) if pse_type == 1 else scale * qb @ kb.T + pse
             logits = logits.masked_fill(~keep, float("-inf"))
             if S_ink is not None:
                 logits = torch.cat([logits, S_ink[h].expand(sq, 1)], dim=1)

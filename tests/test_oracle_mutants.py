@@ -34,6 +34,8 @@ MUTANTS = {
         "return !masked && (j - i >= -p->pre_tokens) && (j - i <= p->next_tokens);", "return !masked;"),
     "prefix_inclusive": ("j < p->prefix[b]", "j <= p->prefix[b]"),
     "prefix_top_left_anchor": ("case 6: return j <= i + (skv - sq)", "case 6: return j <= i"),
+    "pse_rows_above_not_along_diagonal": ("        c = j - r;\n        r = 0;", "        r = 0;"),
+    "pse_type_swapped": ("return p->pse_type == 1 ? p->scale * (qk + pse)", "return p->pse_type == 0 ? p->scale * (qk + pse)"),
 }
 
 
@@ -53,6 +55,9 @@ def _pin_suite(ora):
         pins.test_prefix_predicate_matches_explicit_matrix(ora, 5, 9)
         for ci in range(len(pins.MASK_CASES)):
             pins.test_masked_forward_and_grad_match_autograd(ora, ci)
+        for pse_type in (0, 1):
+            pins.test_alibi_pse_matches_autograd_with_the_full_bias(ora, pse_type, [1300, 40])
+            pins.test_random_pse_short_sequences_match_autograd(ora, pse_type)
     except AssertionError:
         return False
     return True

@@ -209,6 +209,121 @@ def test_masked_grad_matches_central_differences(ora):
 
 
 # --------------------------------------------------------------------------
+# pse (positional bias), stored as the last 1024 rows of each sequence's bias
+# --------------------------------------------------------------------------
+
+def _alibi_full(slopes, sq):
+    """Full [Nq, sq, sq] alibi bias slope_h * (j - i): depends only on i - j."""
+    ij = np.arange(sq)[None, :] - np.arange(sq)[:, None]
+    return np.asarray(slopes, np.float64)[:, None, None] * ij[None]
+
+
+def _store_last_rows(full, rng):
+    """[Nq, 1024, S] store of a full [Nq, sq, S] bias: its last 1024 rows (numpy
+    slicing); a shorter bias fills the bottom rows, the rows above hold noise."""
+    nq, sq, s = full.shape
+    out = rng.standard_normal((nq, 1024, s))
+    out[:, max(0, 1024 - sq):, :] = full[:, -1024:, :]
+    return out
+
+
+@pytest.mark.parametrize("pse_type", [0, 1])
+@pytest.mark.parametrize("seqs", [[1300, 40], [700]])
+def test_alibi_pse_matches_autograd_with_the_full_bias(ora, pse_type, seqs):
+    """The stored rows of an alibi bias reproduce the whole [Sq, Sq] bias: rows
+    above the last 1024 are read along their diagonal."""
+    nq, nkv, d = 2, 1, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(41 + len(seqs), seqs, seqs, nq, nkv, d)
+    slopes = [0.05, -0.02]
+    s2 = max(seqs)
+    store = np.zeros((len(seqs), nq, 1024, s2))
+    full = []
+    for b, sq in enumerate(seqs):
+        f = _alibi_full(slopes, sq)
+        full.append(f)
+        padded = np.zeros((nq, sq, s2))
+        padded[:, :, :sq] = f
+        store[b] = _store_last_rows(padded, rng)
+    scale = scale_for(d)
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, sparse_mode=3, pse=store, pse_type=pse_type)
+    ref = autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, mode=3, bias=full, pse_type=pse_type)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(smax, ref["smax"], rtol=1e-12, atol=1e-12)
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-11, err_msg=name)
+
+
+@pytest.mark.parametrize("pse_type", [0, 1])
+def test_random_pse_short_sequences_match_autograd(ora, pse_type):
+    """Sequences shorter than 1024 take the bottom rows of the store as their
+    bias, whatever it holds (broadcast over the batch when its first dim is 1)."""
+    seqs, nq, nkv, d = [37, 64, 5], 4, 2, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(53, seqs, seqs, nq, nkv, d)
+    store = rng.standard_normal((1, nq, 1024, max(seqs)))
+    full = [store[0, :, 1024 - sq:, :sq] for sq in seqs]
+    scale = scale_for(d) * 1.3
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, sparse_mode=2, pse=store, pse_type=pse_type)
+    ref = autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, mode=2, bias=full, pse_type=pse_type)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-12)
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-11, err_msg=name)
+
+
+def test_pse_special_cases(ora):
+    """Zero pse is no pse; a pse constant along each row shifts the max only."""
+    seqs, nq, nkv, d = [1100, 30], 2, 2, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(61, seqs, seqs, nq, nkv, d)
+    scale = scale_for(d)
+    base = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, sparse_mode=3)
+    o0, m0, l0 = ora.fwd(base, q, k, v)
+    g0 = ora.grad(base, q, k, v, dy, o0, m0, l0)
+    zero = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, sparse_mode=3, pse=np.zeros((1, nq, 1024, 1100)))
+    o1, m1, l1 = ora.fwd(zero, q, k, v)
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(m1, m0)
+    # a constant c per (head, stored row) is constant along every row of the full
+    # bias (rows above the stored ones read stored row 0); rows shift by c
+    # (pseType 0) or scale * c (pseType 1)
+    c = rng.standard_normal((2, nq, 1024, 1))
+    store = np.broadcast_to(c, (2, nq, 1024, 1100)).copy()
+    for pse_type, mul in ((0, 1.0), (1, scale)):
+        pp = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, sparse_mode=3, pse=store, pse_type=pse_type)
+        o2, m2, l2 = ora.fwd(pp, q, k, v)
+        np.testing.assert_allclose(o2, o0, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(l2, l0, rtol=1e-12)
+        for b, sq in enumerate(seqs):
+            rows = np.maximum(np.arange(sq) - (sq - 1024), 0)
+            shift = mul * c[b][:, rows, 0].T                  # [sq, nq]
+            np.testing.assert_allclose(m2[cu_q[b]:cu_q[b + 1]], m0[cu_q[b]:cu_q[b + 1]] + shift, rtol=1e-12,
+                                       atol=1e-12)
+        g2 = ora.grad(pp, q, k, v, dy, o2, m2, l2)
+        for a_, b_ in zip(g2[:3], g0[:3]):
+            np.testing.assert_allclose(a_, b_, rtol=1e-10, atol=1e-12)
+
+
+def test_pse_grad_matches_central_differences(ora):
+    seqs, nq, nkv, d = [1030], 2, 1, 4
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(71, seqs, seqs, nq, nkv, d)
+    store = 0.3 * rng.standard_normal((1, nq, 1024, 1030))
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, 0.4, sparse_mode=3, pse=store, pse_type=1)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, _, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    h = 1e-6
+    for name, arr, g in (("q", q, dq), ("k", k, dk)):
+        for idx in [(0, 0, 1), (5, arr.shape[1] - 1, 3), (1029, 0, 2), (1028, arr.shape[1] - 1, 0)]:
+            a1, a2 = arr.copy(), arr.copy()
+            a1[idx] += h
+            a2[idx] -= h
+            f = lambda a: float(np.sum(ora.fwd(p, *((a, k, v) if name == "q" else (q, a, v)))[0] * dy))
+            fd = (f(a1) - f(a2)) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
+# --------------------------------------------------------------------------
 # dropout keep-bit layout
 # --------------------------------------------------------------------------
 
