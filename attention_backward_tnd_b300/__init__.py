@@ -53,11 +53,11 @@ def lib():
                    _int, ctypes.POINTER(ctypes.c_uint64)]
         L.tnd_attn_fwd_workspace_size.argtypes = ws_args
         L.tnd_attn_grad_workspace_size.argtypes = ws_args
-        L.tnd_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64p, _i64, _i64,
-                                   _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64, _vp]
-        L.tnd_attn_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64, _i64p, _i64p,
-                                    _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
-                                    _vp, _u64, _vp]
+        L.tnd_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64p,
+                                   _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64, _vp]
+        L.tnd_attn_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64,
+                                    _i64p, _i64p, _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp,
+                                    _vp, _vp, _vp, _u64, _vp]
         L.tnd_attn_device_status.argtypes = [_vp, _u64, _vp]
         L.tnd_status_string.argtypes = [_int]
         L.tnd_status_string.restype = ctypes.c_char_p
@@ -125,24 +125,25 @@ def tnd_attn_grad_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv
     return st, out.value
 
 
-def tnd_attn_fwd(query, key, value, drop_mask, atten_mask, sink, dtype, batch, cu_q, cu_kv, prefix, head_num,
-                 kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, attention_out,
-                 softmax_max, softmax_sum, workspace, workspace_size, stream):
+def tnd_attn_fwd(query, key, value, pse, pse_batch, pse_type, drop_mask, atten_mask, sink, dtype, batch, cu_q,
+                 cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens,
+                 sparse_mode, attention_out, softmax_max, softmax_sum, workspace, workspace_size, stream):
     cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
-    return lib().tnd_attn_fwd(query, key, value, drop_mask, atten_mask, sink, dtype, batch, _p(cq), _p(ck),
-                              _pp(pf), head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens,
-                              next_tokens, sparse_mode, attention_out, softmax_max, softmax_sum, workspace,
-                              workspace_size, stream)
+    return lib().tnd_attn_fwd(query, key, value, pse, pse_batch, pse_type, drop_mask, atten_mask, sink, dtype, batch,
+                              _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, head_dim, scale_value, keep_prob,
+                              pre_tokens, next_tokens, sparse_mode, attention_out, softmax_max, softmax_sum,
+                              workspace, workspace_size, stream)
 
 
-def tnd_attn_grad(query, key, value, dy, drop_mask, atten_mask, softmax_max, softmax_sum, attention_in, sink, dtype,
-                  batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens,
-                  next_tokens, sparse_mode, dq, dk, dv, dsink, workspace, workspace_size, stream):
+def tnd_attn_grad(query, key, value, dy, pse, pse_batch, pse_type, drop_mask, atten_mask, softmax_max, softmax_sum,
+                  attention_in, sink, dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value,
+                  keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv, dsink, workspace, workspace_size,
+                  stream):
     cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
-    return lib().tnd_attn_grad(query, key, value, dy, drop_mask, atten_mask, softmax_max, softmax_sum,
-                               attention_in, sink, dtype, batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num,
-                               head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv,
-                               dsink, workspace, workspace_size, stream)
+    return lib().tnd_attn_grad(query, key, value, dy, pse, pse_batch, pse_type, drop_mask, atten_mask, softmax_max,
+                               softmax_sum, attention_in, sink, dtype, batch, _p(cq), _p(ck), _pp(pf), head_num,
+                               kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                               dq, dk, dv, dsink, workspace, workspace_size, stream)
 
 
 def tnd_attn_grad_static_ws(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink, dtype,
@@ -226,6 +227,17 @@ def _check_amask(atten_mask, cu_q, cu_kv):
         raise ValueError(f"atten_mask must be a contiguous uint8/bool tensor of shape ({s1}, {s2})")
 
 
+def _check_pse(pse, q, cu_kv, batch) -> int:
+    """pse must be a contiguous [B or 1, Nq, 1024, S2Max] tensor of q's dtype; returns its first dim (0 = none)."""
+    if pse is None:
+        return 0
+    s2 = int(np.max(np.diff(_cu(cu_kv))))
+    if pse.dim() != 4 or pse.shape[0] not in (1, batch) or tuple(pse.shape[1:]) != (q.shape[1], 1024, s2) or \
+            pse.dtype != q.dtype or not pse.is_contiguous():
+        raise ValueError(f"pse must be a contiguous [{batch} or 1, {q.shape[1]}, 1024, {s2}] tensor of {q.dtype}")
+    return int(pse.shape[0])
+
+
 def _stream():
     import torch
     return torch.cuda.current_stream().cuda_stream
@@ -233,9 +245,10 @@ def _stream():
 
 def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_prob: float = 1.0,
         pre_tokens: int = 2147483647, next_tokens: int = 2147483647, sparse_mode: int = 0, drop_mask=None,
-        sink=None, workspace=None, atten_mask=None, prefix=None):
+        sink=None, workspace=None, atten_mask=None, prefix=None, pse=None, pse_type: int = 1):
     """Forward on torch CUDA tensors: returns (out, softmax_max, softmax_sum) ([T,N,8] fp32 stats).
-    atten_mask: uint8/bool CUDA tensor [S1Max, S2Max] (nonzero masks); prefix: host ints (sparse_mode 6)."""
+    atten_mask: uint8/bool CUDA tensor [S1Max, S2Max] (nonzero masks); prefix: host ints (sparse_mode 6);
+    pse: CUDA tensor [B or 1, Nq, 1024, S2Max] in q's dtype (the last 1024 rows of each sequence's bias)."""
     import torch
     tq, nq, d = q.shape
     nkv = k.shape[1]
@@ -252,10 +265,11 @@ def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_p
     ssum = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
-    st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(drop_mask), _ptr(atten_mask), _ptr(sink), dt,
-                      batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens,
-                      sparse_mode, out.data_ptr(), smax.data_ptr(), ssum.data_ptr(), workspace.data_ptr(),
-                      workspace.numel(), _stream())
+    pb = _check_pse(pse, q, cu_kv, batch)
+    st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(pse), pb, pse_type, _ptr(drop_mask),
+                      _ptr(atten_mask), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob,
+                      pre_tokens, next_tokens, sparse_mode, out.data_ptr(), smax.data_ptr(), ssum.data_ptr(),
+                      workspace.data_ptr(), workspace.numel(), _stream())
     if st != TND_OK:
         raise TndError(st, "tnd_attn_fwd")
     return out, smax, ssum
@@ -274,7 +288,7 @@ def grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob=1.0, pre_tokens=214
 
 def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_prob=1.0,
          pre_tokens=2147483647, next_tokens=2147483647, sparse_mode=0, drop_mask=None, sink=None,
-         workspace=None, outputs=None, atten_mask=None, prefix=None):
+         workspace=None, outputs=None, atten_mask=None, prefix=None, pse=None, pse_type: int = 1):
     """Gradient on torch CUDA tensors: returns (dq, dk, dv, dsink or None)."""
     import torch
     tq, nq, d = q.shape
@@ -291,11 +305,12 @@ def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_pr
         dsink = torch.empty(nq, dtype=torch.float32, device=q.device) if sink is not None else None
     else:
         dq, dk, dv, dsink = outputs
-    st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(drop_mask), _ptr(atten_mask),
-                       softmax_max.data_ptr(), softmax_sum.data_ptr(), out.data_ptr(), _ptr(sink), dt, batch, cu_q,
-                       cu_kv, prefix, nq, nkv, d, scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _ptr(dsink), workspace.data_ptr(),
-                       workspace.numel(), _stream())
+    pb = _check_pse(pse, q, cu_kv, batch)
+    st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(pse), pb, pse_type,
+                       _ptr(drop_mask), _ptr(atten_mask), softmax_max.data_ptr(), softmax_sum.data_ptr(),
+                       out.data_ptr(), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob,
+                       pre_tokens, next_tokens, sparse_mode, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       _ptr(dsink), workspace.data_ptr(), workspace.numel(), _stream())
     if st != TND_OK:
         raise TndError(st, "tnd_attn_grad")
     return dq, dk, dv, dsink

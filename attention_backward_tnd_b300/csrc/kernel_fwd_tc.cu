@@ -121,6 +121,7 @@ __device__ __forceinline__ uint32_t fpack2(float lo, float hi)
 
 struct FUnit {
     int qg, h, jlo, n;   // global q block, head, first kv block, kv blocks (0: no key)
+    int b;               // sequence
     SeqDesc sd;
     int64_t q0;          // first q row of the block within its sequence
 };
@@ -134,6 +135,7 @@ __device__ __forceinline__ FUnit funit(const FwdArgs &a, int u)
     const QBlockInfo qi = a.qblk[fu.x];
     const int2 qr = a.qblk_rows[fu.x];
     U.sd = a.seqs[qr.x];
+    U.b = qr.x;
     U.q0 = qr.y;
     U.jlo = qi.jlo;
     U.n = qi.jlo < 0 ? 0 : qi.jhi - qi.jlo + 1;
@@ -180,7 +182,31 @@ __device__ __forceinline__ void fetch_keep128(const FwdArgs &a, const SeqDesc &s
     }
 }
 
-template <bool BF16, int HD>
+// pse terms (log2 units of C * S) of row i over kv columns jc .. jc + 31, 0
+// outside the sequence (those columns are masked anyway)
+template <bool BF16>
+__device__ __forceinline__ void fpse_chunk(const FwdArgs &a, const FUnit &U, int64_t i, bool row_ok, int64_t jc,
+                                           float C, float (&t)[32])
+{
+    using Elt = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    const Elt *pp = reinterpret_cast<const Elt *>(a.pse.ptr);
+    const float mul = a.pse.type == 1 ? C : kLog2e;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const int64_t j = jc + c;
+        float x = 0.0f;
+        if (row_ok && j < U.sd.skv) {
+            const Elt e = pp[pse_index(a.pse, a.nq, U.b, U.h, U.sd.sq, i, j)];
+            if constexpr (BF16) x = __bfloat162float(e);
+            else x = __half2float(e);
+        }
+        t[c] = x * mul;
+    }
+}
+
+// PSE = true adds pseShiftOptional to the scores: pass 1 writes C S + pse term
+// back into the S buffer, which pass 2 then reads as is.
+template <bool BF16, int HD, bool PSE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV)
@@ -437,13 +463,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // pass 1: block max over kept columns
                 float bmax = -INFINITY;
+                const float cs = PSE ? 1.0f : C;      // with a pse, the S buffer holds C S + pse term
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t raw[32];
                     tmem_ld32(s_addr + 32 * ch, raw);
+                    if constexpr (PSE) {
+                        float t[32];
+                        fpse_chunk<BF16>(a, U, i, row_ok, j0 + 32 * ch, C, t);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(fmaf(__uint_as_float(raw[c]), C, t[c]));
+                        tmem_st32(s_addr + 32 * ch, raw);
+                    }
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        if ((km[ch] >> c) & 1u) bmax = fmaxf(bmax, __uint_as_float(raw[c]) * C);
+                        if ((km[ch] >> c) & 1u) bmax = fmaxf(bmax, __uint_as_float(raw[c]) * cs);
                     }
                 }
                 // lazy rescale: only when the max in use falls more than 2^8 behind
@@ -486,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const bool kept = (km[ch] >> c) & 1u;
-                        p[c] = kept ? ex2(fmaf(__uint_as_float(raw[c]), C, mneg)) : 0.0f;
+                        p[c] = kept ? ex2(fmaf(__uint_as_float(raw[c]), cs, mneg)) : 0.0f;
                         l += p[c];
                     }
                     uint32_t pk[16];
@@ -602,7 +636,7 @@ bool fmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t heads, int hd, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool BF16, int HD>
+template <bool BF16, int HD, bool PSE>
 cudaError_t flaunch(const FwdArgs &a, cudaStream_t s)
 {
     CUtensorMap mq, mk, mv;
@@ -611,9 +645,10 @@ cudaError_t flaunch(const FwdArgs &a, cudaStream_t s)
         return cudaErrorInvalidValue;
     const int grid = std::min<int>(a.num_sms, a.n_fwd_units);
     constexpr uint32_t smem = FGeo<HD>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<BF16, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_tc_kernel<BF16, HD, PSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fwd_tc_kernel<BF16, HD><<<grid, kThreads, smem, s>>>(a, mq, mk, mv);
+    fwd_tc_kernel<BF16, HD, PSE><<<grid, kThreads, smem, s>>>(a, mq, mk, mv);
     return cudaGetLastError();
 }
 
@@ -625,8 +660,13 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t s)
 {
     if (a.n_fwd_units == 0) return cudaSuccess;
     const bool bf16 = a.dtype == TND_BF16;
-    if (a.d == 128) return bf16 ? flaunch<true, 128>(a, s) : flaunch<false, 128>(a, s);
-    if (a.d == 64) return bf16 ? flaunch<true, 64>(a, s) : flaunch<false, 64>(a, s);
+    if (a.pse.ptr) {
+        if (a.d == 128) return bf16 ? flaunch<true, 128, true>(a, s) : flaunch<false, 128, true>(a, s);
+        if (a.d == 64) return bf16 ? flaunch<true, 64, true>(a, s) : flaunch<false, 64, true>(a, s);
+        return cudaErrorInvalidValue;
+    }
+    if (a.d == 128) return bf16 ? flaunch<true, 128, false>(a, s) : flaunch<false, 128, false>(a, s);
+    if (a.d == 64) return bf16 ? flaunch<true, 64, false>(a, s) : flaunch<false, 64, false>(a, s);
     return cudaErrorInvalidValue;
 }
 

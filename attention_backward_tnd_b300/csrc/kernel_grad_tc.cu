@@ -396,9 +396,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return BF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
+// pse terms (in the log2 units of C * S^T) of q rows qc .. qc + 31 for kv row
+// jj of head h, 0 outside the sequence (those columns are masked anyway)
+template <bool BF16>
+__device__ __forceinline__ void pse_chunk(const GradArgs &a, const UnitInfo &U, int h, int64_t qc, int64_t jj, float C,
+                                          float (&t)[32])
+{
+    using Elt = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    const Elt *pp = reinterpret_cast<const Elt *>(a.pse.ptr);
+    const float mul = a.pse.type == 1 ? C : kLog2e;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const int64_t i = qc + c;
+        float x = 0.0f;
+        if (i < U.sd.sq && jj < U.sd.skv) {
+            const Elt e = pp[pse_index(a.pse, a.nq, U.b, h, U.sd.sq, i, jj)];
+            if constexpr (BF16) x = __bfloat162float(e);
+            else x = __half2float(e);
+        }
+        t[c] = x * mul;
+    }
+}
+
 // DROP = false: the kernel carries no dropout code, which keeps the compute
 // warps' loop small; DROP = true applies the keep-bits when the call has them.
-template <bool BF16, int HD, bool DROP>
+// PSE = true adds pseShiftOptional to the recomputed scores.
+template <bool BF16, int HD, bool DROP, bool PSE>
 __global__ void __launch_bounds__(kThreads, 1)
     grad_tc_kernel(const __grid_constant__ GradArgs a, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -846,17 +869,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // its first 16 columns (the dV operand)
                 const uint32_t s_addr = tmem + lane_addr + TM_S + 64 * half;
                 float p[64];
+                const float cs = PSE ? 1.0f : C;      // with a pse, raw already holds C S^T + pse term
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     uint32_t raw[32];
                     tmem_ld32(s_addr + 32 * ch, raw);
+                    if constexpr (PSE) {
+                        float t[32];
+                        pse_chunk<BF16>(a, U, h, qc0 + 32 * ch, jj, C, t);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(fmaf(__uint_as_float(raw[c]), C, t[c]));
+                    }
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         const float4 l = lse4[8 * ch + c4];
-                        p[32 * ch + 4 * c4 + 0] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 0]), C, -l.x));
-                        p[32 * ch + 4 * c4 + 1] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 1]), C, -l.y));
-                        p[32 * ch + 4 * c4 + 2] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 2]), C, -l.z));
-                        p[32 * ch + 4 * c4 + 3] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 3]), C, -l.w));
+                        p[32 * ch + 4 * c4 + 0] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 0]), cs, -l.x));
+                        p[32 * ch + 4 * c4 + 1] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 1]), cs, -l.y));
+                        p[32 * ch + 4 * c4 + 2] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 2]), cs, -l.z));
+                        p[32 * ch + 4 * c4 + 3] = ex2(fmaf(__uint_as_float(raw[4 * c4 + 3]), cs, -l.w));
                     }
                     if (!full) {
                         const uint32_t kh = (uint32_t)(keep >> (32 * ch));
@@ -1088,7 +1118,7 @@ bool make_acc_map(CUtensorMap *m, const float *ptr, int64_t rows, int64_t heads,
     return r == CUDA_SUCCESS;
 }
 
-template <bool BF16, int HD, bool DROP>
+template <bool BF16, int HD, bool DROP, bool PSE>
 cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
 {
     CUtensorMap mq, mk, mv, mdy, mdq;
@@ -1099,10 +1129,10 @@ cudaError_t launch_hd(const GradArgs &a, cudaStream_t s)
     const int grid = std::min<int>(a.num_sms, a.n_units);
     constexpr uint32_t smem = Geo<HD>::kSmemBytes;
     cudaError_t e =
-        cudaFuncSetAttribute(grad_tc_kernel<BF16, HD, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(grad_tc_kernel<BF16, HD, DROP, PSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(grad_tc_kernel<BF16, HD, DROP>, dim3(grid), dim3(kThreads), smem, s, a, mq, mk, mv, mdy,
-                            mdq);
+    return launch_dependent(grad_tc_kernel<BF16, HD, DROP, PSE>, dim3(grid), dim3(kThreads), smem, s, a, mq, mk, mv,
+                            mdy, mdq);
 }
 
 // dQ = scale * accumulator in the output dtype, one block per (128-row q
@@ -1155,13 +1185,19 @@ cudaError_t launch_grad_tc(const GradArgs &a, cudaStream_t s)
     if (a.n_units == 0) return cudaSuccess;
     const bool bf16 = a.dtype == TND_BF16;
     const bool drop = a.has_drop != 0;
+    if (a.pse.ptr) {
+        // with a pse: the dropout-capable instances (keep-bits applied when the call has them)
+        if (a.d == 128) return bf16 ? launch_hd<true, 128, true, true>(a, s) : launch_hd<false, 128, true, true>(a, s);
+        if (a.d == 64) return bf16 ? launch_hd<true, 64, true, true>(a, s) : launch_hd<false, 64, true, true>(a, s);
+        return cudaErrorInvalidValue;
+    }
     if (a.d == 128) {
-        if (bf16) return drop ? launch_hd<true, 128, true>(a, s) : launch_hd<true, 128, false>(a, s);
-        return drop ? launch_hd<false, 128, true>(a, s) : launch_hd<false, 128, false>(a, s);
+        if (bf16) return drop ? launch_hd<true, 128, true, false>(a, s) : launch_hd<true, 128, false, false>(a, s);
+        return drop ? launch_hd<false, 128, true, false>(a, s) : launch_hd<false, 128, false, false>(a, s);
     }
     if (a.d == 64) {
-        if (bf16) return drop ? launch_hd<true, 64, true>(a, s) : launch_hd<true, 64, false>(a, s);
-        return drop ? launch_hd<false, 64, true>(a, s) : launch_hd<false, 64, false>(a, s);
+        if (bf16) return drop ? launch_hd<true, 64, true, false>(a, s) : launch_hd<true, 64, false, false>(a, s);
+        return drop ? launch_hd<false, 64, true, false>(a, s) : launch_hd<false, 64, false, false>(a, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -53,6 +53,16 @@ __device__ __forceinline__ void block_union(int64_t lo, int64_t hi, int64_t &ulo
     uhi = b;
 }
 
+// pse term of (sequence b, head h, row i, column j) in the log2 units of the
+// scores (pseType 1 is scaled like QK^T, pseType 0 is added after the scale).
+template <typename T>
+__device__ __forceinline__ float pse_term(const PseSpec &ps, int32_t nq, float C, int64_t b, int64_t h, int64_t sq,
+                                          int64_t i, int64_t j)
+{
+    const T *pp = (const T *)ps.ptr;
+    return Elem<T>::load(pp + pse_index(ps, nq, b, h, sq, i, j)) * (ps.type == 1 ? C : kLog2e);
+}
+
 __device__ __forceinline__ float quad_sum(float x)
 {
     x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -123,6 +133,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
             for (int k = 0; k < DP; ++k) s += qreg[k] * Ks[c * DMAX + c4 + 4 * k];
             s = quad_sum(s);
             if (j >= lo && j <= hi && matrix_keeps(a.mask, i, j)) {
+                if (a.pse.ptr) s += pse_term<T>(a.pse, a.nq, C, it.x, h, sd.sq, i, j);
                 const float mn = fmaxf(m, s);
                 const float corr = ex2(m - mn);
                 const float p = ex2(s - mn);
@@ -309,6 +320,7 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
                 int64_t rlo = 1, rhi = 0;
                 if (i < sd.sq) key_range(a.mask, sd.sq, sd.skv, sd.prefix, i, rlo, rhi);
                 if (row_ok && j >= rlo && j <= rhi && matrix_keeps(a.mask, i, j)) {
+                    if (a.pse.ptr) s += pse_term<T>(a.pse, a.nq, C, it.x, h, sd.sq, i, j);
                     const float p = ex2(s - lses[rr]);
                     const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
                     const float pz = p * z;
@@ -387,6 +399,7 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
             s = quad_sum(s);
             dp = quad_sum(dp);
             if (j >= lo && j <= hi && matrix_keeps(a.mask, i, j)) {
+                if (a.pse.ptr) s += pse_term<T>(a.pse, a.nq, C, it.x, h, sd.sq, i, j);
                 const float p = ex2(s - lse);
                 const float z = a.has_drop ? drop_z(a.drop_mask, sd.mask_base, h, i, j, sd.sq, sd.skv, a.inv_keep) : 1.0f;
                 const float ds = p * (z * dp - Di);

@@ -166,6 +166,34 @@ tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t 
     return TND_OK;
 }
 
+// pseShiftOptional checks ([UnpadGrad] parameters: shape [B or 1, N, 1024, S];
+// alibi needs a lower-triangle mask and Sq = Skv; [ScoreV2] parameters:
+// pseType 0 / 1 take the given pse, 2 / 3 generate it inside, which is not
+// implemented here).
+tnd_status check_pse(const Problem &p, const void *pse, int64_t pse_batch, int64_t pse_type)
+{
+    if (!pse) return TND_OK;
+    if (pse_type == 2 || pse_type == 3) return TND_ERR_UNSUPPORTED;
+    if (pse_type != 0 && pse_type != 1) return TND_ERR_INVALID;
+    if (pse_batch != 1 && pse_batch != p.batch) return TND_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(pse) & 15u) != 0) return TND_ERR_INVALID;
+    if (p.mode != 2 && p.mode != 3) return TND_ERR_UNSUPPORTED;
+    for (int64_t b = 0; b < p.batch; ++b) {
+        if (p.cuq[b + 1] - p.cuq[b] != p.cukv[b + 1] - p.cukv[b]) return TND_ERR_UNSUPPORTED;
+    }
+    return TND_OK;
+}
+
+PseSpec pse_of(const Problem &p, const void *pse, int64_t pse_batch, int64_t pse_type)
+{
+    PseSpec ps{};
+    ps.ptr = pse;
+    ps.batch = (int32_t)pse_batch;
+    ps.type = (int32_t)pse_type;
+    ps.cols = p.s2max;
+    return ps;
+}
+
 // The index rule of the problem's sparseMode (the matrix pointers are filled
 // in by the run calls).
 MaskSpec mask_of(const Problem &p)
@@ -697,16 +725,19 @@ tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int
     return TND_OK;
 }
 
-tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8_t *drop_mask,
-                        const uint8_t *atten_mask, const float *sink, tnd_dtype dtype, int64_t batch,
-                        const int64_t *cuq, const int64_t *cukv, const int64_t *prefix, int64_t nq, int64_t nkv,
-                        int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *out,
-                        float *smax, float *ssum, void *ws, uint64_t ws_size, void *stream)
+tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const void *pse, int64_t pse_batch,
+                        int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *sink,
+                        tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
+                        const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale, double keep,
+                        int64_t pre, int64_t next, int64_t mode, void *out, float *smax, float *ssum, void *ws,
+                        uint64_t ws_size, void *stream)
 {
     if (!q || !k || !v || !out || !smax || !ssum) return TND_ERR_NULLPTR;
     Problem p;
     tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
                              drop_mask != nullptr, atten_mask != nullptr, sink != nullptr, p);
+    if (st != TND_OK) return st;
+    st = check_pse(p, pse, pse_batch, pse_type);
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, (const void *)out, (const void *)smax, (const void *)ssum})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
@@ -730,6 +761,7 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const uint8
     a.smax = smax;
     a.ssum = ssum;
     a.mask_bytes = (mask_bits_total(p) + 7) / 8;
+    a.pse = pse_of(p, pse, pse_batch, pse_type);
     a.qblk = (const QBlockInfo *)(w + L.qblk);
     a.qblk_rows = (const int2 *)(w + L.qblk_rows);
     a.fwd_units = (const int2 *)(w + L.fwd_units);
@@ -781,12 +813,12 @@ tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const in
 
 namespace tnd {
 
-tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                    const uint8_t *atten_mask, const float *smax, const float *ssum, const void *o,
-                    const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                    const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale, double keep,
-                    int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv, float *dsink, void *ws,
-                    uint64_t ws_size, void *stream, bool pinned_upload)
+tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const void *pse, int64_t pse_batch,
+                    int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *smax,
+                    const float *ssum, const void *o, const float *sink, tnd_dtype dtype, int64_t batch,
+                    const int64_t *cuq, const int64_t *cukv, const int64_t *prefix, int64_t nq, int64_t nkv,
+                    int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq,
+                    void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload)
 {
     if (!q || !k || !v || !dy || !smax || !ssum || !o || !dq || !dk || !dv) return TND_ERR_NULLPTR;
     if (sink && !dsink) return TND_ERR_NULLPTR;
@@ -795,6 +827,8 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
     Problem p;
     tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
                              drop_mask != nullptr, atten_mask != nullptr, sink != nullptr, p);
+    if (st != TND_OK) return st;
+    st = check_pse(p, pse, pse_batch, pse_type);
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, dy, (const void *)smax, (const void *)ssum, o, (const void *)dq,
                             (const void *)dk, (const void *)dv})
@@ -840,6 +874,7 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
     a.flags = (int32_t *)(w + L.flags);
     a.dqacc = tc_layout ? (float *)(w + L.dqacc) : nullptr;
     a.mask_bytes = (mask_bits_total(p) + 7) / 8;
+    a.pse = pse_of(p, pse, pse_batch, pse_type);
     {
         const DeviceInfo di = device_info();
         a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)di.clock_khz;
@@ -881,15 +916,16 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
 
 extern "C" {
 
-tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                         const uint8_t *atten_mask, const float *smax, const float *ssum, const void *o,
-                         const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                         const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale, double keep,
-                         int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv, float *dsink,
-                         void *ws, uint64_t ws_size, void *stream)
+tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void *dy, const void *pse,
+                         int64_t pse_batch, int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask,
+                         const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
+                         int64_t batch, const int64_t *cuq, const int64_t *cukv, const int64_t *prefix, int64_t nq,
+                         int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode,
+                         void *dq, void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream)
 {
-    return grad_run(q, k, v, dy, drop_mask, atten_mask, smax, ssum, o, sink, dtype, batch, cuq, cukv, prefix, nq,
-                    nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, ws_size, stream, true);
+    return grad_run(q, k, v, dy, pse, pse_batch, pse_type, drop_mask, atten_mask, smax, ssum, o, sink, dtype, batch,
+                    cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, ws_size,
+                    stream, true);
 }
 
 tnd_status tnd_attn_device_status(const void *ws, uint64_t ws_size, void *stream)

@@ -90,6 +90,30 @@ __host__ __device__ inline bool matrix_keeps(const MaskSpec &m, int64_t i, int64
     return m.amask == nullptr || m.amask[i * m.amask_cols + j] == 0;
 }
 
+// pseShiftOptional: for each sequence (or for all, when batch is 1) and query
+// head, the last 1024 rows of the sequence's [Sq, Skv] bias, stored as
+// [batch][Nq][1024][cols] in the element dtype.  Row i of a sequence is stored
+// row i - (Sq - 1024); a row above the stored ones is read along its diagonal
+// from stored row 0, column j + (Sq - 1024 - i).
+struct PseSpec {
+    const void *ptr;   // NULL = no pse
+    int32_t batch;     // 1 or B
+    int32_t type;      // pseType 0: s = scale*qk + pse;  1: s = scale*(qk + pse)
+    int64_t cols;      // S2Max
+};
+
+__host__ __device__ inline int64_t pse_index(const PseSpec &ps, int32_t nq, int64_t b, int64_t h, int64_t sq,
+                                             int64_t i, int64_t j)
+{
+    int64_t r = i - (sq - 1024), c = j;
+    if (r < 0) {
+        c = j - r;
+        r = 0;
+    }
+    const int64_t bb = ps.batch == 1 ? 0 : b;
+    return ((bb * nq + h) * 1024 + r) * ps.cols + c;
+}
+
 // Work unit of the tensor-core gradient: kv block j of kv head g of
 // sequence b, visiting q blocks [qb_lo, qb_hi) for each of the group's heads.
 struct GradUnit {
@@ -124,6 +148,7 @@ struct GradArgs {
     int64_t tq, tkv;
     float scale, keep_prob, inv_keep;
     MaskSpec mask;
+    PseSpec pse;
     int has_drop, has_sink;
     // workspace regions
     uint32_t *status;
@@ -159,6 +184,7 @@ struct FwdArgs {
     int64_t tq, tkv;
     float scale, keep_prob, inv_keep;
     MaskSpec mask;
+    PseSpec pse;
     int has_drop, has_sink;
     uint32_t *status;
     const SeqDesc *seqs;
@@ -220,8 +246,9 @@ cudaError_t launch_dq_finalize(const GradArgs &a, cudaStream_t s);
 // The gradient call behind tnd_attn_grad.  pinned_upload = false copies the
 // plan from pageable host memory and allocates nothing (the library's pinned
 // staging slots are allocated on first use).
-tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const uint8_t *drop_mask,
-                    const uint8_t *atten_mask, const float *smax, const float *ssum, const void *o,
+tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy, const void *pse, int64_t pse_batch,
+                    int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *smax,
+                    const float *ssum, const void *o,
                     const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
                     const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d,
                     double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv,

@@ -90,9 +90,9 @@ tnd_status tnd_attn_grad_static_ws(const void *q, const void *k, const void *v, 
     if (need > tnd::kStaticWsBytes) return TND_ERR_WORKSPACE;
     void *ws = tnd::static_ws_address();
     if (!ws) return TND_ERR_CUDA;
-    return tnd::grad_run(q, k, v, dy, drop_mask, nullptr, smax, ssum, o, sink, dtype, batch, cuq, cukv, nullptr, nq,
-                         nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, tnd::kStaticWsBytes, stream,
-                         false);
+    return tnd::grad_run(q, k, v, dy, nullptr, 0, 1, drop_mask, nullptr, smax, ssum, o, sink, dtype, batch, cuq, cukv,
+                         nullptr, nq, nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, tnd::kStaticWsBytes,
+                         stream, false);
 }
 
 tnd_status tnd_attn_grad_static_ws_status(void *stream)

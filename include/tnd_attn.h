@@ -63,6 +63,21 @@
  *   values N_b, read only by mode 6 (NULL otherwise).
  * A row that keeps no key (and has no sink) gets max = -inf, sum = 0 and a
  * zero output row; its gradient rows are zero.
+ * pse ([UnpadGrad] parameters, pseShiftOptional; [ScoreV2] parameters,
+ *   pseType): device tensor in the element dtype, [pse_batch, Nq, 1024,
+ *   S2Max] row-major with pse_batch = B (one per sequence) or 1 (shared).
+ *   It holds the last 1024 rows of each sequence's [Sq, Skv] bias (the
+ *   pages' alibi compression, ori_pse[:, :, -1024:, :]): row i of a sequence
+ *   is stored row i - (Sq - 1024), so a sequence shorter than 1024 uses the
+ *   bottom Sq rows; a row above the stored ones (i < Sq - 1024) is read along
+ *   its diagonal from stored row 0, column j + (Sq - 1024 - i), which is
+ *   exact for a bias that depends on i - j only (alibi).  pse_type 1 adds it
+ *   before the scale (scale * (QK^T + pse), the grad page's formula), 0 after
+ *   it (scale * QK^T + pse); 2 and 3 (pse generated inside) return
+ *   TND_ERR_UNSUPPORTED.  With a pse, sparse_mode must be 2 or 3 and Sq_b ==
+ *   Skv_b for every sequence (the pages' alibi constraint), else
+ *   TND_ERR_UNSUPPORTED.  NULL = no pse (pse_batch and pse_type ignored).
+ *   dpseOut is a reserved output on the pages and is not produced.
  * GQA: Nq % Nkv == 0; query head h uses key/value head h / (Nq/Nkv).
  *
  * Two phases, as on the pages ([UnpadGrad] function prototype section): a
@@ -119,12 +134,14 @@ tnd_status tnd_attn_fwd_workspace_size(
 /*
  * Forward ([ScoreV2] function description and parameters): writes
  * attention_out [Tq,Nq,D] (dtype), softmax_max and softmax_sum [Tq,Nq,8]
- * (fp32).  drop_mask, atten_mask, sink and prefix may be NULL where the
- * conventions above allow it.
+ * (fp32).  pse, drop_mask, atten_mask, sink and prefix may be NULL where the
+ * conventions above allow it; the pse checks are made here (the workspace
+ * size does not depend on it).
  */
 tnd_status tnd_attn_fwd(
-    const void *query, const void *key, const void *value, const uint8_t *drop_mask,
-    const uint8_t *atten_mask, const float *sink, tnd_dtype dtype, int64_t batch,
+    const void *query, const void *key, const void *value, const void *pse, int64_t pse_batch,
+    int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *sink,
+    tnd_dtype dtype, int64_t batch,
     const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, const int64_t *prefix,
     int64_t head_num, int64_t kv_head_num, int64_t head_dim, double scale_value,
     double keep_prob, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
@@ -145,14 +162,15 @@ tnd_status tnd_attn_grad_workspace_size(
  * parameters section, plus sinkInOptional / dSink of [UnpadGradV5]).
  * Inputs: query, key, value, dy; softmax_max, softmax_sum and attention_in
  * as written by tnd_attn_fwd; drop_mask (NULL when keep_prob == 1);
- * atten_mask and prefix as for the forward (the same ones it was given);
+ * pse, atten_mask and prefix as for the forward (the same ones it was given);
  * sink (NULL = no sink).  Outputs: dq [Tq,Nq,D], dk and dv [Tkv,Nkv,D]
  * (dtype; dk and dv are summed over the Nq/Nkv query heads of each kv
  * head), dsink [Nq] fp32 (required when sink is given, ignored otherwise).
  */
 tnd_status tnd_attn_grad(
-    const void *query, const void *key, const void *value, const void *dy,
-    const uint8_t *drop_mask, const uint8_t *atten_mask, const float *softmax_max,
+    const void *query, const void *key, const void *value, const void *dy, const void *pse,
+    int64_t pse_batch, int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask,
+    const float *softmax_max,
     const float *softmax_sum, const void *attention_in, const float *sink, tnd_dtype dtype,
     int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
     const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
@@ -230,7 +248,8 @@ tnd_status tnd_attn_grad_plan(
  * that only receives buffers from its host framework's allocator, or a
  * process that reserved all device memory at start-up.  Arguments and
  * results are those of tnd_attn_grad without `workspace` / `workspace_size`,
- * `atten_mask` and `prefix` (so sparse_mode 1 and 6 return TND_ERR_NULLPTR);
+ * `pse`, `atten_mask` and `prefix` (so sparse_mode 1 and 6 return
+ * TND_ERR_NULLPTR);
  * the caller still passes every input and output.
  *
  * The workspace is a fixed device array inside this library of

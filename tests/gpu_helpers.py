@@ -26,6 +26,7 @@ def upload(inp: workloads.Inputs):
     dev["sink"] = None if inp.sink is None else torch.from_numpy(inp.sink).cuda()
     dev["mask"] = None if inp.mask is None else torch.from_numpy(inp.mask).cuda()
     dev["amask"] = None if inp.amask is None else torch.from_numpy(inp.amask).cuda()
+    dev["pse"] = None if inp.pse is None else to_device(inp.pse, wl.dtype)
     return dev
 
 
@@ -35,10 +36,10 @@ def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0):
     dev = dev or upload(inp)
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, grad_path) == tnd.TND_OK
     try:
-        amask = dev.get("amask")
+        amask, pse = dev.get("amask"), dev.get("pse")
         out, smax, ssum = tnd.fwd(dev["q"], dev["k"], dev["v"], wl.cu_q, wl.cu_kv, wl.scale, wl.keep_prob,
                                   wl.pre_tokens, wl.next_tokens, wl.sparse_mode, dev["mask"], dev["sink"],
-                                  atten_mask=amask, prefix=wl.prefix)
+                                  atten_mask=amask, prefix=wl.prefix, pse=pse, pse_type=wl.pse_type)
         ws_bytes = tnd.grad_workspace_bytes(dev["q"], dev["k"], wl.cu_q, wl.cu_kv, wl.scale, wl.keep_prob,
                                             wl.pre_tokens, wl.next_tokens, wl.sparse_mode,
                                             dev["mask"] is not None, dev["sink"] is not None,
@@ -47,7 +48,7 @@ def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0):
         dq, dk, dv, dsink = tnd.grad(dev["q"], dev["k"], dev["v"], dev["dy"], out, smax, ssum, wl.cu_q,
                                      wl.cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens, wl.next_tokens,
                                      wl.sparse_mode, dev["mask"], dev["sink"], workspace=ws,
-                                     atten_mask=amask, prefix=wl.prefix)
+                                     atten_mask=amask, prefix=wl.prefix, pse=pse, pse_type=wl.pse_type)
         torch.cuda.synchronize()
         st = tnd.device_status(ws)
         assert st == tnd.TND_OK, f"device status {st}: {tnd.tnd_status_string(st)}"
@@ -62,7 +63,7 @@ def host64(t: torch.Tensor) -> np.ndarray:
 
 def oracle_problem(inp: workloads.Inputs, **kw) -> oracle.Problem:
     return oracle.problem_from_workload(inp.wl, drop_mask=inp.mask, sink=inp.sink, atten_mask=inp.amask,
-                                        prefix=inp.wl.prefix, **kw)
+                                        prefix=inp.wl.prefix, pse=inp.pse64, pse_type=inp.wl.pse_type, **kw)
 
 
 def oracle_reference(inp: workloads.Inputs, **kw):
@@ -81,6 +82,18 @@ def gamma(n):
     n-term fp32 sum or dot product (|fl(x.y) - x.y| <= gamma_n sum |x_i y_i|)."""
     nu = np.asarray(n, dtype=np.float64) * U32
     return nu / (1.0 - nu)
+
+
+def pse_matrix(p, b, h, sq, skv):
+    """The [sq, skv] pse of (sequence b, head h) as the oracle reads it (zeros without one)."""
+    if p.pse is None:
+        return np.zeros((sq, skv))
+    return np.array([[oracle.pse_at(p, b, h, i, j) for j in range(skv)] for i in range(sq)]).reshape(sq, skv)
+
+
+def pse_logit(wl, qk, pse):
+    """Scores from Q K^T and the pse, in the pse type's order."""
+    return wl.scale * (qk + pse) if wl.pse_type == 1 else wl.scale * qk + pse
 
 
 def fp32_error_bound(inp: workloads.Inputs, ref: dict) -> dict:
@@ -122,8 +135,10 @@ def fp32_error_bound(inp: workloads.Inputs, ref: dict) -> dict:
             else:
                 Z = np.ones((sq, skv))
             live = l > 0
-            S = wl.scale * Q @ K.T
-            Sabs = wl.scale * np.abs(Q) @ np.abs(K).T
+            PSE = pse_matrix(p, b, h, sq, skv)
+            S = pse_logit(wl, Q @ K.T, PSE)
+            # |terms| of the score sum; the pse is one more term (one more rounding)
+            Sabs = pse_logit(wl, np.abs(Q) @ np.abs(K).T, np.abs(PSE))
             P = np.where(keep & live[:, None], np.exp(S - np.where(live, m, 0)[:, None])
                          / np.where(live, l, 1)[:, None], 0.0)
             smax_abs = np.where(keep, Sabs, 0).max(axis=1)
@@ -174,7 +189,8 @@ def plain_fp32_eval(inp: workloads.Inputs) -> dict:
             kv = h // g
             Q, dY = q[q0:q0 + sq, h], dy[q0:q0 + sq, h]
             K, V = k[k0:k0 + skv, kv], v[k0:k0 + skv, kv]
-            S = (Q @ K.T) * wl.scale
+            PSE = torch.from_numpy(pse_matrix(p, b, h, sq, skv)).float()
+            S = (Q @ K.T + PSE) * wl.scale if wl.pse_type == 1 else (Q @ K.T) * wl.scale + PSE
             S = torch.where(keep, S, torch.tensor(-float("inf")))
             m = S.max(dim=1).values
             if inp.sink is not None:

@@ -107,7 +107,8 @@ def test_null_workspace_size_pointer_and_seqlens():
 def _grad_call(**over):
     """tnd_attn_grad with fake aligned device addresses; only arguments that
     fail validation are used, so nothing is ever dereferenced."""
-    args = dict(query=4096, key=4096, value=4096, dy=4096, drop_mask=None, atten_mask=None, softmax_max=4096,
+    args = dict(query=4096, key=4096, value=4096, dy=4096, pse=None, pse_batch=0, pse_type=1, drop_mask=None,
+                atten_mask=None, softmax_max=4096,
                 softmax_sum=4096, attention_in=4096, sink=None, dtype=tnd.TND_BF16, batch=1, cu_q=[0, 8],
                 cu_kv=[0, 8], prefix=None, head_num=2, kv_head_num=1, head_dim=128, scale_value=0.1,
                 keep_prob=1.0, pre_tokens=INF, next_tokens=INF,
@@ -126,6 +127,12 @@ def _grad_call(**over):
     (dict(sparse_mode=1), tnd.TND_ERR_NULLPTR),                  # no attention-mask matrix
     (dict(sparse_mode=6), tnd.TND_ERR_NULLPTR),                  # no prefix
     (dict(sparse_mode=6, prefix=[9]), tnd.TND_ERR_INVALID),
+    (dict(pse=4096, pse_batch=1, sparse_mode=0), tnd.TND_ERR_UNSUPPORTED),   # pse needs a lower triangle
+    (dict(pse=4096, pse_batch=1, pse_type=2), tnd.TND_ERR_UNSUPPORTED),      # pse generated inside
+    (dict(pse=4096, pse_batch=1, pse_type=5), tnd.TND_ERR_INVALID),
+    (dict(pse=4096, pse_batch=3), tnd.TND_ERR_INVALID),                      # first dim is 1 or B
+    (dict(pse=4098, pse_batch=1), tnd.TND_ERR_INVALID),                      # misaligned
+    (dict(pse=4096, pse_batch=1, cu_kv=[0, 9]), tnd.TND_ERR_UNSUPPORTED),    # Sq != Skv
     (dict(head_num=3, kv_head_num=2), tnd.TND_ERR_INVALID),
     (dict(query=4098), tnd.TND_ERR_INVALID),                     # misaligned
     (dict(workspace=None, workspace_size=0), tnd.TND_ERR_WORKSPACE),

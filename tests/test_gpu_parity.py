@@ -53,6 +53,12 @@ SMALL = {
                                    dict(prefix=[0, 64])),
     "prefix_fp32_d64_dropout": ("f32", [70, 40], [70, 90], 2, 1, 64, 6, INF, INF, 0.75, False,
                                 dict(prefix=[10, 90])),
+    # pseShiftOptional: the stored last 1024 rows (rows above read along their diagonal), pseType 1 / 0
+    "pse_alibi_bf16_long": ("bf16", [1300, 200], None, 4, 2, 128, 3, INF, INF, 1.0, False,
+                            dict(pse=("alibi", 2, 1))),
+    "pse_random_fp16_d64_type0": ("f16", [300, 129], None, 2, 2, 64, 2, INF, INF, 0.9, True,
+                                  dict(pse=("random", 1, 0))),
+    "pse_random_fp32": ("f32", [90, 33], None, 2, 1, 64, 3, INF, INF, 1.0, False, dict(pse=("random", 2, 1))),
 }
 
 
@@ -61,7 +67,8 @@ def _small(name, seed=777):
     extra = SMALL[name][11] if len(SMALL[name]) > 11 else {}
     wl = workloads.custom(name, dt, sq, sq if skv is None else skv, nq, nkv, d, keep_prob=keep,
                           pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, has_sink=sink, seed=seed,
-                          amask_density=extra.get("amask", 0.0), prefix=extra.get("prefix"))
+                          amask_density=extra.get("amask", 0.0), prefix=extra.get("prefix"),
+                          **(dict(zip(("pse_kind", "pse_batch", "pse_type"), extra["pse"])) if "pse" in extra else {}))
     return workloads.make_inputs(wl)
 
 

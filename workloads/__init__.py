@@ -34,6 +34,11 @@ element 1 (masked) with probability ``amask_density`` (uniform 16-bit integer
 against round(density * 65536)); every row i with i % 97 == 5 is fully
 masked, so rows that keep no key occur.  Prefix values (sparseMode 6) are
 given with the workload.
+
+pse (positional bias), stored as [B or 1, Nq, 1024, S2Max], the last 1024
+rows of each sequence's bias: "random" draws every stored element N(0, 0.25);
+"alibi" stores slope_h * (j - i) with slope_h = 2^-(4 + h) (zero beyond the
+sequence's columns); both are rounded to the dtype like the other tensors.
 """
 
 from __future__ import annotations
@@ -45,7 +50,7 @@ from typing import Dict, List, Optional
 import numpy as np
 
 # stream ids of the independent tensors drawn for one workload
-_STREAM = {"seqlens": 1, "q": 2, "k": 3, "v": 4, "dy": 5, "sink": 6, "mask": 7, "amask": 8}
+_STREAM = {"seqlens": 1, "q": 2, "k": 3, "v": 4, "dy": 5, "sink": 6, "mask": 7, "amask": 8, "pse": 9}
 
 BASE_SEED = 20261202
 
@@ -70,6 +75,9 @@ class Workload:
     seed: int = BASE_SEED
     amask_density: float = 0.0             # > 0: an attention-mask matrix is drawn
     prefix: Optional[List[int]] = None     # prefixOptional (sparseMode 6)
+    pse_kind: str = ""                     # "", "random" or "alibi"
+    pse_batch: int = 1                     # 1 (shared) or B
+    pse_type: int = 1                      # pseType 0 / 1
 
     @property
     def batch(self) -> int:
@@ -229,6 +237,8 @@ class Inputs:
     sink: Optional[np.ndarray]          # float32 [Nq] or None
     mask: Optional[np.ndarray]          # uint8 packed keep-bits or None
     amask: Optional[np.ndarray] = None  # uint8 [S1Max, S2Max] attention-mask matrix (nonzero masks) or None
+    pse: Optional[np.ndarray] = None    # [pse_batch, Nq, 1024, S2Max] in the storage dtype, or None
+    pse64: Optional[np.ndarray] = None  # its exact fp64 values
 
 
 def make_inputs(wl: Workload, with_fp64: bool = True) -> Inputs:
@@ -246,9 +256,29 @@ def make_inputs(wl: Workload, with_fp64: bool = True) -> Inputs:
     amask = None
     if wl.amask_density > 0:
         amask = atten_mask_matrix(wl.seed, max(wl.seqlens_q), max(wl.seqlens_kv), wl.amask_density)
+    pse = pse64 = None
+    if wl.pse_kind:
+        pse, pse64 = pse_store(wl)
     if not with_fp64:
         q64 = k64 = v64 = dy64 = None
-    return Inputs(wl, q, k, v, dy, q64, k64, v64, dy64, sink, mask, amask)
+    return Inputs(wl, q, k, v, dy, q64, k64, v64, dy64, sink, mask, amask, pse, pse64)
+
+
+def pse_store(wl: Workload):
+    """[pse_batch, Nq, 1024, S2Max] pse store ("random" or "alibi"), rounded to the dtype."""
+    s2 = max(wl.seqlens_kv)
+    shape = (wl.pse_batch, wl.nq, 1024, s2)
+    if wl.pse_kind == "random":
+        x = 0.5 * _rng(wl.seed, "pse").standard_normal(size=shape, dtype=np.float64)
+    else:
+        x = np.zeros(shape)
+        slopes = 2.0 ** -(4.0 + np.arange(wl.nq))
+        for b in range(wl.pse_batch):
+            sq = wl.seqlens_q[b]
+            rows = np.arange(1024) + (sq - 1024)          # the sequence row each stored row holds
+            cols = np.arange(s2)
+            x[b] = slopes[:, None, None] * (cols[None, None, :] - rows[None, :, None])
+    return round_to_dtype(x, wl.dtype)
 
 
 def atten_mask_matrix(seed: int, rows: int, cols: int, density: float) -> np.ndarray:
@@ -264,9 +294,10 @@ def atten_mask_matrix(seed: int, rows: int, cols: int, density: float) -> np.nda
 def custom(name: str, dtype: str, seqlens_q, seqlens_kv, nq: int, nkv: int, d: int, *,
            scale: Optional[float] = None, keep_prob: float = 1.0, pre_tokens: int = 2147483647,
            next_tokens: int = 2147483647, sparse_mode: int = 0, has_sink: bool = False,
-           seed: int = BASE_SEED, amask_density: float = 0.0, prefix=None) -> Workload:
+           seed: int = BASE_SEED, amask_density: float = 0.0, prefix=None, pse_kind: str = "",
+           pse_batch: int = 1, pse_type: int = 1) -> Workload:
     """A workload with explicit shapes (used for edge cases and small parity runs)."""
     return Workload(name, dtype, list(seqlens_q), list(seqlens_kv), nq, nkv, d,
                     1.0 / math.sqrt(d) if scale is None else scale, keep_prob, pre_tokens,
                     next_tokens, sparse_mode, has_sink, seed, amask_density,
-                    None if prefix is None else list(prefix))
+                    None if prefix is None else list(prefix), pse_kind, pse_batch, pse_type)
