@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libtndattn.so")
 TND_OK, TND_ERR_NULLPTR, TND_ERR_INVALID, TND_ERR_UNSUPPORTED = 0, 1, 2, 3
 TND_ERR_WORKSPACE, TND_ERR_CUDA, TND_ERR_DEVICE_TIMEOUT, TND_ERR_DEVICE_CHECK = 4, 5, 6, 7
 TND_F16, TND_BF16, TND_F32 = 0, 1, 2
-TND_OPT_GRAD_PATH, TND_OPT_WAIT_LIMIT_MS, TND_OPT_PROFILE, TND_OPT_TEST_SKIP_LOAD = 0, 1, 2, 3
+TND_OPT_GRAD_PATH, TND_OPT_WAIT_LIMIT_MS, TND_OPT_PROFILE, TND_OPT_TEST_SKIP_LOAD, TND_OPT_DETERMINISTIC = 0, 1, 2, 3, 4
 
 # exported symbols, in header order
 SYMBOLS = ["tnd_attn_fwd_workspace_size", "tnd_attn_fwd", "tnd_attn_grad_workspace_size", "tnd_attn_grad",

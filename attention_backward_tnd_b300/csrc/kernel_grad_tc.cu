@@ -20,7 +20,11 @@
 // each only after its predecessor's counter says that update is complete.
 // dq_finalize_kernel then writes dQ = scale * accumulator in the output
 // dtype.  The adds are read-modify-writes in global memory, but their order
-// is fixed, so results are bitwise deterministic.
+// is fixed, so results are bitwise deterministic.  With the library's
+// deterministic option off (the non-deterministic default of the
+// "aclnnFlashAttentionUnpaddingScoreGradV5" constraints), a
+// later contributor waits only for the first one's store and adds in
+// arrival order: the same sum, rounded in a run-dependent order.
 //
 // Tiles are 128 kv rows x 128 q rows, so S^T, dP^T and dQ^T are N = 128
 // UMMAs.  TMEM (512 columns): dV, dK accumulators; S^T (then Pd^T packed
@@ -971,8 +975,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t ui = 0, gt = 0;
             bool ok = true;
+            // counter release owed for the last issued tile.  In chain order
+            // it is settled at once (a later release holds up the next
+            // contributor: measured slower).  In arrival order only first
+            // contributors release, and their writes are waited for once the
+            // next tile is issued, as long as the writer has a staged tile
+            // and a ready chain to go on with; before any wait the release is
+            // settled, so the writer never waits while holding back a
+            // counter another CTA may wait on
+            int *owed = nullptr;
+            int owed_val = 0;
+            auto settle = [&]() {
+                if (owed) {
+                    bulk_wait0();
+                    fence_async_global();
+                    fence_acq_rel_gpu();
+                    st_relaxed_gpu(owed, owed_val);
+                    owed = nullptr;
+                }
+            };
             while (ok) {
                 int u;
+                if (!mbar_test_wait(sm.bar(B_UNIT_FULL + (ui & 1u)), (ui >> 1) & 1u)) settle();
                 if (!read_unit1(sm, ui, a, u)) break;
                 ++ui;
                 if (u < 0) break;
@@ -984,29 +1008,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int *flag = a.flags + (int64_t)qg * a.nq + h;
                     const int pos = qi.jhi - U.jb;
                     const uint32_t s = gt & 1u;
-                    if (!wait_k(sm, B_STG_FULL + s, gt >> 1, a)) {
-                        ok = false;
-                        break;
+                    if (!mbar_test_wait(sm.bar(B_STG_FULL + s), (gt >> 1) & 1u)) {
+                        settle();
+                        if (!wait_k(sm, B_STG_FULL + s, gt >> 1, a)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     TRACE(EV_W_STG, gt);
-                    if (pos > 0) {
-                        const long long t0 = clock64();
-                        while (ld_acquire_gpu(flag) < pos) {
-                            if (*sm.abort_flag()) {
-                                ok = false;
-                                break;
+                    // ordered: every earlier contributor's update is complete;
+                    // arrival order: the first contributor's store is
+                    const int need = a.deterministic ? pos : min(pos, 1);
+                    if (need > 0) {
+                        if (ld_acquire_gpu(flag) < need) {
+                            settle();
+                            const long long t0 = clock64();
+                            while (ld_acquire_gpu(flag) < need) {
+                                if (*sm.abort_flag()) {
+                                    ok = false;
+                                    break;
+                                }
+                                if (clock64() - t0 > a.wait_limit_cycles) {
+                                    // detail: the awaited position and the (q block, head) counter
+                                    set_status(a.status, TND_ERR_DEVICE_TIMEOUT,
+                                               0x80000000u | ((uint32_t)pos << 24) | (uint32_t)(qg * a.nq + h));
+                                    *sm.abort_flag() = 1;
+                                    ok = false;
+                                    break;
+                                }
+                                __nanosleep(32);
                             }
-                            if (clock64() - t0 > a.wait_limit_cycles) {
-                                // detail: the awaited position and the (q block, head) counter
-                                set_status(a.status, TND_ERR_DEVICE_TIMEOUT,
-                                           0x80000000u | ((uint32_t)pos << 24) | (uint32_t)(qg * a.nq + h));
-                                *sm.abort_flag() = 1;
-                                ok = false;
-                                break;
-                            }
-                            __nanosleep(32);
+                            if (!ok) break;
                         }
-                        if (!ok) break;
                         fence_async_global();   // the counter's acquire before the async-proxy adds
                     }
                     TRACE(EV_W_CHAIN, gt);
@@ -1033,19 +1066,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit();
                     }
                     TRACE(EV_W_ISSUED, gt);
+                    if (owed) {
+                        // every group but this tile's two: the previous tile's writes
+                        bulk_wait2();
+                        fence_async_global();
+                        fence_acq_rel_gpu();
+                        st_relaxed_gpu(owed, owed_val);
+                        owed = nullptr;
+                    }
                     bulk_wait_read1();                              // the Q-stage half
                     mbar_arrive(sm.bar(B_Q_EMPTY + s));
                     bulk_wait_read0();                              // the dY-stage half
                     mbar_arrive(sm.bar(B_DY_EMPTY + s));
                     TRACE(EV_W_READ, gt);
-                    bulk_wait0();
-                    fence_async_global();
-                    fence_acq_rel_gpu();
-                    st_relaxed_gpu(flag, pos + 1);
+                    if (a.deterministic || pos == 0) {
+                        owed = flag;
+                        owed_val = pos + 1;
+                        if (a.deterministic) settle();
+                    }
                     TRACE(EV_W_WRITTEN, gt);
                 }
             }
-            bulk_wait0();
+            settle();
         }
         __syncwarp();
     }

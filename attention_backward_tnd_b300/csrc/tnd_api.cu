@@ -24,6 +24,7 @@ struct Options {
     int64_t wait_limit_ms = 2000;
     int profile = 0;
     int test_skip_load = 0;
+    int deterministic = 1;
 };
 Options g_opt;
 std::mutex g_mu;
@@ -675,6 +676,10 @@ tnd_status tnd_attn_set_option(tnd_option option, int64_t value)
         if (value != 0 && value != 1) return TND_ERR_INVALID;
         g_opt.test_skip_load = (int)value;
         return TND_OK;
+    case TND_OPT_DETERMINISTIC:
+        if (value != 0 && value != 1) return TND_ERR_INVALID;
+        g_opt.deterministic = (int)value;
+        return TND_OK;
     }
     return TND_ERR_INVALID;
 }
@@ -880,6 +885,7 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
         a.wait_limit_cycles = g_opt.wait_limit_ms * (int64_t)di.clock_khz;
         a.num_sms = di.num_sms;
         a.test_flags = g_opt.test_skip_load ? 1 : 0;
+        a.deterministic = g_opt.deterministic;
     }
     if (p.has_amask) {
         a.mask.amask = atten_mask;

@@ -171,6 +171,7 @@ struct GradArgs {
     int64_t wait_limit_cycles;
     int32_t num_sms;
     int32_t test_flags;       // bit 0: CTA 0 skips its first K load (bounded-wait test)
+    int32_t deterministic;    // 1: dQ contributions added in chain order; 0: in arrival order
 };
 
 struct FwdArgs {

@@ -418,6 +418,44 @@ def run_ours(args, wl, rank, world, local_rank):
                    "tflops": 4.0 * wl.d * kept_pairs(wl) / (fms * 1e-3) / 1e12,
                    "flop": "4 * D per kept pair (S = Q K^T and O = P V)"}
 
+    # the same steps with deterministic computing off (dQ contributions added
+    # in arrival order): reported beside the default, deterministic figures
+    arrival = None
+    if main.startswith("grad_tc"):
+        assert tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, 0) == tnd.TND_OK
+        try:
+            for _ in range(max(args.warmup, 0)):
+                flush.fill_(1)
+                step()
+            a_ms = []
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                starts[i].record()
+                step()
+                ends[i].record()
+            torch.cuda.synchronize()
+            a_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+            tnd.tnd_attn_set_option(tnd.TND_OPT_PROFILE, 1)
+            tnd.tnd_attn_profile_read(reset=True)
+            for i in range(prof_steps):
+                flush.fill_(i & 0xFF)
+                step()
+            torch.cuda.synchronize()
+            aprof = tnd.tnd_attn_profile_read(reset=True)
+        finally:
+            tnd.tnd_attn_set_option(tnd.TND_OPT_PROFILE, 0)
+            tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, 1)
+        st = tnd.device_status(ws)
+        if st != tnd.TND_OK:
+            raise SystemExit(f"device status after arrival-order steps: {tnd.tnd_status_string(st)}")
+        a_step = float(statistics.median(a_ms))
+        a_main = aprof[main][0] / aprof[main][1]
+        arrival = {"ms_per_step": a_step, "value": flop / (a_step * 1e-3) / 1e12, "main_ms": a_main,
+                   "main_frac": flop / (a_main * 1e-3) / 1e12 / peak,
+                   "note": "deterministic computing off: each (q block, head)'s dQ contributions are added in "
+                           "arrival order (not bitwise repeatable); value and roofline above are the default, "
+                           "deterministic order"}
+
     # end to end: pinned host inputs -> device, gradient, device -> pinned host outputs
     host_in = [t.cpu().pin_memory() for t in (q, k, v, dy, out, smax, ssum)]
     dev_in = [q, k, v, dy, out, smax, ssum]
@@ -474,6 +512,7 @@ def run_ours(args, wl, rank, world, local_rank):
             "kernels_note": f"device time per launch from a separate pass of {prof_steps} steps with per-kernel "
                             "events (the timed steps run without them)",
             "forward": forward,
+            "arrival_order": arrival,
             "gpu_launches": launches,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},

@@ -204,12 +204,22 @@ const char *tnd_status_string(tnd_status status);
  *                    the wait for it expires and the call reports
  *                    TND_ERR_DEVICE_TIMEOUT through tnd_attn_device_status
  *                    (its outputs are then invalid); 0 = off (default).
+ *   TND_OPT_DETERMINISTIC: deterministic computing ([UnpadGradV5]
+ *                    constraints: the gradient is non-deterministic unless
+ *                    deterministic computing is switched on).  1 (default) = the tensor-core
+ *                    gradient adds the dQ contributions of every (q block,
+ *                    head) in a fixed order, so repeated calls give bitwise
+ *                    identical results; 0 = they are added in arrival order
+ *                    (same tolerance against the exact result, rounding
+ *                    order varies from call to call).  The CUDA-core kernels
+ *                    are deterministic either way.
  */
 typedef enum tnd_option {
     TND_OPT_GRAD_PATH = 0,
     TND_OPT_WAIT_LIMIT_MS = 1,
     TND_OPT_PROFILE = 2,
-    TND_OPT_TEST_SKIP_LOAD = 3
+    TND_OPT_TEST_SKIP_LOAD = 3,
+    TND_OPT_DETERMINISTIC = 4
 } tnd_option;
 tnd_status tnd_attn_set_option(tnd_option option, int64_t value);
 

@@ -30,11 +30,12 @@ def upload(inp: workloads.Inputs):
     return dev
 
 
-def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0):
+def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0, deterministic: bool = True):
     """Forward then gradient through the library; returns device tensors."""
     wl = inp.wl
     dev = dev or upload(inp)
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, grad_path) == tnd.TND_OK
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, int(deterministic)) == tnd.TND_OK
     try:
         amask, pse = dev.get("amask"), dev.get("pse")
         out, smax, ssum = tnd.fwd(dev["q"], dev["k"], dev["v"], wl.cu_q, wl.cu_kv, wl.scale, wl.keep_prob,
@@ -54,6 +55,7 @@ def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0):
         assert st == tnd.TND_OK, f"device status {st}: {tnd.tnd_status_string(st)}"
     finally:
         tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, 0)
+        tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, 1)
     return {"out": out, "smax": smax, "ssum": ssum, "dq": dq, "dk": dk, "dv": dv, "dsink": dsink, "ws": ws}
 
 

@@ -150,6 +150,9 @@ def test_set_option_checks_values():
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_GRAD_PATH, 0) == tnd.TND_OK
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_TEST_SKIP_LOAD, 2) == tnd.TND_ERR_INVALID
     assert tnd.tnd_attn_set_option(tnd.TND_OPT_TEST_SKIP_LOAD, 0) == tnd.TND_OK
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, 2) == tnd.TND_ERR_INVALID
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, 0) == tnd.TND_OK
+    assert tnd.tnd_attn_set_option(tnd.TND_OPT_DETERMINISTIC, 1) == tnd.TND_OK
 
 
 # ---------------------------------------------------------------------------
