@@ -54,6 +54,7 @@ class _Problem(ctypes.Structure):
         ("prefix", ctypes.POINTER(ctypes.c_int64)),
         ("pse", ctypes.POINTER(ctypes.c_double)),
         ("pse_batch", ctypes.c_int64), ("pse_cols", ctypes.c_int64), ("pse_type", ctypes.c_int64),
+        ("Dv", ctypes.c_int64),
     ]
 
 
@@ -112,6 +113,8 @@ class Problem:
     ``row_lo`` (one int per sequence) skips query rows i < row_lo[b].
     ``atten_mask`` is the [S1Max, S2Max] attention-mask matrix (nonzero masks)
     for sparseMode 0 / 1; ``prefix`` the per-sequence prefix N for mode 6.
+    ``dv`` is the head dim of value, dy, the output and dV (default ``d``;
+    the pages allow qD == kD >= vD).
     """
 
     def __init__(self, cu_q: Sequence[int], cu_kv: Sequence[int], nq: int, nkv: int, d: int,
@@ -120,11 +123,14 @@ class Problem:
                  drop_mask: Optional[np.ndarray] = None, sink: Optional[np.ndarray] = None,
                  heads: Optional[Sequence[int]] = None, row_lo: Optional[Sequence[int]] = None,
                  atten_mask: Optional[np.ndarray] = None, prefix: Optional[Sequence[int]] = None,
-                 pse: Optional[np.ndarray] = None, pse_type: int = 1):
+                 pse: Optional[np.ndarray] = None, pse_type: int = 1, dv: Optional[int] = None):
         self.cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
         self.cu_kv = np.ascontiguousarray(cu_kv, dtype=np.int64)
         self.nq, self.nkv, self.d = int(nq), int(nkv), int(d)
+        self.dv = self.d if dv is None else int(dv)
         assert self.nq % self.nkv == 0
+        if not 1 <= self.dv <= self.d:
+            raise ValueError("value head dim must be in [1, D] (qD == kD >= vD)")
         self.drop_mask = None if drop_mask is None else np.ascontiguousarray(drop_mask, dtype=np.uint8)
         self.sink = None if sink is None else np.ascontiguousarray(sink, dtype=np.float64)
         self.row_lo = None if row_lo is None else np.ascontiguousarray(row_lo, dtype=np.int64)
@@ -172,7 +178,7 @@ class Problem:
             else self.pse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
             0 if self.pse is None else self.pse.shape[0],
             0 if self.pse is None else self.pse.shape[3],
-            int(pse_type))
+            int(pse_type), self.dv)
 
     @property
     def tq(self) -> int:
@@ -193,6 +199,7 @@ class Problem:
 
 def problem_from_workload(wl, drop_mask=None, sink=None, **kw) -> Problem:
     """Problem for a ``workloads.Workload`` (the sink is passed as fp64)."""
+    kw.setdefault("dv", getattr(wl, "dv", None))
     return Problem(wl.cu_q, wl.cu_kv, wl.nq, wl.nkv, wl.d, wl.scale, wl.keep_prob,
                    wl.pre_tokens, wl.next_tokens, wl.sparse_mode, drop_mask,
                    None if sink is None else np.asarray(sink, dtype=np.float64), **kw)
@@ -221,9 +228,9 @@ def keep_bit(mask: np.ndarray, index: int) -> int:
 
 
 def fwd(p: Problem, q: np.ndarray, k: np.ndarray, v: np.ndarray):
-    """fp64 forward: returns (out [Tq,Nq,D], smax [Tq,Nq], ssum [Tq,Nq])."""
+    """fp64 forward: returns (out [Tq,Nq,Dv], smax [Tq,Nq], ssum [Tq,Nq])."""
     q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
-    out = np.zeros((p.tq, p.nq, p.d))
+    out = np.zeros((p.tq, p.nq, p.dv))
     smax = np.full((p.tq, p.nq), np.nan)
     ssum = np.full((p.tq, p.nq), np.nan)
     rc = lib().ora_fwd(ctypes.byref(p._c), _dptr(q), _dptr(k), _dptr(v), _dptr(out),

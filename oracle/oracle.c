@@ -74,6 +74,10 @@
  *     is read along its diagonal from stored row 0, column j + (Sq - 1024 - i),
  *     which reproduces a bias that depends only on i - j (alibi).  dpseOut is
  *     a reserved output on the pages and is not computed.
+ *   - head dims [UnpadGrad, constraints: qD == kD >= vD]: query, key, dQ and
+ *     dK have D columns; value, dy, the attention output and dV have Dv <= D
+ *     (Dv = D when not given).  <Q_i, K_j> runs over D, <dY_i, V_j> and
+ *     <dY_i, O_i> over Dv; scaleValue is used as given.
  *
  * Everything is plain fp64 loops over rows; the selection fields of
  * ora_problem (head range, first row per sequence) only narrow loop bounds so
@@ -105,6 +109,8 @@ typedef struct ora_problem {
     /* pseShiftOptional [pse_batch][Nq][1024][pse_cols] (NULL = none) and pseType */
     const double *pse;
     int64_t pse_batch, pse_cols, pse_type;
+    /* head dim of value, dy, attention out and dv (0 = D); query and key use D */
+    int64_t Dv;
 } ora_problem;
 
 /* sparseMode predicate; [UnpadGrad, parameters: sparseMode]. */
@@ -190,6 +196,9 @@ static double dot(const double *a, const double *b, int64_t n)
     return acc;
 }
 
+/* vD [UnpadGrad, constraints: qD == kD >= vD] */
+static int64_t value_dim(const ora_problem *p) { return p->Dv > 0 ? p->Dv : p->D; }
+
 static int row_selected(const ora_problem *p, int64_t b, int64_t i)
 {
     return p->row_lo == NULL || i >= p->row_lo[b];
@@ -253,7 +262,7 @@ static int row_of(const ora_problem *p, int64_t r, int64_t *b_out, int64_t *h_ou
 }
 
 /*
- * Forward: out [Tq][Nq][D], smax / ssum [Tq][Nq] (natural-log units).
+ * Forward: out [Tq][Nq][Dv], smax / ssum [Tq][Nq] (natural-log units).
  * [UnpadGrad] Y = Dropout(Softmax(Mask(scale QK^T)), keep_prob) V, with the
  * forward's max and sum as described for softmaxMax / softmaxSum [ScoreV2].
  * Every query row is independent; rows run in parallel.
@@ -261,7 +270,7 @@ static int row_of(const ora_problem *p, int64_t r, int64_t *b_out, int64_t *h_ou
 int ora_fwd(const ora_problem *p, const double *q, const double *k, const double *v,
             double *out, double *smax, double *ssum)
 {
-    const int64_t D = p->D, G = p->Nq / p->Nkv;
+    const int64_t Dv = value_dim(p), G = p->Nq / p->Nkv;
     const int64_t nrows = p->cu_q[p->B] * p->Nq, skvmax = max_skv(p);
     int err = 0;
 #pragma omp parallel
@@ -280,14 +289,14 @@ int ora_fwd(const ora_problem *p, const double *q, const double *k, const double
             double m, l;
             row_scores(p, q, k, b, h, i, s, kept);
             row_max_sum(p, h, s, kept, skv, &m, &l);
-            double *o = out + r * D;
-            for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+            double *o = out + r * Dv;
+            for (int64_t d = 0; d < Dv; ++d) o[d] = 0.0;
             if (l > 0.0) {
                 for (int64_t j = 0; j < skv; ++j) {
                     if (!kept[j]) continue;
                     const double w = exp(s[j] - m) / l * drop_z(p, base, h, i, j, sq, skv);
-                    const double *vj = v + ((tk + j) * p->Nkv + g) * D;
-                    for (int64_t d = 0; d < D; ++d) o[d] += w * vj[d];
+                    const double *vj = v + ((tk + j) * p->Nkv + g) * Dv;
+                    for (int64_t d = 0; d < Dv; ++d) o[d] += w * vj[d];
                 }
             }
             smax[r] = m;
@@ -304,17 +313,17 @@ static double grad_ds(const ora_problem *p, const double *q, const double *k, co
                       const double *dy, double m, double l, double Di, int64_t b, int64_t base,
                       int64_t h, int64_t i, int64_t j, double *pz_out)
 {
-    const int64_t G = p->Nq / p->Nkv, g = h / G, D = p->D;
+    const int64_t G = p->Nq / p->Nkv, g = h / G, D = p->D, Dv = value_dim(p);
     const int64_t tq = p->cu_q[b], tk = p->cu_kv[b];
     const int64_t sq = p->cu_q[b + 1] - tq, skv = p->cu_kv[b + 1] - tk;
     *pz_out = 0.0;
     if (!ora_keep_at(p, b, sq, skv, i, j) || !(l > 0.0)) return 0.0;
     const int64_t r = (tq + i) * p->Nq + h;
-    const double *kj = k + ((tk + j) * p->Nkv + g) * D, *vj = v + ((tk + j) * p->Nkv + g) * D;
+    const double *kj = k + ((tk + j) * p->Nkv + g) * D, *vj = v + ((tk + j) * p->Nkv + g) * Dv;
     const double s = logit(p, dot(q + r * D, kj, D), b, h, sq, i, j);
     const double pij = exp(s - m) / l;
     const double z = drop_z(p, base, h, i, j, sq, skv);
-    const double dP = dot(dy + r * D, vj, D);
+    const double dP = dot(dy + r * Dv, vj, Dv);
     *pz_out = pij * z;
     return pij * (z * dP - Di);
 }
@@ -322,7 +331,7 @@ static double grad_ds(const ora_problem *p, const double *q, const double *k, co
 /*
  * Gradient from the forward's out / smax / ssum (as the grad operator consumes
  * attentionIn, softmaxMax and softmaxSum [UnpadGrad, parameters]).
- * dq like q; dk, dv like k; dsink [Nq] (may be NULL without a sink).
+ * dq like q, dk like k, dv like v; dsink [Nq] (may be NULL without a sink).
  * ds_dense (may be NULL): dS at the flat keep-bit index of every (b,h,i,j).
  * Only selected heads / rows are written; dk / dv of every kv row of every
  * selected kv group are overwritten (they sum over the selected rows only).
@@ -333,13 +342,13 @@ int ora_grad(const ora_problem *p, const double *q, const double *k, const doubl
              const double *dy, const double *out, const double *smax, const double *ssum,
              double *dq, double *dk, double *dv, double *dsink, double *ds_dense)
 {
-    const int64_t D = p->D, G = p->Nq / p->Nkv;
+    const int64_t D = p->D, Dv = value_dim(p), G = p->Nq / p->Nkv;
     const int64_t nrows = p->cu_q[p->B] * p->Nq, nkvrows = p->cu_kv[p->B] * p->Nkv;
     double *Drow = (double *)calloc((size_t)(nrows > 0 ? nrows : 1), sizeof(double));
     if (!Drow) return 1;
     /* D_i = <dY_i, O_i> */
 #pragma omp parallel for schedule(static)
-    for (int64_t r = 0; r < nrows; ++r) Drow[r] = dot(dy + r * D, out + r * D, D);
+    for (int64_t r = 0; r < nrows; ++r) Drow[r] = dot(dy + r * Dv, out + r * Dv, Dv);
     /* dQ_i = scale * sum_j dS_ij K_j */
 #pragma omp parallel for schedule(dynamic, 16)
     for (int64_t r = 0; r < nrows; ++r) {
@@ -370,8 +379,9 @@ int ora_grad(const ora_problem *p, const double *q, const double *k, const doubl
         if (b >= p->B) continue;
         const int64_t j = t - p->cu_kv[b], tq = p->cu_q[b], sq = p->cu_q[b + 1] - tq;
         const int64_t base = ora_mask_base(p, b);
-        double *dkj = dk + kr * D, *dvj = dv + kr * D;
-        for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+        double *dkj = dk + kr * D, *dvj = dv + kr * Dv;
+        for (int64_t d = 0; d < D; ++d) dkj[d] = 0.0;
+        for (int64_t d = 0; d < Dv; ++d) dvj[d] = 0.0;
         for (int64_t h = g * G; h < (g + 1) * G; ++h) {
             if (h < p->h_lo || h >= p->h_hi) continue;
             for (int64_t i = 0; i < sq; ++i) {
@@ -379,11 +389,9 @@ int ora_grad(const ora_problem *p, const double *q, const double *k, const doubl
                 const int64_t r = (tq + i) * p->Nq + h;
                 double pz;
                 const double dS = grad_ds(p, q, k, v, dy, smax[r], ssum[r], Drow[r], b, base, h, i, j, &pz);
-                const double *qi = q + r * D, *dyi = dy + r * D;
-                for (int64_t d = 0; d < D; ++d) {
-                    dkj[d] += p->scale * dS * qi[d];
-                    dvj[d] += pz * dyi[d];
-                }
+                const double *qi = q + r * D, *dyi = dy + r * Dv;
+                for (int64_t d = 0; d < D; ++d) dkj[d] += p->scale * dS * qi[d];
+                for (int64_t d = 0; d < Dv; ++d) dvj[d] += pz * dyi[d];
             }
         }
     }

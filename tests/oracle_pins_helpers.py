@@ -57,7 +57,7 @@ def autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, *, mode=0, p
     V = torch.tensor(v, dtype=torch.float64, requires_grad=True)
     dY = torch.tensor(dy, dtype=torch.float64)
     S_ink = None if sink is None else torch.tensor(np.asarray(sink, np.float64), requires_grad=True)
-    out = torch.zeros_like(Q)
+    out = torch.zeros((Q.shape[0], nq, V.shape[2]), dtype=torch.float64)   # value head dim
     smax = torch.full((Q.shape[0], nq), float("nan"), dtype=torch.float64)
     ssum = torch.full((Q.shape[0], nq), float("nan"), dtype=torch.float64)
     pieces = []
@@ -111,15 +111,17 @@ def autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, *, mode=0, p
     return res
 
 
-def random_problem(seed, seqlens_q, seqlens_kv, nq, nkv, d):
+def random_problem(seed, seqlens_q, seqlens_kv, nq, nkv, d, dv=None):
+    """Random Q, K [.., d] and V, dY [.., dv] (dv = d by default)."""
     rng = np.random.default_rng(seed)
+    dv = d if dv is None else dv
     tq, tkv = sum(seqlens_q), sum(seqlens_kv)
     cu_q = np.concatenate([[0], np.cumsum(seqlens_q)]).astype(np.int64)
     cu_kv = np.concatenate([[0], np.cumsum(seqlens_kv)]).astype(np.int64)
     q = rng.standard_normal((tq, nq, d))
     k = rng.standard_normal((tkv, nkv, d))
-    v = rng.standard_normal((tkv, nkv, d))
-    dy = rng.standard_normal((tq, nq, d))
+    v = rng.standard_normal((tkv, nkv, dv))
+    dy = rng.standard_normal((tq, nq, dv))
     return rng, cu_q, cu_kv, q, k, v, dy
 
 

@@ -36,6 +36,8 @@ MUTANTS = {
     "prefix_top_left_anchor": ("case 6: return j <= i + (skv - sq)", "case 6: return j <= i"),
     "pse_rows_above_not_along_diagonal": ("        c = j - r;\n        r = 0;", "        r = 0;"),
     "pse_type_swapped": ("return p->pse_type == 1 ? p->scale * (qk + pse)", "return p->pse_type == 0 ? p->scale * (qk + pse)"),
+    "dp_drops_last_value_column": ("const double dP = dot(dy + r * Dv, vj, Dv);", "const double dP = dot(dy + r * Dv, vj, Dv - 1);"),
+    "drow_drops_last_value_column": ("Drow[r] = dot(dy + r * Dv, out + r * Dv, Dv);", "Drow[r] = dot(dy + r * Dv, out + r * Dv, Dv - 1);"),
 }
 
 
@@ -58,6 +60,8 @@ def _pin_suite(ora):
         for pse_type in (0, 1):
             pins.test_alibi_pse_matches_autograd_with_the_full_bias(ora, pse_type, [1300, 40])
             pins.test_random_pse_short_sequences_match_autograd(ora, pse_type)
+        for ci in range(len(pins.DV_CASES)):
+            pins.test_unequal_head_dims_match_autograd(ora, ci)
     except AssertionError:
         return False
     return True

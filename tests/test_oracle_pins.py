@@ -418,6 +418,76 @@ def test_forward_and_grad_match_autograd(ora, ci):
 
 
 # --------------------------------------------------------------------------
+# value head dim below the query/key head dim (qD == kD >= vD)
+# --------------------------------------------------------------------------
+
+DV_CASES = [
+    # seqlens_q, seqlens_kv, nq, nkv, d, dv, mode, pre, nxt, dropout, sink
+    ([5, 9], [5, 9], 2, 2, 8, 3, 3, INF, INF, False, False),
+    ([6, 3], [9, 3], 4, 2, 8, 5, 3, INF, INF, True, True),
+    ([8, 11], [8, 11], 2, 1, 6, 1, 4, 3, 1, True, False),
+    ([7, 0, 5], [7, 3, 5], 2, 2, 4, 2, 0, INF, INF, False, True),
+]
+
+
+def _dv_case(ora, ci):
+    sq, skv, nq, nkv, d, dv, mode, pre, nxt, drop, sink = DV_CASES[ci]
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(600 + ci, sq, skv, nq, nkv, d, dv)
+    scale = scale_for(d) * 1.3
+    bits, packed, kp = None, None, 1.0
+    if drop:
+        bits, packed = random_bits(rng, [(nq, a, b) for a, b in zip(sq, skv)], 0.8)
+        kp = 0.8
+    snk = rng.standard_normal(nq) if sink else None
+    kw = dict(keep_prob=kp, pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, drop_mask=packed, sink=snk)
+    return (cu_q, cu_kv, nq, nkv, d, dv, scale, kw), (q, k, v, dy), (bits, kp, snk, mode, pre, nxt)
+
+
+@pytest.mark.parametrize("ci", range(len(DV_CASES)))
+def test_unequal_head_dims_match_autograd(ora, ci):
+    """Value / dY / O / dV with Dv < D columns (aclnnFlashAttentionUnpaddingScoreGrad,
+    constraints: qD == kD >= vD) against autograd of the textbook forward."""
+    (cu_q, cu_kv, nq, nkv, d, dv, scale, kw), (q, k, v, dy), (bits, kp, snk, mode, pre, nxt) = _dv_case(ora, ci)
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, dv=dv, **kw)
+    ref = autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, mode=mode, pre=pre, nxt=nxt,
+                             bits=bits, keep_prob=kp, sink=snk)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    assert out.shape == (q.shape[0], nq, dv)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-12)
+    dq, dk, dvv, dsink = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    np.testing.assert_allclose(dq, ref["dq"], rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dk, ref["dk"], rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dvv, ref["dv"], rtol=1e-10, atol=1e-11)
+    if snk is not None:
+        np.testing.assert_allclose(dsink, ref["dsink"], rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("ci", range(len(DV_CASES)))
+def test_unequal_head_dims_equal_zero_padded_value(ora, ci):
+    """Appending D - Dv zero columns to V and dY gives the equal-dims problem:
+    its O and dV are those of the Dv problem followed by zeros, its dQ, dK, max,
+    sum and dSink are the same, bit for bit (the extra terms are exact zeros)."""
+    (cu_q, cu_kv, nq, nkv, d, dv, scale, kw), (q, k, v, dy), _ = _dv_case(ora, ci)
+    pad = lambda x: np.concatenate([x, np.zeros(x.shape[:2] + (d - dv,))], axis=2)
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, dv=dv, **kw)
+    pf = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, **kw)
+    small = ora.fwd_grad(p, q, k, v, dy)
+    full = ora.fwd_grad(pf, q, k, pad(v), pad(dy))
+    for n, a, b in zip(("out", "smax", "ssum", "dq", "dk", "dv", "dsink"), small, full):
+        if n in ("out", "dv"):
+            np.testing.assert_array_equal(b[..., dv:], 0.0, err_msg=n)
+            b = b[..., :dv]
+        np.testing.assert_array_equal(a, b, err_msg=n)
+
+
+def test_value_head_dim_bounds(ora):
+    with pytest.raises(ValueError):
+        _problem(ora, [0, 3], [0, 3], 1, 1, 8, 0.3, dv=9)
+    with pytest.raises(ValueError):
+        _problem(ora, [0, 3], [0, 3], 1, 1, 8, 0.3, dv=0)
+
+
+# --------------------------------------------------------------------------
 # finite differences of L = sum(dY * O) through the oracle's own forward
 # --------------------------------------------------------------------------
 
