@@ -49,15 +49,16 @@ def lib():
             raise RuntimeError(f"CUDA library {LIB_PATH} is missing; build it with "
                                "attention_backward_tnd_b300.build.build()")
         L = ctypes.CDLL(LIB_PATH)
-        ws_args = [_int, _i64, _i64p, _i64p, _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _int, _int,
-                   _int, ctypes.POINTER(ctypes.c_uint64)]
+        ws_args = [_int, _i64, _i64p, _i64p, _i64p, _i64, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _int,
+                   _int, _int, ctypes.POINTER(ctypes.c_uint64)]
         L.tnd_attn_fwd_workspace_size.argtypes = ws_args
         L.tnd_attn_grad_workspace_size.argtypes = ws_args
         L.tnd_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _int, _i64, _i64p, _i64p, _i64p,
-                                   _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64, _vp]
+                                   _i64, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _u64,
+                                   _vp]
         L.tnd_attn_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _i64,
-                                    _i64p, _i64p, _i64p, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp, _vp,
-                                    _vp, _vp, _vp, _u64, _vp]
+                                    _i64p, _i64p, _i64p, _i64, _i64, _i64, _i64, _f64, _f64, _i64, _i64, _i64, _vp,
+                                    _vp, _vp, _vp, _vp, _u64, _vp]
         L.tnd_attn_device_status.argtypes = [_vp, _u64, _vp]
         L.tnd_status_string.argtypes = [_int]
         L.tnd_status_string.restype = ctypes.c_char_p
@@ -103,47 +104,49 @@ def _pp(arr):
 
 # --- one-to-one wrappers of the C entry points --------------------------------------------
 
-def tnd_attn_fwd_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value,
-                                keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_atten_mask,
-                                has_sink):
+def tnd_attn_fwd_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, value_head_dim,
+                                scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask,
+                                has_atten_mask, has_sink):
     cq, ck, pf, out = _cu(cu_q), _cu(cu_kv), _pre(prefix), ctypes.c_uint64(0)
     st = lib().tnd_attn_fwd_workspace_size(dtype, batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, head_dim,
-                                           scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                           value_head_dim, scale_value, keep_prob, pre_tokens, next_tokens,
+                                           sparse_mode,
                                            int(has_drop_mask), int(has_atten_mask), int(has_sink),
                                            ctypes.byref(out))
     return st, out.value
 
 
-def tnd_attn_grad_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value,
-                                 keep_prob, pre_tokens, next_tokens, sparse_mode, has_drop_mask, has_atten_mask,
-                                 has_sink):
+def tnd_attn_grad_workspace_size(dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim,
+                                 value_head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                 has_drop_mask, has_atten_mask, has_sink):
     cq, ck, pf, out = _cu(cu_q), _cu(cu_kv), _pre(prefix), ctypes.c_uint64(0)
     st = lib().tnd_attn_grad_workspace_size(dtype, batch, _p(cq), _p(ck), _pp(pf), head_num, kv_head_num,
-                                            head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                            head_dim, value_head_dim, scale_value, keep_prob, pre_tokens,
+                                            next_tokens, sparse_mode,
                                             int(has_drop_mask), int(has_atten_mask), int(has_sink),
                                             ctypes.byref(out))
     return st, out.value
 
 
 def tnd_attn_fwd(query, key, value, pse, pse_batch, pse_type, drop_mask, atten_mask, sink, dtype, batch, cu_q,
-                 cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens,
-                 sparse_mode, attention_out, softmax_max, softmax_sum, workspace, workspace_size, stream):
+                 cu_kv, prefix, head_num, kv_head_num, head_dim, value_head_dim, scale_value, keep_prob, pre_tokens,
+                 next_tokens, sparse_mode, attention_out, softmax_max, softmax_sum, workspace, workspace_size, stream):
     cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
     return lib().tnd_attn_fwd(query, key, value, pse, pse_batch, pse_type, drop_mask, atten_mask, sink, dtype, batch,
-                              _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, head_dim, scale_value, keep_prob,
-                              pre_tokens, next_tokens, sparse_mode, attention_out, softmax_max, softmax_sum,
-                              workspace, workspace_size, stream)
+                              _p(cq), _p(ck), _pp(pf), head_num, kv_head_num, head_dim, value_head_dim, scale_value,
+                              keep_prob, pre_tokens, next_tokens, sparse_mode, attention_out, softmax_max,
+                              softmax_sum, workspace, workspace_size, stream)
 
 
 def tnd_attn_grad(query, key, value, dy, pse, pse_batch, pse_type, drop_mask, atten_mask, softmax_max, softmax_sum,
-                  attention_in, sink, dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim, scale_value,
-                  keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv, dsink, workspace, workspace_size,
-                  stream):
+                  attention_in, sink, dtype, batch, cu_q, cu_kv, prefix, head_num, kv_head_num, head_dim,
+                  value_head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode, dq, dk, dv, dsink,
+                  workspace, workspace_size, stream):
     cq, ck, pf = _cu(cu_q), _cu(cu_kv), _pre(prefix)
     return lib().tnd_attn_grad(query, key, value, dy, pse, pse_batch, pse_type, drop_mask, atten_mask, softmax_max,
                                softmax_sum, attention_in, sink, dtype, batch, _p(cq), _p(ck), _pp(pf), head_num,
-                               kv_head_num, head_dim, scale_value, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                               dq, dk, dv, dsink, workspace, workspace_size, stream)
+                               kv_head_num, head_dim, value_head_dim, scale_value, keep_prob, pre_tokens,
+                               next_tokens, sparse_mode, dq, dk, dv, dsink, workspace, workspace_size, stream)
 
 
 def tnd_attn_grad_static_ws(query, key, value, dy, drop_mask, softmax_max, softmax_sum, attention_in, sink, dtype,
@@ -251,24 +254,24 @@ def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_p
     pse: CUDA tensor [B or 1, Nq, 1024, S2Max] in q's dtype (the last 1024 rows of each sequence's bias)."""
     import torch
     tq, nq, d = q.shape
-    nkv = k.shape[1]
+    nkv, dv = k.shape[1], v.shape[2]
     batch = len(cu_q) - 1
     dt = dtype_code(q)
     _check_amask(atten_mask, cu_q, cu_kv)
-    st, ws_bytes = tnd_attn_fwd_workspace_size(dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob,
+    st, ws_bytes = tnd_attn_fwd_workspace_size(dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, dv, scale, keep_prob,
                                                pre_tokens, next_tokens, sparse_mode, drop_mask is not None,
                                                atten_mask is not None, sink is not None)
     if st != TND_OK:
         raise TndError(st, "tnd_attn_fwd_workspace_size")
-    out = torch.empty_like(q)
+    out = torch.empty((tq, nq, dv), dtype=q.dtype, device=q.device)
     smax = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
     ssum = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
     pb = _check_pse(pse, q, cu_kv, batch)
     st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(pse), pb, pse_type, _ptr(drop_mask),
-                      _ptr(atten_mask), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob,
-                      pre_tokens, next_tokens, sparse_mode, out.data_ptr(), smax.data_ptr(), ssum.data_ptr(),
+                      _ptr(atten_mask), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, dv, scale,
+                      keep_prob, pre_tokens, next_tokens, sparse_mode, out.data_ptr(), smax.data_ptr(), ssum.data_ptr(),
                       workspace.data_ptr(), workspace.numel(), _stream())
     if st != TND_OK:
         raise TndError(st, "tnd_attn_fwd")
@@ -277,9 +280,11 @@ def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_p
 
 def grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob=1.0, pre_tokens=2147483647,
                          next_tokens=2147483647, sparse_mode=0, has_drop=False, has_sink=False,
-                         has_atten_mask=False, prefix=None) -> int:
+                         has_atten_mask=False, prefix=None, v=None) -> int:
+    """Workspace bytes of the gradient (v gives the value head dim; default q's)."""
+    dv = q.shape[2] if v is None else v.shape[2]
     st, n = tnd_attn_grad_workspace_size(dtype_code(q), len(cu_q) - 1, cu_q, cu_kv, prefix, q.shape[1], k.shape[1],
-                                         q.shape[2], scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
+                                         q.shape[2], dv, scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
                                          has_drop, has_atten_mask, has_sink)
     if st != TND_OK:
         raise TndError(st, "tnd_attn_grad_workspace_size")
@@ -292,13 +297,13 @@ def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_pr
     """Gradient on torch CUDA tensors: returns (dq, dk, dv, dsink or None)."""
     import torch
     tq, nq, d = q.shape
-    nkv = k.shape[1]
+    nkv, dvd = k.shape[1], v.shape[2]
     batch = len(cu_q) - 1
     dt = dtype_code(q)
     _check_amask(atten_mask, cu_q, cu_kv)
     if workspace is None:
         n = grad_workspace_bytes(q, k, cu_q, cu_kv, scale, keep_prob, pre_tokens, next_tokens, sparse_mode,
-                                 drop_mask is not None, sink is not None, atten_mask is not None, prefix)
+                                 drop_mask is not None, sink is not None, atten_mask is not None, prefix, v)
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     if outputs is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -308,8 +313,8 @@ def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_pr
     pb = _check_pse(pse, q, cu_kv, batch)
     st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(pse), pb, pse_type,
                        _ptr(drop_mask), _ptr(atten_mask), softmax_max.data_ptr(), softmax_sum.data_ptr(),
-                       out.data_ptr(), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, scale, keep_prob,
-                       pre_tokens, next_tokens, sparse_mode, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       out.data_ptr(), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, dvd, scale,
+                       keep_prob, pre_tokens, next_tokens, sparse_mode, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                        _ptr(dsink), workspace.data_ptr(), workspace.numel(), _stream())
     if st != TND_OK:
         raise TndError(st, "tnd_attn_grad")

@@ -1,8 +1,10 @@
 // CUDA-core kernels of the TND attention library: the forward, the gradient
 // prepass (rowsum(dY o O), log2-sum-exp, sink terms), a dK/dV kernel, a dQ
-// kernel and the dSink reduction.  They serve every dtype (fp32 included)
-// and every head dim up to 256; the tensor-core gradient replaces the dK/dV
-// and dQ kernels for bf16/fp16 at D = 64 and 128.
+// kernel and the dSink reduction.  They serve every dtype (fp32 included),
+// every head dim up to 768 and a value head dim below the query / key one
+// ("aclnnFlashAttentionUnpaddingScoreGrad", constraints: qD == kD >= vD; Q, K,
+// dQ, dK have D columns, V, dY, O, dV have Dv); the tensor-core gradient
+// replaces the dK/dV and dQ kernels for bf16/fp16 at D = Dv = 64 and 128.
 //
 // Formulas: "aclnnFlashAttentionUnpaddingScoreGrad", function description
 // (forward Y = Dropout(Softmax(Mask(scale Q K^T)), keep_prob) V; backward
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
     float *Ks = smem, *Vs = smem + R * DMAX;
     const int2 it = a.q_items[blockIdx.x];
     const SeqDesc sd = a.seqs[it.x];
-    const int h = blockIdx.y, g = h / a.group, D = a.d;
+    const int h = blockIdx.y, g = h / a.group, D = a.d, Dv = a.vd;
     const int r = threadIdx.x >> 2, c4 = threadIdx.x & 3;
     const int64_t i = (int64_t)it.y + r;
     const bool row_ok = i < sd.sq;
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
     for (int64_t kt = (ulo <= uhi) ? (ulo / R) * R : 1; kt <= uhi; kt += R) {
         __syncthreads();
         load_tile<T, DMAX>(Ks, K, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
-        load_tile<T, DMAX>(Vs, V, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
+        load_tile<T, DMAX>(Vs, V, sd.tk, kt, sd.skv, a.nkv, g, Dv, 1.0f);
         __syncthreads();
         for (int c = 0; c < R; ++c) {
             const int64_t j = kt + c;
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a)
 #pragma unroll
     for (int k = 0; k < DP; ++k) {
         const int col = c4 + 4 * k;
-        if (col < D) Elem<T>::store(O + ((sd.tq + i) * a.nq + h) * (int64_t)D + col, acc[k] * inv);
+        if (col < Dv) Elem<T>::store(O + ((sd.tq + i) * a.nq + h) * (int64_t)Dv + col, acc[k] * inv);
     }
     const float mnat = (m == -INFINITY) ? -INFINITY : m * kLn2;
     const int64_t rbase = ((sd.tq + i) * a.nq + h) * 8;
@@ -192,8 +194,9 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
     const int2 qr = a.qblk_rows[qg];
     const SeqDesc sd = a.seqs[qr.x];
     const T *dY = (const T *)a.dy, *O = (const T *)a.o;
-    const bool vec = ((a.d * (int)sizeof(T)) & 15) == 0 && a.d * (int)sizeof(T) <= 256;
-    const int chunks = a.d * (int)sizeof(T) / 16;          // 16-byte chunks per row (at most 16)
+    const int Dv = a.vd;                                    // dY and O rows
+    const bool vec = ((Dv * (int)sizeof(T)) & 15) == 0 && Dv * (int)sizeof(T) <= 256;
+    const int chunks = Dv * (int)sizeof(T) / 16;            // 16-byte chunks per row (at most 16)
     // the forward's max and sum of the group's rows, requested with dY and O
     // (one lane per row reads them)
     float mv[4], lv[4];
@@ -216,8 +219,8 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
             for (int e = 0; e < 2; ++e) {
                 const int c = sub + 8 * e;
                 const bool ld = i < sd.sq && c < chunks;
-                y[k][e] = ld ? __ldg(reinterpret_cast<const uint4 *>(dY + r * a.d) + c) : make_uint4(0, 0, 0, 0);
-                o[k][e] = ld ? __ldg(reinterpret_cast<const uint4 *>(O + r * a.d) + c) : make_uint4(0, 0, 0, 0);
+                y[k][e] = ld ? __ldg(reinterpret_cast<const uint4 *>(dY + r * Dv) + c) : make_uint4(0, 0, 0, 0);
+                o[k][e] = ld ? __ldg(reinterpret_cast<const uint4 *>(O + r * Dv) + c) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(256) prepass_kernel(GradArgs a, int tc_state)
             const int64_t r = (sd.tq + i) * a.nq + h;
             dot[k] = 0.0f;
             if (i < sd.sq)
-                for (int c = sub; c < a.d; c += 8) dot[k] += Elem<T>::load(dY + r * a.d + c) * Elem<T>::load(O + r * a.d + c);
+                for (int c = sub; c < Dv; c += 8) dot[k] += Elem<T>::load(dY + r * Dv + c) * Elem<T>::load(O + r * Dv + c);
         }
     }
 #pragma unroll
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
     float *lses = dYs + R * DMAX, *Ds = lses + R;
     const int2 it = a.kv_items[blockIdx.x];
     const SeqDesc sd = a.seqs[it.x];
-    const int g = blockIdx.y, D = a.d;
+    const int g = blockIdx.y, D = a.d, Dv = a.vd;
     const int r = threadIdx.x >> 2, c4 = threadIdx.x & 3;
     const int64_t j = (int64_t)it.y + r;
     const bool row_ok = j < sd.skv;
@@ -281,10 +284,9 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
 #pragma unroll
     for (int k = 0; k < DP; ++k) {
         const int col = c4 + 4 * k;
-        const bool ok = row_ok && col < D;
-        const int64_t off = ((sd.tk + j) * a.nkv + g) * (int64_t)D + col;
-        kreg[k] = ok ? Elem<T>::load(K + off) * C : 0.0f;
-        vreg[k] = ok ? Elem<T>::load(V + off) : 0.0f;
+        const int64_t row = (sd.tk + j) * a.nkv + g;
+        kreg[k] = (row_ok && col < D) ? Elem<T>::load(K + row * D + col) * C : 0.0f;
+        vreg[k] = (row_ok && col < Dv) ? Elem<T>::load(V + row * Dv + col) : 0.0f;
         adk[k] = 0.0f;
         adv[k] = 0.0f;
     }
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
             const bool hit = (lo <= hi) && (hi >= j0) && (lo <= j1);
             if (!__syncthreads_or(hit)) continue;
             load_tile<T, DMAX>(Qs, Q, sd.tq, qt, sd.sq, a.nq, h, D, 1.0f);
-            load_tile<T, DMAX>(dYs, dY, sd.tq, qt, sd.sq, a.nq, h, D, 1.0f);
+            load_tile<T, DMAX>(dYs, dY, sd.tq, qt, sd.sq, a.nq, h, Dv, 1.0f);
             if (threadIdx.x < R) {
                 const int64_t i = qt + threadIdx.x;
                 const bool ok = i < sd.sq;
@@ -340,11 +342,9 @@ __global__ void __launch_bounds__(kThreads) grad_dkdv_simt_kernel(GradArgs a)
 #pragma unroll
     for (int k = 0; k < DP; ++k) {
         const int col = c4 + 4 * k;
-        if (col < D) {
-            const int64_t off = ((sd.tk + j) * a.nkv + g) * (int64_t)D + col;
-            Elem<T>::store(dK + off, adk[k] * a.scale);
-            Elem<T>::store(dV + off, adv[k]);
-        }
+        const int64_t row = (sd.tk + j) * a.nkv + g;
+        if (col < D) Elem<T>::store(dK + row * D + col, adk[k] * a.scale);
+        if (col < Dv) Elem<T>::store(dV + row * Dv + col, adv[k]);
     }
 }
 
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
     float *Ks = smem, *Vs = smem + R * DMAX;
     const int2 it = a.q_items[blockIdx.x];
     const SeqDesc sd = a.seqs[it.x];
-    const int h = blockIdx.y, g = h / a.group, D = a.d;
+    const int h = blockIdx.y, g = h / a.group, D = a.d, Dv = a.vd;
     const int r = threadIdx.x >> 2, c4 = threadIdx.x & 3;
     const int64_t i = (int64_t)it.y + r;
     const bool row_ok = i < sd.sq;
@@ -370,10 +370,9 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
 #pragma unroll
     for (int k = 0; k < DP; ++k) {
         const int col = c4 + 4 * k;
-        const bool ok = row_ok && col < D;
-        const int64_t off = ((sd.tq + i) * a.nq + h) * (int64_t)D + col;
-        qreg[k] = ok ? Elem<T>::load(Q + off) * C : 0.0f;
-        dyreg[k] = ok ? Elem<T>::load(dY + off) : 0.0f;
+        const int64_t row = (sd.tq + i) * a.nq + h;
+        qreg[k] = (row_ok && col < D) ? Elem<T>::load(Q + row * D + col) * C : 0.0f;
+        dyreg[k] = (row_ok && col < Dv) ? Elem<T>::load(dY + row * Dv + col) : 0.0f;
         acc[k] = 0.0f;
     }
     const float lse = row_ok ? a.lse2[row_vec_index(sd, a.nq, h, i)] : INFINITY;
@@ -386,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) grad_dq_simt_kernel(GradArgs a)
     for (int64_t kt = (ulo <= uhi) ? (ulo / R) * R : 1; kt <= uhi; kt += R) {
         __syncthreads();
         load_tile<T, DMAX>(Ks, K, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
-        load_tile<T, DMAX>(Vs, V, sd.tk, kt, sd.skv, a.nkv, g, D, 1.0f);
+        load_tile<T, DMAX>(Vs, V, sd.tk, kt, sd.skv, a.nkv, g, Dv, 1.0f);
         __syncthreads();
         for (int c = 0; c < R; ++c) {
             const int64_t j = kt + c;

@@ -82,6 +82,7 @@ struct Problem {
     int64_t batch = 0;
     const int64_t *cuq = nullptr, *cukv = nullptr;
     int64_t nq = 0, nkv = 0, d = 0;
+    int64_t dv = 0;                    // value / dy / output head dim (qD == kD >= vD)
     double scale = 0, keep = 1;
     int64_t pre = 0, next = 0, mode = 0;
     bool has_drop = false, has_sink = false;
@@ -106,8 +107,8 @@ constexpr int64_t kSimtMaxHeadDim = 768;          // the CUDA-core kernels (inst
 // passed with them is not read); mode 6 reads prefix; 5, 7 and 8 are not
 // implemented.
 tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv, const int64_t *prefix,
-                    int64_t nq, int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next,
-                    int64_t mode, bool has_drop, bool has_amask, bool has_sink, Problem &p)
+                    int64_t nq, int64_t nkv, int64_t d, int64_t vd, double scale, double keep, int64_t pre,
+                    int64_t next, int64_t mode, bool has_drop, bool has_amask, bool has_sink, Problem &p)
 {
     if (!cuq || !cukv) return TND_ERR_NULLPTR;
     if (keep < 1.0 && !has_drop) return TND_ERR_NULLPTR;  // dropMask needed when keepProb < 1
@@ -124,6 +125,7 @@ tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t 
     if (p.tq < 1 || p.tq > kMaxTokens || p.tkv < 1 || p.tkv > kMaxTokens) return TND_ERR_INVALID;
     if (nq < 1 || nq > kMaxHeads || nkv < 1 || nkv > kMaxHeads || nq % nkv != 0) return TND_ERR_INVALID;
     if (d < 1 || d > kMaxHeadDim) return TND_ERR_INVALID;
+    if (vd < 1 || vd > d) return TND_ERR_INVALID;         // qD == kD >= vD
     if (!(keep > 0.0 && keep <= 1.0)) return TND_ERR_INVALID;
     if (!std::isfinite(scale)) return TND_ERR_INVALID;
     if (mode < 0 || mode > 8) return TND_ERR_INVALID;
@@ -151,6 +153,7 @@ tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t 
     p.nq = nq;
     p.nkv = nkv;
     p.d = d;
+    p.dv = vd;
     p.scale = scale;
     p.keep = keep;
     p.pre = pre;
@@ -513,8 +516,11 @@ DeviceInfo device_info()
     return di;
 }
 
-bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && grad_tc_supported(p.dtype, (int)p.d); }
-bool use_fwd_tc(const Problem &p) { return g_opt.grad_path == 0 && fwd_tc_supported(p.dtype, (int)p.d); }
+// The tensor-core kernels take equal head dims only.
+bool tc_grad_layout(const Problem &p) { return grad_tc_supported(p.dtype, (int)p.d) && p.dv == p.d; }
+bool tc_fwd_layout(const Problem &p) { return fwd_tc_supported(p.dtype, (int)p.d) && p.dv == p.d; }
+bool use_tc(const Problem &p) { return g_opt.grad_path == 0 && tc_grad_layout(p); }
+bool use_fwd_tc(const Problem &p) { return g_opt.grad_path == 0 && tc_fwd_layout(p); }
 
 // Pinned host staging of plan uploads.  A copy from pageable host memory may
 // make the runtime wait for the stream before it starts, so a run call would
@@ -591,6 +597,7 @@ void fill_common(A &a, const Problem &p, const Plan &pl, const Layout &L, void *
     a.nq = (int32_t)p.nq;
     a.nkv = (int32_t)p.nkv;
     a.d = (int32_t)p.d;
+    a.vd = (int32_t)p.dv;
     a.group = (int32_t)(p.nq / p.nkv);
     a.tq = p.tq;
     a.tkv = p.tkv;
@@ -715,16 +722,16 @@ tnd_status tnd_attn_profile_read(const char **names, double *total_ms, int64_t *
 }
 
 tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                                       const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale,
-                                       double keep, int64_t pre, int64_t next, int64_t mode, int has_drop,
-                                       int has_amask, int has_sink, uint64_t *ws_size)
+                                       const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, int64_t vd,
+                                       double scale, double keep, int64_t pre, int64_t next, int64_t mode,
+                                       int has_drop, int has_amask, int has_sink, uint64_t *ws_size)
 {
     if (!ws_size) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, vd, scale, keep, pre, next, mode,
                              has_drop != 0, has_amask != 0, has_sink != 0, p);
     if (st != TND_OK) return st;
-    const bool tc_layout = fwd_tc_supported(p.dtype, (int)p.d);
+    const bool tc_layout = tc_fwd_layout(p);
     auto plp = get_plan(p, tc_layout);
     *ws_size = layout_for(p, *plp, false, tc_layout).total;
     return TND_OK;
@@ -733,20 +740,20 @@ tnd_status tnd_attn_fwd_workspace_size(tnd_dtype dtype, int64_t batch, const int
 tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const void *pse, int64_t pse_batch,
                         int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *sink,
                         tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                        const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale, double keep,
-                        int64_t pre, int64_t next, int64_t mode, void *out, float *smax, float *ssum, void *ws,
-                        uint64_t ws_size, void *stream)
+                        const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, int64_t vd, double scale,
+                        double keep, int64_t pre, int64_t next, int64_t mode, void *out, float *smax, float *ssum,
+                        void *ws, uint64_t ws_size, void *stream)
 {
     if (!q || !k || !v || !out || !smax || !ssum) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, vd, scale, keep, pre, next, mode,
                              drop_mask != nullptr, atten_mask != nullptr, sink != nullptr, p);
     if (st != TND_OK) return st;
     st = check_pse(p, pse, pse_batch, pse_type);
     if (st != TND_OK) return st;
     for (const void *ptr : {q, k, v, (const void *)out, (const void *)smax, (const void *)ssum})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
-    const bool tc_layout = fwd_tc_supported(p.dtype, (int)p.d);
+    const bool tc_layout = tc_fwd_layout(p);
     auto plp = get_plan(p, tc_layout);
     const Plan &pl = *plp;
     const Layout L = layout_for(p, pl, false, tc_layout);
@@ -799,16 +806,16 @@ tnd_status tnd_attn_fwd(const void *q, const void *k, const void *v, const void 
 }
 
 tnd_status tnd_attn_grad_workspace_size(tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                                        const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, double scale,
-                                        double keep, int64_t pre, int64_t next, int64_t mode, int has_drop,
-                                        int has_amask, int has_sink, uint64_t *ws_size)
+                                        const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, int64_t vd,
+                                        double scale, double keep, int64_t pre, int64_t next, int64_t mode,
+                                        int has_drop, int has_amask, int has_sink, uint64_t *ws_size)
 {
     if (!ws_size) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, vd, scale, keep, pre, next, mode,
                              has_drop != 0, has_amask != 0, has_sink != 0, p);
     if (st != TND_OK) return st;
-    const bool tc = grad_tc_supported(p.dtype, (int)p.d);
+    const bool tc = tc_grad_layout(p);
     auto plp = get_plan(p, tc);
     *ws_size = layout_for(p, *plp, true, tc).total;
     return TND_OK;
@@ -822,15 +829,16 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
                     int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *smax,
                     const float *ssum, const void *o, const float *sink, tnd_dtype dtype, int64_t batch,
                     const int64_t *cuq, const int64_t *cukv, const int64_t *prefix, int64_t nq, int64_t nkv,
-                    int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq,
-                    void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload)
+                    int64_t d, int64_t vd, double scale, double keep, int64_t pre, int64_t next, int64_t mode,
+                    void *dq, void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream,
+                    bool pinned_upload)
 {
     if (!q || !k || !v || !dy || !smax || !ssum || !o || !dq || !dk || !dv) return TND_ERR_NULLPTR;
     if (sink && !dsink) return TND_ERR_NULLPTR;
     HostClock hc;
     (void)hc;
     Problem p;
-    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode,
+    tnd_status st = validate(dtype, batch, cuq, cukv, prefix, nq, nkv, d, vd, scale, keep, pre, next, mode,
                              drop_mask != nullptr, atten_mask != nullptr, sink != nullptr, p);
     if (st != TND_OK) return st;
     st = check_pse(p, pse, pse_batch, pse_type);
@@ -839,7 +847,7 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
                             (const void *)dk, (const void *)dv})
         if (!aligned16(ptr)) return TND_ERR_INVALID;
     HOST_LAP(0);
-    const bool tc_layout = grad_tc_supported(p.dtype, (int)p.d);
+    const bool tc_layout = tc_grad_layout(p);
     const bool tc = use_tc(p);
     auto plp = get_plan(p, tc_layout);
     const Plan &pl = *plp;
@@ -926,11 +934,12 @@ tnd_status tnd_attn_grad(const void *q, const void *k, const void *v, const void
                          int64_t pse_batch, int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask,
                          const float *smax, const float *ssum, const void *o, const float *sink, tnd_dtype dtype,
                          int64_t batch, const int64_t *cuq, const int64_t *cukv, const int64_t *prefix, int64_t nq,
-                         int64_t nkv, int64_t d, double scale, double keep, int64_t pre, int64_t next, int64_t mode,
-                         void *dq, void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size, void *stream)
+                         int64_t nkv, int64_t d, int64_t vd, double scale, double keep, int64_t pre, int64_t next,
+                         int64_t mode, void *dq, void *dk, void *dv, float *dsink, void *ws, uint64_t ws_size,
+                         void *stream)
 {
     return grad_run(q, k, v, dy, pse, pse_batch, pse_type, drop_mask, atten_mask, smax, ssum, o, sink, dtype, batch,
-                    cuq, cukv, prefix, nq, nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, ws_size,
+                    cuq, cukv, prefix, nq, nkv, d, vd, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, ws_size,
                     stream, true);
 }
 
@@ -953,7 +962,7 @@ tnd_status tnd_attn_grad_plan(int64_t batch, const int64_t *cuq, const int64_t *
 {
     if (!n_units || !kept_pairs) return TND_ERR_NULLPTR;
     Problem p;
-    tnd_status st = validate(TND_BF16, batch, cuq, cukv, prefix, nq, nkv, 128, 1.0, 1.0, pre, next, mode, false,
+    tnd_status st = validate(TND_BF16, batch, cuq, cukv, prefix, nq, nkv, 128, 128, 1.0, 1.0, pre, next, mode, false,
                              has_amask != 0, false, p);
     if (st != TND_OK) return st;
     Plan pl;

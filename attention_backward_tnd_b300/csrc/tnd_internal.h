@@ -145,6 +145,7 @@ struct GradArgs {
     float *dsink;
     int dtype;
     int32_t batch, nq, nkv, d, group;
+    int32_t vd;               // head dim of value, dy, the output and dV (<= d)
     int64_t tq, tkv;
     float scale, keep_prob, inv_keep;
     MaskSpec mask;
@@ -182,6 +183,7 @@ struct FwdArgs {
     float *smax, *ssum;
     int dtype;
     int32_t batch, nq, nkv, d, group;
+    int32_t vd;               // head dim of value, dy, the output and dV (<= d)
     int64_t tq, tkv;
     float scale, keep_prob, inv_keep;
     MaskSpec mask;
@@ -251,7 +253,7 @@ tnd_status grad_run(const void *q, const void *k, const void *v, const void *dy,
                     int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *smax,
                     const float *ssum, const void *o,
                     const float *sink, tnd_dtype dtype, int64_t batch, const int64_t *cuq, const int64_t *cukv,
-                    const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d,
+                    const int64_t *prefix, int64_t nq, int64_t nkv, int64_t d, int64_t vd,
                     double scale, double keep, int64_t pre, int64_t next, int64_t mode, void *dq, void *dk, void *dv,
                     float *dsink, void *ws, uint64_t ws_size, void *stream, bool pinned_upload);
 

@@ -84,15 +84,15 @@ tnd_status tnd_attn_grad_static_ws(const void *q, const void *k, const void *v, 
                                    float *dsink, void *stream)
 {
     uint64_t need = 0;
-    tnd_status st = tnd_attn_grad_workspace_size(dtype, batch, cuq, cukv, nullptr, nq, nkv, d, scale, keep, pre, next,
-                                                 mode, drop_mask != nullptr, 0, sink != nullptr, &need);
+    tnd_status st = tnd_attn_grad_workspace_size(dtype, batch, cuq, cukv, nullptr, nq, nkv, d, d, scale, keep, pre,
+                                                 next, mode, drop_mask != nullptr, 0, sink != nullptr, &need);
     if (st != TND_OK) return st;
     if (need > tnd::kStaticWsBytes) return TND_ERR_WORKSPACE;
     void *ws = tnd::static_ws_address();
     if (!ws) return TND_ERR_CUDA;
     return tnd::grad_run(q, k, v, dy, nullptr, 0, 1, drop_mask, nullptr, smax, ssum, o, sink, dtype, batch, cuq, cukv,
-                         nullptr, nq, nkv, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws, tnd::kStaticWsBytes,
-                         stream, false);
+                         nullptr, nq, nkv, d, d, scale, keep, pre, next, mode, dq, dk, dv, dsink, ws,
+                         tnd::kStaticWsBytes, stream, false);
 }
 
 tnd_status tnd_attn_grad_static_ws_status(void *stream)

@@ -15,8 +15,13 @@
  * --------------------------------
  * Layout "TND" ([UnpadGrad] parameters section, inputLayout): rows of all
  * sequences packed back to back.
- *   query, dy, attention_out / attention_in, dq : [Tq,  Nq,  D] row-major
- *   key, value, dk, dv                          : [Tkv, Nkv, D] row-major
+ *   query, dq                      : [Tq,  Nq,  D]  row-major
+ *   key, dk                        : [Tkv, Nkv, D]  row-major
+ *   dy, attention_out / attention_in : [Tq,  Nq,  Dv] row-major
+ *   value, dv                      : [Tkv, Nkv, Dv] row-major
+ *   D = head_dim, Dv = value_head_dim ([UnpadGrad] constraints: qD == kD >=
+ *   vD, so 1 <= Dv <= D; scale_value is used as given).  The tensor-core
+ *   kernels take Dv == D; other calls run on the CUDA-core kernels.
  *   softmax_max, softmax_sum                    : fp32 [Tq, Nq, 8]; the 8
  *       values of a row are equal copies (the pages fix the [T,N,8] shape
  *       without saying what the 8 lanes hold).  The forward writes all 8,
@@ -89,7 +94,8 @@
  * no device memory.  Argument errors are reported before any device work is
  * enqueued and leave every output untouched.  Outputs are fully overwritten
  * on success, zero where nothing contributes.  Results are bitwise
- * deterministic run to run.  Calls on one workspace must not overlap in time.
+ * deterministic run to run unless TND_OPT_DETERMINISTIC is switched off.
+ * Calls on one workspace must not overlap in time.
  */
 #ifndef TND_ATTN_H
 #define TND_ATTN_H
@@ -119,6 +125,7 @@ typedef enum tnd_dtype { TND_F16 = 0, TND_BF16 = 1, TND_F32 = 2 } tnd_dtype;
  * Forward workspace size ([UnpadGrad]/[ScoreV2] function prototype: first
  * phase).  Checks all shape / scalar arguments ([UnpadGrad] and
  * [UnpadGradV5] constraints: T in [1, 1M], N in [1, 256], D in [1, 768],
+ * Dv in [1, D],
  * B in [1, 20000], keep_prob in (0, 1], headNum == Nq, Nq % Nkv == 0) and
  * the sparse_mode rules above.  has_drop_mask / has_atten_mask / has_sink
  * say whether the run call will pass those inputs; prefix is the host
@@ -127,13 +134,13 @@ typedef enum tnd_dtype { TND_F16 = 0, TND_BF16 = 1, TND_F32 = 2 } tnd_dtype;
 tnd_status tnd_attn_fwd_workspace_size(
     tnd_dtype dtype, int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
     const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
-    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
-    int64_t sparse_mode, int has_drop_mask, int has_atten_mask, int has_sink,
+    int64_t value_head_dim, double scale_value, double keep_prob, int64_t pre_tokens,
+    int64_t next_tokens, int64_t sparse_mode, int has_drop_mask, int has_atten_mask, int has_sink,
     uint64_t *workspace_size);
 
 /*
  * Forward ([ScoreV2] function description and parameters): writes
- * attention_out [Tq,Nq,D] (dtype), softmax_max and softmax_sum [Tq,Nq,8]
+ * attention_out [Tq,Nq,Dv] (dtype), softmax_max and softmax_sum [Tq,Nq,8]
  * (fp32).  pse, drop_mask, atten_mask, sink and prefix may be NULL where the
  * conventions above allow it; the pse checks are made here (the workspace
  * size does not depend on it).
@@ -143,18 +150,18 @@ tnd_status tnd_attn_fwd(
     int64_t pse_type, const uint8_t *drop_mask, const uint8_t *atten_mask, const float *sink,
     tnd_dtype dtype, int64_t batch,
     const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv, const int64_t *prefix,
-    int64_t head_num, int64_t kv_head_num, int64_t head_dim, double scale_value,
-    double keep_prob, int64_t pre_tokens, int64_t next_tokens, int64_t sparse_mode,
-    void *attention_out, float *softmax_max, float *softmax_sum, void *workspace,
-    uint64_t workspace_size, void *stream);
+    int64_t head_num, int64_t kv_head_num, int64_t head_dim, int64_t value_head_dim,
+    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
+    int64_t sparse_mode, void *attention_out, float *softmax_max, float *softmax_sum,
+    void *workspace, uint64_t workspace_size, void *stream);
 
 /* Gradient workspace size (first phase of [UnpadGrad]); same arguments and
  * checks as the forward's. */
 tnd_status tnd_attn_grad_workspace_size(
     tnd_dtype dtype, int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
     const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
-    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
-    int64_t sparse_mode, int has_drop_mask, int has_atten_mask, int has_sink,
+    int64_t value_head_dim, double scale_value, double keep_prob, int64_t pre_tokens,
+    int64_t next_tokens, int64_t sparse_mode, int has_drop_mask, int has_atten_mask, int has_sink,
     uint64_t *workspace_size);
 
 /*
@@ -163,7 +170,7 @@ tnd_status tnd_attn_grad_workspace_size(
  * Inputs: query, key, value, dy; softmax_max, softmax_sum and attention_in
  * as written by tnd_attn_fwd; drop_mask (NULL when keep_prob == 1);
  * pse, atten_mask and prefix as for the forward (the same ones it was given);
- * sink (NULL = no sink).  Outputs: dq [Tq,Nq,D], dk and dv [Tkv,Nkv,D]
+ * sink (NULL = no sink).  Outputs: dq [Tq,Nq,D], dk [Tkv,Nkv,D], dv [Tkv,Nkv,Dv]
  * (dtype; dk and dv are summed over the Nq/Nkv query heads of each kv
  * head), dsink [Nq] fp32 (required when sink is given, ignored otherwise).
  */
@@ -174,9 +181,9 @@ tnd_status tnd_attn_grad(
     const float *softmax_sum, const void *attention_in, const float *sink, tnd_dtype dtype,
     int64_t batch, const int64_t *cu_seqlens_q, const int64_t *cu_seqlens_kv,
     const int64_t *prefix, int64_t head_num, int64_t kv_head_num, int64_t head_dim,
-    double scale_value, double keep_prob, int64_t pre_tokens, int64_t next_tokens,
-    int64_t sparse_mode, void *dq, void *dk, void *dv, float *dsink, void *workspace,
-    uint64_t workspace_size, void *stream);
+    int64_t value_head_dim, double scale_value, double keep_prob, int64_t pre_tokens,
+    int64_t next_tokens, int64_t sparse_mode, void *dq, void *dk, void *dv, float *dsink,
+    void *workspace, uint64_t workspace_size, void *stream);
 
 /*
  * Waits for `stream`, then reports the device-side status of the last
@@ -258,8 +265,8 @@ tnd_status tnd_attn_grad_plan(
  * that only receives buffers from its host framework's allocator, or a
  * process that reserved all device memory at start-up.  Arguments and
  * results are those of tnd_attn_grad without `workspace` / `workspace_size`,
- * `pse`, `atten_mask` and `prefix` (so sparse_mode 1 and 6 return
- * TND_ERR_NULLPTR);
+ * `pse`, `atten_mask`, `prefix` and `value_head_dim` (value and dy have
+ * head_dim columns; sparse_mode 1 and 6 return TND_ERR_NULLPTR);
  * the caller still passes every input and output.
  *
  * The workspace is a fixed device array inside this library of

@@ -44,7 +44,7 @@ def run_library(inp: workloads.Inputs, dev=None, grad_path: int = 0, determinist
         ws_bytes = tnd.grad_workspace_bytes(dev["q"], dev["k"], wl.cu_q, wl.cu_kv, wl.scale, wl.keep_prob,
                                             wl.pre_tokens, wl.next_tokens, wl.sparse_mode,
                                             dev["mask"] is not None, dev["sink"] is not None,
-                                            amask is not None, wl.prefix)
+                                            amask is not None, wl.prefix, v=dev["v"])
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
         dq, dk, dv, dsink = tnd.grad(dev["q"], dev["k"], dev["v"], dev["dy"], out, smax, ssum, wl.cu_q,
                                      wl.cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens, wl.next_tokens,
@@ -177,7 +177,7 @@ def plain_fp32_eval(inp: workloads.Inputs) -> dict:
     import torch
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).float()  # noqa: E731
     q, k, v, dy = t(inp.q64), t(inp.k64), t(inp.v64), t(inp.dy64)
-    out = torch.zeros_like(q)
+    out = torch.zeros_like(dy)   # value head dim
     dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
     dsink = torch.zeros(wl.nq)
     p = oracle_problem(inp)
@@ -307,7 +307,7 @@ def compare_all(inp: workloads.Inputs, got: dict, ref: dict, q_rows=None, kv_row
     bnd = fp32_error_bound(inp, ref) if wl.dtype == "f32" else {}
     res = {}
     out = host64(got["out"])
-    res["out"] = assert_close(out, ref["out"], wl.dtype, "attention_out", qsel[..., None].repeat(wl.d, -1),
+    res["out"] = assert_close(out, ref["out"], wl.dtype, "attention_out", qsel[..., None].repeat(wl.dv, -1),
                               bnd.get("out"))
     smax = got["smax"].cpu().numpy().astype(np.float64)
     ssum = got["ssum"].cpu().numpy().astype(np.float64)
@@ -320,7 +320,7 @@ def compare_all(inp: workloads.Inputs, got: dict, ref: dict, q_rows=None, kv_row
                              bnd.get("dq"))
     res["dk"] = assert_close(host64(got["dk"]), ref["dk"], wl.dtype, "dk", ksel[..., None].repeat(wl.d, -1),
                              bnd.get("dk"))
-    res["dv"] = assert_close(host64(got["dv"]), ref["dv"], wl.dtype, "dv", ksel[..., None].repeat(wl.d, -1),
+    res["dv"] = assert_close(host64(got["dv"]), ref["dv"], wl.dtype, "dv", ksel[..., None].repeat(wl.dv, -1),
                              bnd.get("dv"))
     if got["dsink"] is not None:
         ds = got["dsink"].cpu().numpy().astype(np.float64)

@@ -43,9 +43,9 @@ def test_status_strings():
 
 
 def ws(dtype=tnd.TND_BF16, batch=2, cu_q=(0, 5, 9), cu_kv=(0, 5, 9), nq=4, nkv=2, d=128, scale=0.1, keep=1.0,
-       pre=INF, nxt=INF, mode=3, drop=False, sink=False, amask=False, prefix=None):
-    return tnd.tnd_attn_grad_workspace_size(dtype, batch, list(cu_q), list(cu_kv), prefix, nq, nkv, d, scale, keep,
-                                            pre, nxt, mode, drop, amask, sink)
+       pre=INF, nxt=INF, mode=3, drop=False, sink=False, amask=False, prefix=None, dv=None):
+    return tnd.tnd_attn_grad_workspace_size(dtype, batch, list(cu_q), list(cu_kv), prefix, nq, nkv, d,
+                                            d if dv is None else dv, scale, keep, pre, nxt, mode, drop, amask, sink)
 
 
 def test_workspace_size_accepts_valid_problems():
@@ -53,8 +53,12 @@ def test_workspace_size_accepts_valid_problems():
     assert st == tnd.TND_OK and n > 0
     st2, n2 = ws(cu_q=(0, 500, 900), cu_kv=(0, 500, 900))
     assert st2 == tnd.TND_OK and n2 > n
-    assert tnd.tnd_attn_fwd_workspace_size(tnd.TND_F32, 2, [0, 5, 9], [0, 5, 9], None, 4, 2, 64, 0.1, 1.0, INF,
+    assert tnd.tnd_attn_fwd_workspace_size(tnd.TND_F32, 2, [0, 5, 9], [0, 5, 9], None, 4, 2, 64, 64, 0.1, 1.0, INF,
                                            INF, 0, False, False, False)[0] == tnd.TND_OK
+    # a value head dim below the query / key one (qD == kD >= vD) runs on the CUDA-core kernels,
+    # which take no tensor-core dQ accumulator
+    assert ws(dv=64)[0] == tnd.TND_OK and ws(dv=64)[1] < ws()[1]
+    assert ws(d=96, dv=1)[0] == tnd.TND_OK
     # the packed matrix of the tensor-core kernels takes workspace
     assert ws(mode=1, amask=True)[1] > ws(mode=0)[1]
     assert ws(mode=6, prefix=[2, 4])[0] == tnd.TND_OK
@@ -93,6 +97,8 @@ def test_workspace_size_accepts_valid_problems():
     (dict(mode=8), tnd.TND_ERR_UNSUPPORTED),
     (dict(mode=4, pre=3, nxt=0, cu_kv=(0, 6, 9)), tnd.TND_ERR_UNSUPPORTED),  # band with Sq != Skv
     (dict(d=769), tnd.TND_ERR_INVALID),                           # D > 768
+    (dict(dv=129), tnd.TND_ERR_INVALID),                          # vD > qD
+    (dict(dv=0), tnd.TND_ERR_INVALID),
 ])
 def test_workspace_size_rejects(kw, expect):
     assert ws(**kw)[0] == expect
@@ -100,7 +106,8 @@ def test_workspace_size_rejects(kw, expect):
 
 def test_null_workspace_size_pointer_and_seqlens():
     L = tnd.lib()
-    assert L.tnd_attn_grad_workspace_size(1, 1, None, None, None, 1, 1, 128, 0.1, 1.0, 0, 0, 0, 0, 0, 0, None) == \
+    assert L.tnd_attn_grad_workspace_size(1, 1, None, None, None, 1, 1, 128, 128, 0.1, 1.0, 0, 0, 0, 0, 0, 0,
+                                          None) == \
         tnd.TND_ERR_NULLPTR
 
 
@@ -110,7 +117,8 @@ def _grad_call(**over):
     args = dict(query=4096, key=4096, value=4096, dy=4096, pse=None, pse_batch=0, pse_type=1, drop_mask=None,
                 atten_mask=None, softmax_max=4096,
                 softmax_sum=4096, attention_in=4096, sink=None, dtype=tnd.TND_BF16, batch=1, cu_q=[0, 8],
-                cu_kv=[0, 8], prefix=None, head_num=2, kv_head_num=1, head_dim=128, scale_value=0.1,
+                cu_kv=[0, 8], prefix=None, head_num=2, kv_head_num=1, head_dim=128, value_head_dim=128,
+                scale_value=0.1,
                 keep_prob=1.0, pre_tokens=INF, next_tokens=INF,
                 sparse_mode=3, dq=4096, dk=4096, dv=4096, dsink=None, workspace=None, workspace_size=0, stream=None)
     args.update(over)
@@ -134,6 +142,7 @@ def _grad_call(**over):
     (dict(pse=4098, pse_batch=1), tnd.TND_ERR_INVALID),                      # misaligned
     (dict(pse=4096, pse_batch=1, cu_kv=[0, 9]), tnd.TND_ERR_UNSUPPORTED),    # Sq != Skv
     (dict(head_num=3, kv_head_num=2), tnd.TND_ERR_INVALID),
+    (dict(value_head_dim=256), tnd.TND_ERR_INVALID),             # vD > qD
     (dict(query=4098), tnd.TND_ERR_INVALID),                     # misaligned
     (dict(workspace=None, workspace_size=0), tnd.TND_ERR_WORKSPACE),
     (dict(workspace=4096, workspace_size=16), tnd.TND_ERR_WORKSPACE),

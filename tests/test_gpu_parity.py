@@ -59,6 +59,12 @@ SMALL = {
     "pse_random_fp16_d64_type0": ("f16", [300, 129], None, 2, 2, 64, 2, INF, INF, 0.9, True,
                                   dict(pse=("random", 1, 0))),
     "pse_random_fp32": ("f32", [90, 33], None, 2, 1, 64, 3, INF, INF, 1.0, False, dict(pse=("random", 2, 1))),
+    # value head dim below the query / key one (qD == kD >= vD), CUDA-core kernels
+    "dv64_d128_causal_gqa_bf16": ("bf16", [200, 129, 1], None, 4, 2, 128, 3, INF, INF, 1.0, False, dict(dv=64)),
+    "dv40_d96_band_dropout_sink_fp16": ("f16", [150, 90], None, 2, 1, 96, 4, 30, 5, 0.8, True, dict(dv=40)),
+    "dv1_d64_full_sq_ne_skv_fp32": ("f32", [70, 33], [50, 40], 2, 2, 64, 0, INF, INF, 1.0, False, dict(dv=1)),
+    "dv256_d512_causal_amask_bf16": ("bf16", [40, 70], None, 2, 1, 512, 1, INF, INF, 1.0, False,
+                                     dict(dv=256, amask=0.3)),
 }
 
 
@@ -67,7 +73,7 @@ def _small(name, seed=777):
     extra = SMALL[name][11] if len(SMALL[name]) > 11 else {}
     wl = workloads.custom(name, dt, sq, sq if skv is None else skv, nq, nkv, d, keep_prob=keep,
                           pre_tokens=pre, next_tokens=nxt, sparse_mode=mode, has_sink=sink, seed=seed,
-                          amask_density=extra.get("amask", 0.0), prefix=extra.get("prefix"),
+                          amask_density=extra.get("amask", 0.0), prefix=extra.get("prefix"), dv=extra.get("dv", 0),
                           **(dict(zip(("pse_kind", "pse_batch", "pse_type"), extra["pse"])) if "pse" in extra else {}))
     return workloads.make_inputs(wl)
 

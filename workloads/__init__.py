@@ -78,6 +78,11 @@ class Workload:
     pse_kind: str = ""                     # "", "random" or "alibi"
     pse_batch: int = 1                     # 1 (shared) or B
     pse_type: int = 1                      # pseType 0 / 1
+    value_d: int = 0                       # head dim of value / dy / output (0: d)
+
+    @property
+    def dv(self) -> int:
+        return self.value_d or self.d
 
     @property
     def batch(self) -> int:
@@ -245,8 +250,8 @@ def make_inputs(wl: Workload, with_fp64: bool = True) -> Inputs:
     """Draw Q, K, V, dY (and sink / dropout mask when the workload uses them)."""
     q, q64 = normal(wl.seed, "q", (wl.tq, wl.nq, wl.d), wl.dtype)
     k, k64 = normal(wl.seed, "k", (wl.tkv, wl.nkv, wl.d), wl.dtype)
-    v, v64 = normal(wl.seed, "v", (wl.tkv, wl.nkv, wl.d), wl.dtype)
-    dy, dy64 = normal(wl.seed, "dy", (wl.tq, wl.nq, wl.d), wl.dtype)
+    v, v64 = normal(wl.seed, "v", (wl.tkv, wl.nkv, wl.dv), wl.dtype)
+    dy, dy64 = normal(wl.seed, "dy", (wl.tq, wl.nq, wl.dv), wl.dtype)
     sink = None
     if wl.has_sink:
         sink = _rng(wl.seed, "sink").standard_normal(size=wl.nq, dtype=np.float64).astype(np.float32)
@@ -295,9 +300,9 @@ def custom(name: str, dtype: str, seqlens_q, seqlens_kv, nq: int, nkv: int, d: i
            scale: Optional[float] = None, keep_prob: float = 1.0, pre_tokens: int = 2147483647,
            next_tokens: int = 2147483647, sparse_mode: int = 0, has_sink: bool = False,
            seed: int = BASE_SEED, amask_density: float = 0.0, prefix=None, pse_kind: str = "",
-           pse_batch: int = 1, pse_type: int = 1) -> Workload:
+           pse_batch: int = 1, pse_type: int = 1, dv: int = 0) -> Workload:
     """A workload with explicit shapes (used for edge cases and small parity runs)."""
     return Workload(name, dtype, list(seqlens_q), list(seqlens_kv), nq, nkv, d,
                     1.0 / math.sqrt(d) if scale is None else scale, keep_prob, pre_tokens,
                     next_tokens, sparse_mode, has_sink, seed, amask_density,
-                    None if prefix is None else list(prefix), pse_kind, pse_batch, pse_type)
+                    None if prefix is None else list(prefix), pse_kind, pse_batch, pse_type, dv)
