@@ -137,8 +137,14 @@ class Problem:
         self.atten_mask = None if atten_mask is None else np.ascontiguousarray(atten_mask, dtype=np.uint8)
         self.prefix = None if prefix is None else np.ascontiguousarray(prefix, dtype=np.int64)
         self.pse = None if pse is None else np.ascontiguousarray(pse, dtype=np.float64)
-        if self.pse is not None:
-            nb = len(cu_q) - 1
+        nb = len(cu_q) - 1
+        if self.pse is not None and pse_type in (2, 3):
+            # slopes: [B, N] or [N] (one set for every sequence)
+            if self.pse.ndim == 1:
+                self.pse = self.pse[None, :]
+            if self.pse.ndim != 2 or self.pse.shape[0] not in (1, nb) or self.pse.shape[1] != nq:
+                raise ValueError("pseType 2 / 3 take slopes of shape [B, Nq] or [Nq]")
+        elif self.pse is not None:
             if self.pse.ndim != 4 or self.pse.shape[0] not in (1, nb) or self.pse.shape[1] != nq or \
                     self.pse.shape[2] != 1024:
                 raise ValueError("pse is [B or 1, Nq, 1024, S]")
@@ -177,7 +183,7 @@ class Problem:
             ctypes.POINTER(ctypes.c_double)() if self.pse is None
             else self.pse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
             0 if self.pse is None else self.pse.shape[0],
-            0 if self.pse is None else self.pse.shape[3],
+            0 if self.pse is None or self.pse.ndim != 4 else self.pse.shape[3],
             int(pse_type), self.dv)
 
     @property
@@ -227,9 +233,18 @@ def keep_bit(mask: np.ndarray, index: int) -> int:
     return int(lib().ora_keep_bit(m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), index))
 
 
+def _check_shapes(p: Problem, **arrays):
+    want = {"q": (p.tq, p.nq, p.d), "k": (p.tkv, p.nkv, p.d), "v": (p.tkv, p.nkv, p.dv),
+            "dy": (p.tq, p.nq, p.dv), "out": (p.tq, p.nq, p.dv), "smax": (p.tq, p.nq), "ssum": (p.tq, p.nq)}
+    for name, a in arrays.items():
+        if a.shape != want[name]:
+            raise ValueError(f"{name} has shape {a.shape}, the problem needs {want[name]}")
+
+
 def fwd(p: Problem, q: np.ndarray, k: np.ndarray, v: np.ndarray):
     """fp64 forward: returns (out [Tq,Nq,Dv], smax [Tq,Nq], ssum [Tq,Nq])."""
     q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+    _check_shapes(p, q=q, k=k, v=v)
     out = np.zeros((p.tq, p.nq, p.dv))
     smax = np.full((p.tq, p.nq), np.nan)
     ssum = np.full((p.tq, p.nq), np.nan)
@@ -244,6 +259,7 @@ def grad(p: Problem, q, k, v, dy, out, smax, ssum, want_ds: bool = False):
     """fp64 gradient: returns (dq, dk, dv, dsink[, ds_dense])."""
     q, k, v, dy, out, smax, ssum = (np.ascontiguousarray(x, dtype=np.float64)
                                     for x in (q, k, v, dy, out, smax, ssum))
+    _check_shapes(p, q=q, k=k, v=v, dy=dy, out=out, smax=smax, ssum=ssum)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)

@@ -74,6 +74,11 @@
  *     is read along its diagonal from stored row 0, column j + (Sq - 1024 - i),
  *     which reproduces a bias that depends only on i - j (alibi).  dpseOut is
  *     a reserved output on the pages and is not computed.
+ *   - pseType 2 / 3 [ScoreV2, parameters]: the pse is generated inside from
+ *     one fp32 slope per (sequence or all, head), [B, N] or [N]; the pages do
+ *     not print the generator.  Reading: the alibi bias -slope |i - j| (2) and
+ *     -slope sqrt(|i - j|) (3, the table's extra sqrt), added after the scale
+ *     (both "multiply, then add").
  *   - head dims [UnpadGrad, constraints: qD == kD >= vD]: query, key, dQ and
  *     dK have D columns; value, dy, the attention output and dV have Dv <= D
  *     (Dv = D when not given).  <Q_i, K_j> runs over D, <dY_i, V_j> and
@@ -143,12 +148,21 @@ int ora_keep_at(const ora_problem *p, int64_t b, int64_t sq, int64_t skv, int64_
     }
 }
 
-/* pse of (b, h, i, j) from the stored last 1024 rows of the sequence's bias
- * [UnpadGrad, parameters: pseShiftOptional; UnpadGradV5, constraints: alibi
- * compression]; rows above the stored ones along their diagonal. */
+/* pse of (b, h, i, j).  pseType 0 / 1: from the stored last 1024 rows of the
+ * sequence's bias [UnpadGrad, parameters: pseShiftOptional; UnpadGradV5,
+ * constraints: alibi compression]; rows above the stored ones along their
+ * diagonal.  pseType 2 / 3: generated from the fp32 slope of (b, h) [ScoreV2,
+ * parameters: realShiftOptional is FLOAT32 [B, N] or [N] for them; the pseType
+ * table: generated inside, multiply then add (3: then sqrt)], read as the alibi
+ * bias -slope |i - j| (2) and -slope sqrt(|i - j|) (3). */
 double ora_pse_at(const ora_problem *p, int64_t b, int64_t h, int64_t sq, int64_t i, int64_t j)
 {
     const int64_t bb = p->pse_batch == 1 ? 0 : b;
+    if (p->pse_type == 2 || p->pse_type == 3) {
+        const double slope = p->pse[bb * p->Nq + h];
+        const double dist = (double)(i > j ? i - j : j - i);
+        return -slope * (p->pse_type == 2 ? dist : sqrt(dist));
+    }
     int64_t r = i - (sq - 1024), c = j;
     if (r < 0) {
         c = j - r;
@@ -157,7 +171,8 @@ double ora_pse_at(const ora_problem *p, int64_t b, int64_t h, int64_t sq, int64_
     return p->pse[((bb * p->Nq + h) * 1024 + r) * p->pse_cols + c];
 }
 
-/* the logit s_ij from <Q_i, K_j> [UnpadGrad: (QK^T + pse)/sqrt(d); ScoreV2: pseType] */
+/* the logit s_ij from <Q_i, K_j> [UnpadGrad: (QK^T + pse)/sqrt(d); ScoreV2: pseType 1
+ * adds then multiplies, every other type multiplies then adds] */
 static double logit(const ora_problem *p, double qk, int64_t b, int64_t h, int64_t sq, int64_t i, int64_t j)
 {
     if (p->pse == NULL) return p->scale * qk;

@@ -36,6 +36,12 @@ MUTANTS = {
     "prefix_top_left_anchor": ("case 6: return j <= i + (skv - sq)", "case 6: return j <= i"),
     "pse_rows_above_not_along_diagonal": ("        c = j - r;\n        r = 0;", "        r = 0;"),
     "pse_type_swapped": ("return p->pse_type == 1 ? p->scale * (qk + pse)", "return p->pse_type == 0 ? p->scale * (qk + pse)"),
+    "generated_alibi_sign": ("return -slope * (p->pse_type == 2 ? dist : sqrt(dist));",
+                             "return slope * (p->pse_type == 2 ? dist : sqrt(dist));"),
+    "generated_alibi_without_sqrt": ("return -slope * (p->pse_type == 2 ? dist : sqrt(dist));",
+                                     "return -slope * dist;"),
+    "generated_pse_before_scale": ("return p->pse_type == 1 ? p->scale * (qk + pse)",
+                                   "return p->pse_type != 0 ? p->scale * (qk + pse)"),
     "dp_drops_last_value_column": ("const double dP = dot(dy + r * Dv, vj, Dv);", "const double dP = dot(dy + r * Dv, vj, Dv - 1);"),
     "drow_drops_last_value_column": ("Drow[r] = dot(dy + r * Dv, out + r * Dv, Dv);", "Drow[r] = dot(dy + r * Dv, out + r * Dv, Dv - 1);"),
 }
@@ -62,6 +68,9 @@ def _pin_suite(ora):
             pins.test_random_pse_short_sequences_match_autograd(ora, pse_type)
         for ci in range(len(pins.DV_CASES)):
             pins.test_unequal_head_dims_match_autograd(ora, ci)
+        pins.test_generated_alibi_causal_equals_a_column_bias_in_one_more_dim(ora)
+        for pse_type in (2, 3):
+            pins.test_generated_alibi_matches_autograd(ora, pse_type, True)
     except AssertionError:
         return False
     return True

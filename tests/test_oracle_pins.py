@@ -324,6 +324,91 @@ def test_pse_grad_matches_central_differences(ora):
 
 
 # --------------------------------------------------------------------------
+# pse generated inside from slopes (pseType 2 / 3), read as alibi
+# --------------------------------------------------------------------------
+
+def test_generated_alibi_causal_equals_a_column_bias_in_one_more_dim(ora):
+    """pseType 2 under the causal mask: for j <= i the bias -slope (i - j) is
+    slope * j plus a constant of the row, which the softmax drops (it only moves
+    the max).  slope * j added after the scale is one more feature: Q gets a
+    column of ones, K the column slope * j / scale.  The no-pse problem in D + 1
+    dims then has the same O, dV, sum, the same dQ and dK in the first D
+    columns, and max + slope * i."""
+    seqs, nq, d = [37, 130, 1], 3, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(81, seqs, seqs, nq, nq, d)
+    slopes = np.array([0.3, -0.15, 0.02])
+    scale = scale_for(d) * 1.2
+    p = _problem(ora, cu_q, cu_kv, nq, nq, d, scale, sparse_mode=3, pse=slopes, pse_type=2)
+    out, smax, ssum, dq, dk, dv, _ = ora.fwd_grad(p, q, k, v, dy)
+    jpos = np.concatenate([np.arange(n) for n in seqs]).astype(np.float64)      # in-sequence index
+    q1 = np.concatenate([q, np.ones(q.shape[:2] + (1,))], axis=2)
+    k1 = np.concatenate([k, (slopes[None, :] * jpos[:, None] / scale)[..., None]], axis=2)
+    p1 = _problem(ora, cu_q, cu_kv, nq, nq, d + 1, scale, sparse_mode=3, dv=d)   # V, dY keep d columns
+    out1, smax1, ssum1, dq1, dk1, dv1, _ = ora.fwd_grad(p1, q1, k1, v, dy)
+    np.testing.assert_allclose(out, out1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ssum, ssum1, rtol=1e-12)
+    np.testing.assert_allclose(smax, smax1 - slopes[None, :] * jpos[:, None], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dq, dq1[..., :d], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, dk1[..., :d], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, dv1, rtol=1e-10, atol=1e-12)
+
+
+def test_generated_alibi_types_agree_at_distances_zero_and_one(ora):
+    """sqrt(0) = 0 and sqrt(1) = 1: with sequences of at most two rows the
+    sqrt variant (pseType 3) is bitwise the linear one (pseType 2)."""
+    seqs, nq, nkv, d = [2, 1, 2, 2], 2, 1, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(83, seqs, seqs, nq, nkv, d)
+    slopes = rng.standard_normal((len(seqs), nq))
+    r2 = ora.fwd_grad(_problem(ora, cu_q, cu_kv, nq, nkv, d, 0.7, sparse_mode=2, pse=slopes, pse_type=2), q, k, v, dy)
+    r3 = ora.fwd_grad(_problem(ora, cu_q, cu_kv, nq, nkv, d, 0.7, sparse_mode=2, pse=slopes, pse_type=3), q, k, v, dy)
+    for a_, b_ in zip(r2, r3):
+        np.testing.assert_array_equal(a_, b_)
+
+
+def test_generated_pse_with_zero_slopes_is_no_pse(ora):
+    seqs, nq, nkv, d = [40, 9], 2, 2, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(85, seqs, seqs, nq, nkv, d)
+    r0 = ora.fwd_grad(_problem(ora, cu_q, cu_kv, nq, nkv, d, 0.3, sparse_mode=3), q, k, v, dy)
+    for pse_type in (2, 3):
+        r = ora.fwd_grad(_problem(ora, cu_q, cu_kv, nq, nkv, d, 0.3, sparse_mode=3, pse=np.zeros(nq),
+                                  pse_type=pse_type), q, k, v, dy)
+        for a_, b_ in zip(r, r0):
+            np.testing.assert_array_equal(a_, b_)
+
+
+@pytest.mark.parametrize("pse_type", [2, 3])
+@pytest.mark.parametrize("per_batch", [False, True])
+def test_generated_alibi_matches_autograd(ora, pse_type, per_batch):
+    """The reading written out as explicit [Nq, Sq, Sq] bias matrices, added
+    after the scale, through torch autograd; slopes per head ([N]) or per
+    sequence and head ([B, N]), GQA and a bias over more than 1024 rows."""
+    seqs, nq, nkv, d = [1100, 57, 3], 4, 2, 8
+    rng, cu_q, cu_kv, q, k, v, dy = random_problem(87 + pse_type, seqs, seqs, nq, nkv, d)
+    slopes = 0.01 * rng.standard_normal((len(seqs), nq) if per_batch else (nq,))
+    full = []
+    for b, sq in enumerate(seqs):
+        sl = slopes[b] if per_batch else slopes
+        dist = np.abs(np.arange(sq)[:, None] - np.arange(sq)[None, :]).astype(np.float64)
+        full.append(-sl[:, None, None] * (dist if pse_type == 2 else np.sqrt(dist))[None])
+    scale = scale_for(d)
+    p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, sparse_mode=3, pse=slopes, pse_type=pse_type)
+    ref = autograd_reference(cu_q, cu_kv, nq, nkv, d, scale, q, k, v, dy, mode=3, bias=full, pse_type=0)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(smax, ref["smax"], rtol=1e-12, atol=1e-12)
+    dq, dk, dv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-11, err_msg=name)
+
+
+def test_generated_pse_slope_shapes(ora):
+    with pytest.raises(ValueError):
+        _problem(ora, [0, 3, 5], [0, 3, 5], 2, 1, 8, 0.3, sparse_mode=3, pse=np.zeros((3, 2)), pse_type=2)
+    with pytest.raises(ValueError):
+        _problem(ora, [0, 3], [0, 3], 2, 1, 8, 0.3, sparse_mode=3, pse=np.zeros(3), pse_type=3)
+
+
+# --------------------------------------------------------------------------
 # dropout keep-bit layout
 # --------------------------------------------------------------------------
 
