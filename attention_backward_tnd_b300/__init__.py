@@ -230,10 +230,18 @@ def _check_amask(atten_mask, cu_q, cu_kv):
         raise ValueError(f"atten_mask must be a contiguous uint8/bool tensor of shape ({s1}, {s2})")
 
 
-def _check_pse(pse, q, cu_kv, batch) -> int:
-    """pse must be a contiguous [B or 1, Nq, 1024, S2Max] tensor of q's dtype; returns its first dim (0 = none)."""
+def _check_pse(pse, q, cu_kv, batch, pse_type=1) -> int:
+    """pse must be a contiguous [B or 1, Nq, 1024, S2Max] tensor of q's dtype (pseType 0 / 1) or
+    float32 slopes [B, Nq] or [Nq] (pseType 2 / 3); returns its first dim (0 = none)."""
+    import torch
     if pse is None:
         return 0
+    if pse_type in (2, 3):
+        if pse.dtype != torch.float32 or not pse.is_contiguous() or pse.shape[-1] != q.shape[1] or \
+                pse.dim() not in (1, 2) or (pse.dim() == 2 and pse.shape[0] != batch):
+            raise ValueError(f"pseType {pse_type} takes contiguous float32 slopes [{batch}, {q.shape[1]}] "
+                             f"or [{q.shape[1]}]")
+        return batch if pse.dim() == 2 else 1
     s2 = int(np.max(np.diff(_cu(cu_kv))))
     if pse.dim() != 4 or pse.shape[0] not in (1, batch) or tuple(pse.shape[1:]) != (q.shape[1], 1024, s2) or \
             pse.dtype != q.dtype or not pse.is_contiguous():
@@ -251,7 +259,8 @@ def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_p
         sink=None, workspace=None, atten_mask=None, prefix=None, pse=None, pse_type: int = 1):
     """Forward on torch CUDA tensors: returns (out, softmax_max, softmax_sum) ([T,N,8] fp32 stats).
     atten_mask: uint8/bool CUDA tensor [S1Max, S2Max] (nonzero masks); prefix: host ints (sparse_mode 6);
-    pse: CUDA tensor [B or 1, Nq, 1024, S2Max] in q's dtype (the last 1024 rows of each sequence's bias)."""
+    pse: CUDA tensor [B or 1, Nq, 1024, S2Max] in q's dtype (the last 1024 rows of each sequence's bias;
+    pse_type 0 / 1), or float32 slopes [B, Nq] or [Nq] (pse_type 2 / 3: the bias is generated)."""
     import torch
     tq, nq, d = q.shape
     nkv, dv = k.shape[1], v.shape[2]
@@ -268,7 +277,7 @@ def fwd(q, k, v, cu_q: Sequence[int], cu_kv: Sequence[int], scale: float, keep_p
     ssum = torch.empty((tq, nq, 8), dtype=torch.float32, device=q.device)
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
-    pb = _check_pse(pse, q, cu_kv, batch)
+    pb = _check_pse(pse, q, cu_kv, batch, pse_type)
     st = tnd_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(pse), pb, pse_type, _ptr(drop_mask),
                       _ptr(atten_mask), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, dv, scale,
                       keep_prob, pre_tokens, next_tokens, sparse_mode, out.data_ptr(), smax.data_ptr(), ssum.data_ptr(),
@@ -310,7 +319,7 @@ def grad(q, k, v, dy, out, softmax_max, softmax_sum, cu_q, cu_kv, scale, keep_pr
         dsink = torch.empty(nq, dtype=torch.float32, device=q.device) if sink is not None else None
     else:
         dq, dk, dv, dsink = outputs
-    pb = _check_pse(pse, q, cu_kv, batch)
+    pb = _check_pse(pse, q, cu_kv, batch, pse_type)
     st = tnd_attn_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), dy.data_ptr(), _ptr(pse), pb, pse_type,
                        _ptr(drop_mask), _ptr(atten_mask), softmax_max.data_ptr(), softmax_sum.data_ptr(),
                        out.data_ptr(), _ptr(sink), dt, batch, cu_q, cu_kv, prefix, nq, nkv, d, dvd, scale,

@@ -189,6 +189,15 @@ __device__ __forceinline__ void fpse_chunk(const FwdArgs &a, const FUnit &U, int
                                            float C, float (&t)[32])
 {
     using Elt = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    if (pse_generated(a.pse)) {
+        const float slope = pse_slope(a.pse, a.nq, U.b, U.h);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int64_t j = jc + c;
+            t[c] = (row_ok && j < U.sd.skv) ? pse_alibi(a.pse.type, slope, i, j) * kLog2e : 0.0f;
+        }
+        return;
+    }
     const Elt *pp = reinterpret_cast<const Elt *>(a.pse.ptr);
     const float mul = a.pse.type == 1 ? C : kLog2e;
 #pragma unroll

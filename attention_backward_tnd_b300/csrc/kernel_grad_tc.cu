@@ -407,6 +407,15 @@ __device__ __forceinline__ void pse_chunk(const GradArgs &a, const UnitInfo &U, 
                                           float (&t)[32])
 {
     using Elt = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    if (pse_generated(a.pse)) {
+        const float slope = pse_slope(a.pse, a.nq, U.b, h);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int64_t i = qc + c;
+            t[c] = (i < U.sd.sq && jj < U.sd.skv) ? pse_alibi(a.pse.type, slope, i, jj) * kLog2e : 0.0f;
+        }
+        return;
+    }
     const Elt *pp = reinterpret_cast<const Elt *>(a.pse.ptr);
     const float mul = a.pse.type == 1 ? C : kLog2e;
 #pragma unroll

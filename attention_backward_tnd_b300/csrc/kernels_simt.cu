@@ -56,11 +56,13 @@ __device__ __forceinline__ void block_union(int64_t lo, int64_t hi, int64_t &ulo
 }
 
 // pse term of (sequence b, head h, row i, column j) in the log2 units of the
-// scores (pseType 1 is scaled like QK^T, pseType 0 is added after the scale).
+// scores (pseType 1 is scaled like QK^T, the others are added after the
+// scale; 2 and 3 are generated from the head's slope).
 template <typename T>
 __device__ __forceinline__ float pse_term(const PseSpec &ps, int32_t nq, float C, int64_t b, int64_t h, int64_t sq,
                                           int64_t i, int64_t j)
 {
+    if (pse_generated(ps)) return pse_alibi(ps.type, pse_slope(ps, nq, b, h), i, j) * kLog2e;
     const T *pp = (const T *)ps.ptr;
     return Elem<T>::load(pp + pse_index(ps, nq, b, h, sq, i, j)) * (ps.type == 1 ? C : kLog2e);
 }

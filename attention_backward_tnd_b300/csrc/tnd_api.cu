@@ -172,13 +172,12 @@ tnd_status validate(int dtype, int64_t batch, const int64_t *cuq, const int64_t 
 
 // pseShiftOptional checks ([UnpadGrad] parameters: shape [B or 1, N, 1024, S];
 // alibi needs a lower-triangle mask and Sq = Skv; [ScoreV2] parameters:
-// pseType 0 / 1 take the given pse, 2 / 3 generate it inside, which is not
-// implemented here).
+// pseType 0 / 1 take the given pse, 2 / 3 generate it inside from fp32 slopes
+// [B, N] or [N], only for Sq = Skv).
 tnd_status check_pse(const Problem &p, const void *pse, int64_t pse_batch, int64_t pse_type)
 {
     if (!pse) return TND_OK;
-    if (pse_type == 2 || pse_type == 3) return TND_ERR_UNSUPPORTED;
-    if (pse_type != 0 && pse_type != 1) return TND_ERR_INVALID;
+    if (pse_type < 0 || pse_type > 3) return TND_ERR_INVALID;
     if (pse_batch != 1 && pse_batch != p.batch) return TND_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(pse) & 15u) != 0) return TND_ERR_INVALID;
     if (p.mode != 2 && p.mode != 3) return TND_ERR_UNSUPPORTED;

@@ -90,17 +90,35 @@ __host__ __device__ inline bool matrix_keeps(const MaskSpec &m, int64_t i, int64
     return m.amask == nullptr || m.amask[i * m.amask_cols + j] == 0;
 }
 
-// pseShiftOptional: for each sequence (or for all, when batch is 1) and query
-// head, the last 1024 rows of the sequence's [Sq, Skv] bias, stored as
-// [batch][Nq][1024][cols] in the element dtype.  Row i of a sequence is stored
-// row i - (Sq - 1024); a row above the stored ones is read along its diagonal
-// from stored row 0, column j + (Sq - 1024 - i).
+// pseShiftOptional.  pseType 0 / 1: for each sequence (or for all, when
+// batch is 1) and query head, the last 1024 rows of the sequence's [Sq, Skv]
+// bias, stored as [batch][Nq][1024][cols] in the element dtype.  Row i of a
+// sequence is stored row i - (Sq - 1024); a row above the stored ones is read
+// along its diagonal from stored row 0, column j + (Sq - 1024 - i).
+// pseType 2 / 3 ("aclnnFlashAttentionScoreV2", parameters: generated inside
+// from FLOAT32 [B, N] or [N]): one fp32 slope per (sequence or all, head),
+// the bias being the alibi -slope |i - j| (2) or -slope sqrt(|i - j|) (3).
 struct PseSpec {
     const void *ptr;   // NULL = no pse
     int32_t batch;     // 1 or B
-    int32_t type;      // pseType 0: s = scale*qk + pse;  1: s = scale*(qk + pse)
-    int64_t cols;      // S2Max
+    int32_t type;      // pseType 1: s = scale*(qk + pse); 0, 2, 3: s = scale*qk + pse
+    int64_t cols;      // S2Max (stored types)
 };
+
+__host__ __device__ inline bool pse_generated(const PseSpec &ps) { return ps.type >= 2; }
+
+// slope of (sequence b, head h) of a generated pse
+__device__ __forceinline__ float pse_slope(const PseSpec &ps, int32_t nq, int64_t b, int64_t h)
+{
+    return reinterpret_cast<const float *>(ps.ptr)[(ps.batch == 1 ? 0 : b) * nq + h];
+}
+
+// the generated bias at distance |i - j|
+__device__ __forceinline__ float pse_alibi(int32_t type, float slope, int64_t i, int64_t j)
+{
+    const float dist = (float)(i > j ? i - j : j - i);
+    return -slope * (type == 2 ? dist : sqrtf(dist));
+}
 
 __host__ __device__ inline int64_t pse_index(const PseSpec &ps, int32_t nq, int64_t b, int64_t h, int64_t sq,
                                              int64_t i, int64_t j)

@@ -78,10 +78,15 @@
  *   its diagonal from stored row 0, column j + (Sq - 1024 - i), which is
  *   exact for a bias that depends on i - j only (alibi).  pse_type 1 adds it
  *   before the scale (scale * (QK^T + pse), the grad page's formula), 0 after
- *   it (scale * QK^T + pse); 2 and 3 (pse generated inside) return
- *   TND_ERR_UNSUPPORTED.  With a pse, sparse_mode must be 2 or 3 and Sq_b ==
- *   Skv_b for every sequence (the pages' alibi constraint), else
- *   TND_ERR_UNSUPPORTED.  NULL = no pse (pse_batch and pse_type ignored).
+ *   it (scale * QK^T + pse).  pse_type 2 and 3 generate the pse inside
+ *   ([ScoreV2] parameters: realShiftOptional is then FLOAT32 [B, N] or [N]):
+ *   pse is a device fp32 array of slopes [pse_batch, Nq] (pse_batch = B or 1)
+ *   and the bias, added after the scale, is -slope * |i - j| (2) or
+ *   -slope * sqrt(|i - j|) (3); the pages do not print the generator, this
+ *   is the alibi reading of their table.  With a pse, sparse_mode must be 2
+ *   or 3 and Sq_b == Skv_b for every sequence (the pages' alibi constraint),
+ *   else TND_ERR_UNSUPPORTED.  NULL = no pse (pse_batch and pse_type
+ *   ignored); a pse_type outside 0..3 is TND_ERR_INVALID.
  *   dpseOut is a reserved output on the pages and is not produced.
  * GQA: Nq % Nkv == 0; query head h uses key/value head h / (Nq/Nkv).
  *

@@ -26,7 +26,12 @@ def upload(inp: workloads.Inputs):
     dev["sink"] = None if inp.sink is None else torch.from_numpy(inp.sink).cuda()
     dev["mask"] = None if inp.mask is None else torch.from_numpy(inp.mask).cuda()
     dev["amask"] = None if inp.amask is None else torch.from_numpy(inp.amask).cuda()
-    dev["pse"] = None if inp.pse is None else to_device(inp.pse, wl.dtype)
+    if inp.pse is None:
+        dev["pse"] = None
+    elif wl.pse_kind == "slopes":            # fp32 slopes of a generated pse (pseType 2 / 3)
+        dev["pse"] = torch.from_numpy(inp.pse).cuda()
+    else:
+        dev["pse"] = to_device(inp.pse, wl.dtype)
     return dev
 
 

@@ -136,7 +136,10 @@ def _grad_call(**over):
     (dict(sparse_mode=6), tnd.TND_ERR_NULLPTR),                  # no prefix
     (dict(sparse_mode=6, prefix=[9]), tnd.TND_ERR_INVALID),
     (dict(pse=4096, pse_batch=1, sparse_mode=0), tnd.TND_ERR_UNSUPPORTED),   # pse needs a lower triangle
-    (dict(pse=4096, pse_batch=1, pse_type=2), tnd.TND_ERR_UNSUPPORTED),      # pse generated inside
+    (dict(pse=4096, pse_batch=1, pse_type=2, sparse_mode=0), tnd.TND_ERR_UNSUPPORTED),  # generated: lower triangle
+    (dict(pse=4096, pse_batch=1, pse_type=3, cu_kv=[0, 9]), tnd.TND_ERR_UNSUPPORTED),   # generated: Sq == Skv
+    (dict(pse=4096, pse_batch=2, pse_type=2), tnd.TND_ERR_INVALID),                     # slopes [B, N] or [N]
+    (dict(pse=4096, pse_batch=1, pse_type=-1), tnd.TND_ERR_INVALID),
     (dict(pse=4096, pse_batch=1, pse_type=5), tnd.TND_ERR_INVALID),
     (dict(pse=4096, pse_batch=3), tnd.TND_ERR_INVALID),                      # first dim is 1 or B
     (dict(pse=4098, pse_batch=1), tnd.TND_ERR_INVALID),                      # misaligned

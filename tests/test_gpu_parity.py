@@ -59,6 +59,12 @@ SMALL = {
     "pse_random_fp16_d64_type0": ("f16", [300, 129], None, 2, 2, 64, 2, INF, INF, 0.9, True,
                                   dict(pse=("random", 1, 0))),
     "pse_random_fp32": ("f32", [90, 33], None, 2, 1, 64, 3, INF, INF, 1.0, False, dict(pse=("random", 2, 1))),
+    # pse generated from slopes (pseType 2 / 3, alibi)
+    "pse_gen_type2_bf16_long": ("bf16", [1300, 200], None, 4, 2, 128, 3, INF, INF, 1.0, False,
+                                dict(pse=("slopes", 2, 2))),
+    "pse_gen_type3_fp16_d64_dropout_sink": ("f16", [300, 129], None, 2, 2, 64, 2, INF, INF, 0.9, True,
+                                            dict(pse=("slopes", 1, 3))),
+    "pse_gen_type2_fp32": ("f32", [90, 33], None, 2, 1, 64, 3, INF, INF, 1.0, False, dict(pse=("slopes", 1, 2))),
     # value head dim below the query / key one (qD == kD >= vD), CUDA-core kernels
     "dv64_d128_causal_gqa_bf16": ("bf16", [200, 129, 1], None, 4, 2, 128, 3, INF, INF, 1.0, False, dict(dv=64)),
     "dv40_d96_band_dropout_sink_fp16": ("f16", [150, 90], None, 2, 1, 96, 4, 30, 5, 0.8, True, dict(dv=40)),

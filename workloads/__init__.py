@@ -50,7 +50,7 @@ from typing import Dict, List, Optional
 import numpy as np
 
 # stream ids of the independent tensors drawn for one workload
-_STREAM = {"seqlens": 1, "q": 2, "k": 3, "v": 4, "dy": 5, "sink": 6, "mask": 7, "amask": 8, "pse": 9}
+_STREAM = {"seqlens": 1, "q": 2, "k": 3, "v": 4, "dy": 5, "sink": 6, "mask": 7, "amask": 8, "pse": 9, "slopes": 10}
 
 BASE_SEED = 20261202
 
@@ -75,7 +75,7 @@ class Workload:
     seed: int = BASE_SEED
     amask_density: float = 0.0             # > 0: an attention-mask matrix is drawn
     prefix: Optional[List[int]] = None     # prefixOptional (sparseMode 6)
-    pse_kind: str = ""                     # "", "random" or "alibi"
+    pse_kind: str = ""                     # "", "random" or "alibi" (stores), "slopes" (pseType 2 / 3)
     pse_batch: int = 1                     # 1 (shared) or B
     pse_type: int = 1                      # pseType 0 / 1
     value_d: int = 0                       # head dim of value / dy / output (0: d)
@@ -262,7 +262,9 @@ def make_inputs(wl: Workload, with_fp64: bool = True) -> Inputs:
     if wl.amask_density > 0:
         amask = atten_mask_matrix(wl.seed, max(wl.seqlens_q), max(wl.seqlens_kv), wl.amask_density)
     pse = pse64 = None
-    if wl.pse_kind:
+    if wl.pse_kind == "slopes":
+        pse, pse64 = pse_slopes(wl)
+    elif wl.pse_kind:
         pse, pse64 = pse_store(wl)
     if not with_fp64:
         q64 = k64 = v64 = dy64 = None
@@ -284,6 +286,17 @@ def pse_store(wl: Workload):
             cols = np.arange(s2)
             x[b] = slopes[:, None, None] * (cols[None, None, :] - rows[None, :, None])
     return round_to_dtype(x, wl.dtype)
+
+
+def pse_slopes(wl: Workload):
+    """fp32 slopes of a generated pse: [pse_batch, Nq], or [Nq] when pse_batch is 1; the
+    usual alibi geometric slopes 2^-(8 (h + 1) / Nq) with a per-sequence jitter."""
+    base = 2.0 ** (-8.0 * (np.arange(wl.nq) + 1) / wl.nq)
+    jit = 1.0 + 0.25 * _rng(wl.seed, "slopes").random(size=(wl.pse_batch, wl.nq))
+    x = (base[None, :] * jit).astype(np.float32)
+    if wl.pse_batch == 1:
+        x = x[0]
+    return x, x.astype(np.float64)
 
 
 def atten_mask_matrix(seed: int, rows: int, cols: int, density: float) -> np.ndarray:
