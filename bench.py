@@ -469,24 +469,64 @@ def run_ours(args, wl, rank, world, local_rank):
     dev_out = [t for t in outs if t is not None]
     h2d = int(sum(t.numel() * t.element_size() for t in host_in))
     d2h = int(sum(t.numel() * t.element_size() for t in host_out))
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(4, min(args.steps, 12))
+    # two device buffer sets, pipelined over three streams: step i's inputs go
+    # up while step i-1 computes and step i-2's results come down (the copy
+    # engines run both directions at once); every step still copies all its
+    # inputs in and all its results out
+    n_in = 7
+    dev_sets = [(dev_in, dev_out), ([torch.empty_like(d) for d in dev_in], [torch.empty_like(d) for d in dev_out])]
+    host_out_sets = [host_out, [torch.empty_like(h).pin_memory() for h in host_out]]
+    comp = torch.cuda.current_stream()
+    s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for hsrc, d in zip(host_in, dev_in):
-            d.copy_(hsrc, non_blocking=True)
-        step()
-        for d, hdst in zip(dev_out, host_out):
-            hdst.copy_(d, non_blocking=True)
+    def step_on(ins, outs_):
+        q_, k_, v_, dy_, o_, m_, l_ = ins[:n_in]
+        extra = ins[n_in:]
+        sink_ = extra[0] if sink is not None else None
+        mask_ = extra[-1] if mask is not None else None
+        tnd.grad(q_, k_, v_, dy_, o_, m_, l_, cu_q, cu_kv, wl.scale, wl.keep_prob, wl.pre_tokens,
+                 wl.next_tokens, wl.sparse_mode, mask_, sink_, workspace=ws,
+                 outputs=tuple(outs_) + ((None,) if sink is None else ()))
 
-    e2e_step()
+    def e2e_run(n, start):
+        for s_ in (s_up, s_down):
+            s_.wait_event(start)
+        for i in range(n):
+            b_ = i % 2
+            ins, outs_ = dev_sets[b_]
+            with torch.cuda.stream(s_up):
+                if i >= 2:
+                    s_up.wait_event(ev_comp[b_])          # step i-2 has read this input set
+                for hsrc, d in zip(host_in, ins):
+                    d.copy_(hsrc, non_blocking=True)
+                ev_in[b_].record(s_up)
+            comp.wait_event(ev_in[b_])
+            if i >= 2:
+                comp.wait_event(ev_out[b_])               # step i-2's results have been read out
+            step_on(ins, outs_)
+            ev_comp[b_].record(comp)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(ev_comp[b_])
+                for d, hdst in zip(outs_, host_out_sets[b_]):
+                    hdst.copy_(d, non_blocking=True)
+                ev_out[b_].record(s_down)
+        for b_ in range(min(n, 2)):
+            comp.wait_event(ev_out[b_])
+
+    warm = torch.cuda.Event()
+    warm.record(comp)
+    e2e_run(2, warm)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record()
+    e0.record(comp)
+    e2e_run(e2e_steps, e0)
+    e1.record(comp)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if dist is not None:
@@ -515,7 +555,10 @@ def run_ours(args, wl, rank, world, local_rank):
             "arrival_order": arrival,
             "gpu_launches": launches,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms, "steps": e2e_steps,
+                    "schedule": "pinned host buffers; each step's inputs copied in, its dq/dk/dv(/dsink) copied "
+                                "out; two device buffer sets, uploads / gradient / downloads on three streams "
+                                "so that consecutive steps overlap"},
             "clocks": clk.summary(),
             "wall_s_timed_region": wall,
         }
