@@ -399,7 +399,7 @@ int ora_grad(const ora_problem *p, const double *q, const double *k, const doubl
         for (int64_t d = 0; d < Dv; ++d) dvj[d] = 0.0;
         for (int64_t h = g * G; h < (g + 1) * G; ++h) {
             if (h < p->h_lo || h >= p->h_hi) continue;
-            for (int64_t i = 0; i < sq; ++i) {
+            for (int64_t i = p->row_lo ? p->row_lo[b] : 0; i < sq; ++i) {
                 if (!row_selected(p, b, i)) continue;
                 const int64_t r = (tq + i) * p->Nq + h;
                 double pz;

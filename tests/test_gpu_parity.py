@@ -349,3 +349,55 @@ def test_paths_agree_closely():
     for n in ("dq", "dk", "dv"):
         x, y = gh.host64(a[n]), gh.host64(b[n])
         assert np.all(np.abs(x - y) <= 1e-2 + 2e-2 * np.abs(y)), n
+
+
+# --------------------------------------------------------------------------
+# the pages' size limits (aclnnFlashAttentionUnpaddingScoreGrad /
+# aclnnFlashAttentionUnpaddingScoreGradV5, constraints: N <= 256, B <= 20000,
+# B <= 1K with prefixOptional, T <= 1M)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("nq,nkv,d", [(256, 4, 64), (256, 256, 128)], ids=["256_on_4_d64", "256_on_256_d128"])
+def test_maximum_head_count_matches_oracle(nq, nkv, d):
+    """256 query heads.  dK and dV sum over G * Sq terms (G = 64 here), and a
+    few of their 35k - 4.5M elements move past the bf16 bar's fixed 1e-2 floor
+    from the rounding of dS and P to bf16 alone (a CPU replay that rounds
+    only dS shows the same); those outputs get the operand-rounding bound on
+    top of the bar.  O, max and sum keep the bar as stated."""
+    wl = workloads.custom(f"heads_{nq}_{nkv}", "bf16", [130, 7], [130, 7], nq, nkv, d, sparse_mode=3, seed=41)
+    inp = workloads.make_inputs(wl)
+    gh.compare_all(inp, gh.run_library(inp), gh.oracle_reference(inp), operand_rounding=True)
+
+
+def test_maximum_batch_of_tiny_sequences_matches_oracle():
+    """20000 sequences of 0-6 rows (empty ones included), GQA, causal, with a sink."""
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(0, 7, size=20000)]
+    wl = workloads.custom("batch_20000", "f16", lens, lens, 2, 1, 64, sparse_mode=3, has_sink=True, seed=43)
+    inp = workloads.make_inputs(wl)
+    gh.compare_all(inp, gh.run_library(inp), gh.oracle_reference(inp))
+
+
+def test_maximum_prefix_batch_matches_oracle():
+    """1024 sequences (the limit with prefixOptional) in the prefix mode."""
+    rng = np.random.default_rng(8)
+    sq = [int(x) for x in rng.integers(1, 40, size=1024)]
+    skv = [s + int(x) for s, x in zip(sq, rng.integers(0, 20, size=1024))]
+    prefix = [int(rng.integers(0, k + 1)) for k in skv]
+    wl = workloads.custom("prefix_1024", "bf16", sq, skv, 2, 2, 128, sparse_mode=6, prefix=prefix, seed=45)
+    inp = workloads.make_inputs(wl)
+    gh.compare_all(inp, gh.run_library(inp), gh.oracle_reference(inp))
+
+
+def test_maximum_token_count_sampled():
+    """T = 2^20 query and key rows (one 512K-row sequence among four), causal:
+    the last 64 query rows of every sequence and the last 64 key rows, whose
+    gradients those rows alone reach, are compared with the oracle."""
+    lens = [524288, 262144, 262143, 1]
+    assert sum(lens) == 1 << 20
+    wl = workloads.custom("tokens_1m", "bf16", lens, lens, 1, 1, 64, sparse_mode=3, seed=47)
+    inp = workloads.make_inputs(wl)
+    got = gh.run_library(inp)
+    qm, row_lo = _suffix_rows(wl, 64)
+    ref = gh.oracle_reference(inp, row_lo=row_lo)
+    gh.compare_all(inp, got, ref, q_rows=qm, kv_rows=_kv_suffix(wl, 64))
