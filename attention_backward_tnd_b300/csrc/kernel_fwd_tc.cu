@@ -16,14 +16,17 @@
 // only when its block max exceeds the max in use by more than 2^8, so P
 // stays below 256; the emitted max and sum are those of the true row max.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over (q block, head)
+// Warp roles (320 threads, one CTA per SM, persistent over (q block, head)
 // units taken in plan order, longest kv range first):
 //   warp 0      TMA producer: Q per unit; K, V per kv block (three stages)
 //   warp 1      TMEM allocator and single-thread UMMA issuer
-//   warps 2-5   softmax warps: thread = TMEM lane = q row (one warp per lane
-//               quarter), all 128 kv columns of a block; O out at unit end
+//   warps 2-9   softmax warps: thread = TMEM lane = q row, two warps per lane
+//               quarter, each on 64 of a block's 128 kv columns (they trade
+//               block maxima and, at a unit's end, sums); O out at unit end,
+//               half of its columns each
 // TMEM: O (HD columns), two S buffers of 128 columns (S(j) in buffer j % 2,
-// then P packed in place until O += P V has read it).
+// then P packed in place, each 32-column chunk in its own first 16 columns,
+// until O += P V has read it).
 // Every wait is bounded; on expiry the kernel records TND_ERR_DEVICE_TIMEOUT
 // in the workspace status word and winds down instead of hanging.
 #include "ptx_sm103.cuh"
@@ -37,7 +40,7 @@ namespace {
 using namespace ptx;
 
 constexpr int BN = kKvBlock;             // 128 kv rows (UMMA N of S, K of O += P V)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int NS = 3;                    // K / V stages
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0, TM_S = 256; // S buffers at 256 and 384
@@ -54,7 +57,8 @@ struct FGeo {
     static constexpr uint32_t OFF_BAR = OFF_V + NS * kTile;
     static constexpr uint32_t kNumBars = 32;
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
-    static constexpr uint32_t kSmemBytes = OFF_MISC + 64;
+    static constexpr uint32_t OFF_XCH = OFF_MISC + 64;     // softmax halves' exchange, 2 x [2][128] fp32
+    static constexpr uint32_t kSmemBytes = OFF_XCH + 2 * 2 * 128 * 4;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -66,13 +70,14 @@ enum : int {
     F_V_FULL = 8,       // [3]  count 1 + tx
     F_V_EMPTY = 11,     // [3]  count 1 (commit after O += P V)
     F_S_FULL = 14,      // [2]  count 1 (commit)
-    F_P_READY = 16,     // [2]  count 128
+    F_P_READY = 16,     // [2]  count 256
     F_PV_DONE = 18,     // [2]  count 1 (commit after O += P V: P read, O current)
     F_O_FULL = 20,      //      count 1 (commit after the unit's last O += P V)
-    F_O_FREE = 21,      //      count 128 (O read out)
+    F_O_FREE = 21,      //      count 256 (O read out)
     F_UNIT_FULL = 22,   // [2]  count 1
-    F_UNIT_EMPTY = 24,  // [2]  count 5 (MMA + 4 softmax warps)
+    F_UNIT_EMPTY = 24,  // [2]  count 9 (MMA + 8 softmax warps)
     F_DRAIN = 26,       //      count 1
+    F_XCH = 27,         // [4]  count 64 (the two softmax warps of a lane quarter)
 };
 constexpr uint32_t MISC_TMEM = 0, MISC_RING = 1, MISC_ABORT = 3;
 
@@ -182,6 +187,11 @@ __device__ __forceinline__ void fetch_keep128(const FwdArgs &a, const SeqDesc &s
     }
 }
 
+// TMEM column of the packed P for kv columns 16 kk .. 16 kk + 15 within an S
+// buffer: each 32-column chunk of S holds its own 32 P values, packed two per
+// column, in its first 16 columns
+__device__ __forceinline__ uint32_t fpk_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
+
 // pse terms (log2 units of C * S) of row i over kv columns jc .. jc + 31, 0
 // outside the sequence (those columns are masked anyway)
 template <bool BF16>
@@ -244,14 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(sm.bar(F_S_FULL + i), 1);
-            mbar_init(sm.bar(F_P_READY + i), 128);
+            mbar_init(sm.bar(F_P_READY + i), 256);
             mbar_init(sm.bar(F_PV_DONE + i), 1);
             mbar_init(sm.bar(F_UNIT_FULL + i), 1);
-            mbar_init(sm.bar(F_UNIT_EMPTY + i), 5);
+            mbar_init(sm.bar(F_UNIT_EMPTY + i), 9);
         }
         mbar_init(sm.bar(F_O_FULL), 1);
-        mbar_init(sm.bar(F_O_FREE), 128);
+        mbar_init(sm.bar(F_O_FREE), 256);
         mbar_init(sm.bar(F_DRAIN), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(sm.bar(F_XCH + q), 64);
         *sm.abort_flag() = 0;
         fence_mbar_init();
     }
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t dv = fdesc_at(dV0, s * G_::kTile);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ts(tmem + TM_O, tmem + TM_S + 128 * b + 8 * kk, fdesc_at(dv, kk * 2048), idO,
+                        mma_ts(tmem + TM_O, tmem + TM_S + 128 * b + fpk_col(kk), fdesc_at(dv, kk * 2048), idO,
                                (g > g0 || kk > 0));
                     mma_commit(sm.bar(F_PV_DONE + b));
                     mma_commit(sm.bar(F_V_EMPTY + s));
@@ -407,10 +418,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ================================================================ softmax warps
+        // Two warps per TMEM lane quarter: warps 2-5 take kv columns 0-63 of
+        // a block, warps 6-9 columns 64-127 (thread = q row).  The two halves
+        // of a row trade their block maxima (and, at a unit's end, their sums)
+        // through shared memory under a 64-thread named barrier per quarter.
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;                 // q row within the block = TMEM lane
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const float C = a.scale * kLog2e;
+        // exchange k of a quarter goes through slot k % 2 ([2 halves][128 rows])
+        // and completion k of the quarter's barrier (64 arrivals); exchange
+        // k + 2 rewrites the slot only after both halves have passed k + 1,
+        // so after both have read k
+        float *xch = reinterpret_cast<float *>(sm.base + G_::OFF_XCH);
+        uint32_t xk = 0;
+        auto trade = [&](float mine, float &other) -> bool {
+            float *slot = xch + (xk & 1u) * 256;
+            slot[half * 128 + row] = mine;
+            mbar_arrive(sm.bar(F_XCH + quarter));
+            const bool okw = fwait_warp(sm, F_XCH + quarter, xk, a);
+            other = slot[(half ^ 1) * 128 + row];
+            ++xk;
+            return okw;
+        };
         Out *O = reinterpret_cast<Out *>(a.o);
         uint32_t ui = 0, ku = 0, gb = 0;
         bool ok = true;
@@ -427,42 +458,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = i < U.sd.sq;
             int64_t lo = 1, hi = 0;                           // kept key range of the row
             if (row_ok) key_range(a.mask, U.sd.sq, U.sd.skv, U.sd.prefix, i, lo, hi);
-            // running state (log2 units): m_use = max in use, m_true = row max
+            // running state (log2 units): m_use = max in use, m_true = row max;
+            // l is this half's share of the row sum (the sink counts in half 0)
             float m_use = -INFINITY, m_true = -INFINITY, l = 0.0f;
             if (a.has_sink && row_ok) {
                 m_use = m_true = a.sink[U.h] * kLog2e;
-                l = 1.0f;
+                l = half == 0 ? 1.0f : 0.0f;
             }
             for (int t = 0; t < U.n; ++t) {
                 const uint32_t g = gb + t, b = g & 1u;
                 const int64_t j0 = (int64_t)(U.jlo + t) * BN;
+                const int64_t jh = j0 + 64 * half;            // this half's first column
                 uint32_t kw[5], ksh = 0;
                 if (a.has_drop) fetch_keep128(a, U.sd, U.h, i, j0, kw, ksh);
-                // attention-mask matrix bits of the row's 128 columns (all kept without one)
-                uint2 am0 = make_uint2(~0u, ~0u), am1 = am0;
+                // attention-mask matrix bits of this half's 64 columns (all kept without one)
+                uint2 am = make_uint2(~0u, ~0u);
                 if (a.mask.keep_q != nullptr) {
-                    if (row_ok) {
-                        const uint2 *src = reinterpret_cast<const uint2 *>(a.mask.keep_q + i * a.mask.words_q + (j0 >> 6));
-                        am0 = __ldg(src);
-                        am1 = __ldg(src + 1);
-                    } else {
-                        am0 = am1 = make_uint2(0u, 0u);
-                    }
+                    am = row_ok ? __ldg(reinterpret_cast<const uint2 *>(a.mask.keep_q + i * a.mask.words_q + (jh >> 6)))
+                                : make_uint2(0u, 0u);
                 }
                 if (!fwait_warp(sm, F_S_FULL + b, g >> 1, a)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * b;
-                // keep bits of the 128 columns: the range [lo, hi] relative to j0,
-                // and the matrix
-                uint32_t km[4];
+                const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * b + 64 * half;
+                // keep bits of the half's two 32-column chunks: the range [lo, hi]
+                // relative to jh, and the matrix
+                uint32_t km[2];
                 {
-                    const int64_t clo = max(lo - j0, (int64_t)0), chi = min(hi - j0, (int64_t)BN - 1);
-                    const uint32_t amw[4] = {am0.x, am0.y, am1.x, am1.y};
+                    const int64_t clo = max(lo - jh, (int64_t)0), chi = min(hi - jh, (int64_t)63);
+                    const uint32_t amw[2] = {am.x, am.y};
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
+                    for (int ch = 0; ch < 2; ++ch) {
                         const int64_t l0 = clo - 32 * ch, h0 = chi - 32 * ch;
                         km[ch] = (l0 > 31 || h0 < 0 || l0 > h0)
                                      ? 0u
@@ -470,16 +498,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         km[ch] &= amw[ch];
                     }
                 }
-                // pass 1: block max over kept columns
+                // pass 1: block max over the half's kept columns, then the row's
                 float bmax = -INFINITY;
                 const float cs = PSE ? 1.0f : C;      // with a pse, the S buffer holds C S + pse term
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < 2; ++ch) {
                     uint32_t raw[32];
                     tmem_ld32(s_addr + 32 * ch, raw);
                     if constexpr (PSE) {
                         float t[32];
-                        fpse_chunk<BF16>(a, U, i, row_ok, j0 + 32 * ch, C, t);
+                        fpse_chunk<BF16>(a, U, i, row_ok, jh + 32 * ch, C, t);
 #pragma unroll
                         for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(fmaf(__uint_as_float(raw[c]), C, t[c]));
                         tmem_st32(s_addr + 32 * ch, raw);
@@ -488,6 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 32; ++c) {
                         if ((km[ch] >> c) & 1u) bmax = fmaxf(bmax, __uint_as_float(raw[c]) * cs);
                     }
+                }
+                {
+                    float other;
+                    if (!trade(bmax, other)) {
+                        ok = false;
+                        break;
+                    }
+                    bmax = fmaxf(bmax, other);
                 }
                 // lazy rescale: only when the max in use falls more than 2^8 behind
                 m_true = fmaxf(m_true, bmax);
@@ -503,28 +539,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (__any_sync(0xffffffffu, rescale_o)) {
                     // O must hold every earlier block's P V before it is scaled
+                    // (each half scales its HD / 2 columns)
                     if (!fwait_warp(sm, F_PV_DONE + (b ^ 1u), (g - 1) >> 1, a)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int ch = 0; ch < HD / 32; ++ch) {
+                    for (int ch = 0; ch < HD / 64; ++ch) {
                         uint32_t raw[32];
-                        tmem_ld32(tmem + lane_addr + TM_O + 32 * ch, raw);
+                        const uint32_t oa = tmem + lane_addr + TM_O + (HD / 2) * half + 32 * ch;
+                        tmem_ld32(oa, raw);
 #pragma unroll
                         for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(__uint_as_float(raw[c]) * alpha);
-                        tmem_st32(tmem + lane_addr + TM_O + 32 * ch, raw);
+                        tmem_st32(oa, raw);
                     }
                 }
-                // pass 2: P = exp2(s C - m_use) on kept columns; l += P; Pd = P z packed
+                // pass 2: P = exp2(s C - m_use) on kept columns; l += P; Pd = P z
+                // packed into the first 16 columns of its own 32-column chunk
                 const float mneg = (m_use == -INFINITY) ? 0.0f : -m_use;
+                // keep-bit words of this half's 64 columns (selected, not indexed,
+                // so kw stays in registers)
+                const uint32_t kwh[3] = {half ? kw[2] : kw[0], half ? kw[3] : kw[1], half ? kw[4] : kw[2]};
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < 2; ++ch) {
                     uint32_t raw[32];
                     tmem_ld32(s_addr + 32 * ch, raw);
                     uint32_t zw = 0xffffffffu;
-                    if (a.has_drop) zw = __funnelshift_r(kw[ch], kw[ch + 1], ksh);
+                    if (a.has_drop) zw = __funnelshift_r(kwh[ch], kwh[ch + 1], ksh);
                     float p[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -546,13 +588,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 16; ++c) pk[c] = fpack2<BF16>(p[2 * c], p[2 * c + 1]);
                     }
-                    tmem_st16(s_addr + 16 * ch, pk);   // packed over S columns already read
+                    tmem_st16(s_addr + 32 * ch, pk);   // over this chunk's already read S columns
                 }
                 tc_fence_before();
                 mbar_arrive(sm.bar(F_P_READY + b));
             }
             if (!ok) break;
             // ---- unit end: O / l, max and sum of the true row max (8 copies)
+            {
+                float other;                                  // the row's sum: both halves
+                if (!trade(l, other)) break;
+                l += other;
+            }
             float m_out = m_true, l_out = l;
             if (m_true > -INFINITY && m_use > -INFINITY) l_out = l * ex2(m_use - m_true);
             const float inv = (l > 0.0f ? 1.0f / l : 0.0f) * (a.has_drop ? a.inv_keep : 1.0f);
@@ -561,11 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!fwait_warp(sm, F_O_FULL, ku, a)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int ch = 0; ch < HD / 32; ++ch) {
+                for (int ch = 0; ch < HD / 64; ++ch) {
                     uint32_t raw[32];
-                    tmem_ld32(tmem + lane_addr + TM_O + 32 * ch, raw);
+                    const int col = (HD / 2) * half + 32 * ch;
+                    tmem_ld32(tmem + lane_addr + TM_O + col, raw);
                     if (row_ok) {
-                        Out *dst = O + r * HD + 32 * ch;
+                        Out *dst = O + r * HD + col;
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             uint4 pkt;
@@ -581,10 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(sm.bar(F_O_FREE));
                 ++ku;
             } else if (row_ok) {
-                Out *dst = O + r * HD;
-                for (int c = 0; c < HD; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
+                Out *dst = O + r * HD + (HD / 2) * half;
+                for (int c = 0; c < HD / 2; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
             }
-            if (row_ok) {
+            if (row_ok && half == 0) {
                 const float mn = (m_out == -INFINITY) ? -INFINITY : m_out * kLn2;
                 const float4 mv = make_float4(mn, mn, mn, mn), lv = make_float4(l_out, l_out, l_out, l_out);
                 float4 *pm = reinterpret_cast<float4 *>(a.smax + r * 8);
@@ -597,7 +645,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             gb += U.n;
         }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
