@@ -18,7 +18,8 @@
 //
 // Warp roles (320 threads, one CTA per SM, persistent over (q block, head)
 // units taken in plan order, longest kv range first):
-//   warp 0      TMA producer: Q per unit; K, V per kv block (three stages)
+//   warp 0      TMA producer: Q per unit (two stages, so the next unit's Q
+//               loads while one runs); K, V per kv block (two stages)
 //   warp 1      TMEM allocator and single-thread UMMA issuer
 //   warps 2-9   softmax warps: thread = TMEM lane = q row, two warps per lane
 //               quarter, each on 64 of a block's 128 kv columns (they trade
@@ -41,7 +42,7 @@ using namespace ptx;
 
 constexpr int BN = kKvBlock;             // 128 kv rows (UMMA N of S, K of O += P V)
 constexpr int kThreads = 320;
-constexpr int NS = 3;                    // K / V stages
+constexpr int NS = 2;                    // K / V stages
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0, TM_S = 256; // S buffers at 256 and 384
 constexpr uint32_t kColBlk = 128 * 128;  // one 64-element column block of 128 rows (16 KB)
@@ -51,11 +52,11 @@ template <int HD>
 struct FGeo {
     static constexpr uint32_t NCB = HD / 64;
     static constexpr uint32_t kTile = 128 * HD * 2;       // Q, K or V tile
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + kTile;       // NS stages
+    static constexpr uint32_t OFF_Q = 0;                   // 2 stages (a unit's Q in stage ku % 2)
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * kTile;   // NS stages
     static constexpr uint32_t OFF_V = OFF_K + NS * kTile;  // NS stages
     static constexpr uint32_t OFF_BAR = OFF_V + NS * kTile;
-    static constexpr uint32_t kNumBars = 32;
+    static constexpr uint32_t kNumBars = 32;   // >= F_NUM_BARS
     static constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
     static constexpr uint32_t OFF_XCH = OFF_MISC + 64;     // softmax halves' exchange, 2 x [2][128] fp32
     static constexpr uint32_t kSmemBytes = OFF_XCH + 2 * 2 * 128 * 4;
@@ -63,22 +64,24 @@ struct FGeo {
 };
 
 enum : int {
-    F_Q_FULL = 0,       //      count 1 + tx
-    F_Q_EMPTY = 1,      //      count 1 (commit after the unit's last S)
-    F_K_FULL = 2,       // [3]  count 1 + tx
-    F_K_EMPTY = 5,      // [3]  count 1 (commit after S)
-    F_V_FULL = 8,       // [3]  count 1 + tx
-    F_V_EMPTY = 11,     // [3]  count 1 (commit after O += P V)
-    F_S_FULL = 14,      // [2]  count 1 (commit)
-    F_P_READY = 16,     // [2]  count 256
-    F_PV_DONE = 18,     // [2]  count 1 (commit after O += P V: P read, O current)
-    F_O_FULL = 20,      //      count 1 (commit after the unit's last O += P V)
-    F_O_FREE = 21,      //      count 256 (O read out)
-    F_UNIT_FULL = 22,   // [2]  count 1
-    F_UNIT_EMPTY = 24,  // [2]  count 9 (MMA + 8 softmax warps)
-    F_DRAIN = 26,       //      count 1
-    F_XCH = 27,         // [4]  count 64 (the two softmax warps of a lane quarter)
+    F_Q_FULL = 0,               // [2]  count 1 + tx (stage ku % 2)
+    F_Q_EMPTY = 2,              // [2]  count 1 (commit after the unit's last UMMA)
+    F_K_FULL = 4,               // [NS] count 1 + tx
+    F_K_EMPTY = F_K_FULL + NS,  // [NS] count 1 (commit after S)
+    F_V_FULL = F_K_EMPTY + NS,  // [NS] count 1 + tx
+    F_V_EMPTY = F_V_FULL + NS,  // [NS] count 1 (commit after O += P V)
+    F_S_FULL = F_V_EMPTY + NS,  // [2]  count 1 (commit)
+    F_P_READY = F_S_FULL + 2,   // [2]  count 256
+    F_PV_DONE = F_P_READY + 2,  // [2]  count 1 (commit after O += P V: P read, O current)
+    F_O_FULL = F_PV_DONE + 2,   //      count 1 (commit after the unit's last O += P V)
+    F_O_FREE = F_O_FULL + 1,    //      count 256 (O read out)
+    F_UNIT_FULL = F_O_FREE + 1, // [2]  count 1
+    F_UNIT_EMPTY = F_UNIT_FULL + 2,  // [2] count 9 (MMA + 8 softmax warps)
+    F_DRAIN = F_UNIT_EMPTY + 2,      //     count 1
+    F_XCH = F_DRAIN + 1,             // [4] count 64 (the two softmax warps of a lane quarter)
+    F_NUM_BARS = F_XCH + 4
 };
+static_assert(F_NUM_BARS <= 32, "barrier slots");
 constexpr uint32_t MISC_TMEM = 0, MISC_RING = 1, MISC_ABORT = 3;
 
 struct FSmem {
@@ -244,8 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Out = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
 
     if (threadIdx.x == 0) {
-        mbar_init(sm.bar(F_Q_FULL), 1);
-        mbar_init(sm.bar(F_Q_EMPTY), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(sm.bar(F_Q_FULL + i), 1);
+            mbar_init(sm.bar(F_Q_EMPTY + i), 1);
+        }
         for (int i = 0; i < NS; ++i) {
             mbar_init(sm.bar(F_K_FULL + i), 1);
             mbar_init(sm.bar(F_K_EMPTY + i), 1);
@@ -300,15 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (u >= a.n_fwd_units) break;
             const FUnit U = funit(a, u);
             if (U.n == 0) continue;
-            if (ku >= 1 && !fwait_warp(sm, F_Q_EMPTY, ku - 1, a)) break;
+            // Q of this unit in stage ku % 2, free once unit ku - 2 is done: it
+            // loads while the previous unit still runs
+            const uint32_t qs = ku & 1u;
+            if (ku >= 2 && !fwait_warp(sm, F_Q_EMPTY + qs, (ku >> 1) - 1, a)) break;
             if (lane == 0) {
-                uint64_t *qb = sm.bar(F_Q_FULL);
+                uint64_t *qb = sm.bar(F_Q_FULL + qs);
                 mbar_arrive_expect_tx(qb, G_::kTile);
                 const int z = (int)(U.sd.tq + U.q0);
                 for (uint32_t cb = 0; cb < G_::NCB; ++cb)
-                    tma_load_3d(sm.base + G_::OFF_Q + cb * kColBlk, &tmQ, qb, 64 * cb, U.h, z);
+                    tma_load_3d(sm.base + G_::OFF_Q + qs * G_::kTile + cb * kColBlk, &tmQ, qb, 64 * cb, U.h, z);
             }
-            ++armed[0];
+            ++armed[qs];
             const int g = U.h / a.group;
             for (int t = 0; t < U.n; ++t, ++kb) {
                 const uint32_t s = kb % NS, k = kb / NS;
@@ -355,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // read P out of it
             auto issue_s = [&](uint32_t g, bool first) -> bool {
                 const uint32_t s = g % NS, b = g & 1u;
-                if (first && !fwait(sm, F_Q_FULL, ku, a)) return false;
+                if (first && !fwait(sm, F_Q_FULL + (ku & 1u), ku >> 1, a)) return false;
                 if (g >= 2 && !fwait(sm, F_PV_DONE + b, (g >> 1) - 1, a)) return false;
                 if (!fwait(sm, F_K_FULL + s, g / NS, a)) return false;
                 tc_fence_after();
@@ -363,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     const uint32_t off = (kk >> 2) * kColBlk + (kk & 3) * 32;
-                    mma_ss(tmem + TM_S + 128 * b, fdesc_at(dQ, off), fdesc_at(dk, off), idS, kk > 0);
+                    mma_ss(tmem + TM_S + 128 * b, fdesc_at(dQ, (ku & 1u) * G_::kTile + off), fdesc_at(dk, off), idS,
+                           kk > 0);
                 }
                 mma_commit(sm.bar(F_S_FULL + b));
                 mma_commit(sm.bar(F_K_EMPTY + s));
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit(sm.bar(F_O_FULL));
-                mma_commit(sm.bar(F_Q_EMPTY));
+                mma_commit(sm.bar(F_Q_EMPTY + (ku & 1u)));
                 gb = g_end;
                 ++ku;
             }
@@ -654,6 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after an abort, TMA loads nobody waited for may still be in flight
     if (warp == 0 && lane == 0 && *sm.abort_flag()) {
         if (armed[0]) fdrain(sm, F_Q_FULL, armed[0] - 1, a);
+        if (armed[1]) fdrain(sm, F_Q_FULL + 1, armed[1] - 1, a);
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             if (armed[2 + s]) fdrain(sm, F_K_FULL + s, armed[2 + s] - 1, a);
