@@ -44,6 +44,22 @@ ORACLE_MAX_S = 8.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
+def max_over_ranks(x: float, dist, dev) -> float:
+    """The largest of every rank's x: the time of the slowest replica (x
+    itself with one process)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flop_per_replica: float, ms: float) -> float:
+    """Whole-job throughput: every replica's FLOP over the slowest replica's time."""
+    return world * flop_per_replica / (ms * 1e-3) / 1e12
+
+
 def kept_pairs(wl) -> int:
     """Kept (q-row, kv-row) pairs summed over sequences and query heads,
     counted row by row from the sparseMode definitions."""
@@ -374,13 +390,9 @@ def run_ours(args, wl, rank, world, local_rank):
     prof = tnd.tnd_attn_profile_read(reset=True)
     tnd.tnd_attn_set_option(tnd.TND_OPT_PROFILE, 0)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_per_step = float(statistics.median(step_ms))
-    if dist is not None:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(float(statistics.median(step_ms)), dist, dev)
     flop = grad_flop(wl)
-    value = world * flop / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, flop, ms_per_step)
     # the library's kernels in the timed region: per-step launches of the profiled pass x steps
     launches = int(round(sum(n for _, n in prof.values()) / prof_steps)) * args.steps
     kernels = {name: {"ms_per_launch": ms / n, "launches": n} for name, (ms, n) in prof.items() if n}
@@ -528,12 +540,8 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e_run(e2e_steps, e0)
     e1.record(comp)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e_value = job_tflops(world, flop, e2e_ms)
 
     if rank == 0:
         line = {
