@@ -134,7 +134,7 @@ class ClockSampler:
         self._handle = None
 
     def _open(self):
-        """NVML through the driver's own library (ctypes), which every GPU machine has."""
+        """NVML through the driver's own library (ctypes), present wherever the driver is."""
         import ctypes
         import torch
         nv = ctypes.CDLL("libnvidia-ml.so.1")
