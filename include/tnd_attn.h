@@ -218,13 +218,14 @@ const char *tnd_status_string(tnd_status status);
  *                    (its outputs are then invalid); 0 = off (default).
  *   TND_OPT_DETERMINISTIC: deterministic computing ([UnpadGradV5]
  *                    constraints: the gradient is non-deterministic unless
- *                    deterministic computing is switched on).  1 (default) = the tensor-core
- *                    gradient adds the dQ contributions of every (q block,
- *                    head) in a fixed order, so repeated calls give bitwise
- *                    identical results; 0 = they are added in arrival order
- *                    (same tolerance against the exact result, rounding
- *                    order varies from call to call).  The CUDA-core kernels
- *                    are deterministic either way.
+ *                    deterministic computing is switched on).  1 (default) =
+ *                    the tensor-core gradient adds the dQ contributions of
+ *                    every (q block, head) in a fixed order, so repeated
+ *                    calls give bitwise identical results; 0 = they are
+ *                    added in arrival order (same tolerance against the
+ *                    exact result, rounding order varies from call to call).
+ *                    The forward and the CUDA-core kernels are deterministic
+ *                    either way.
  */
 typedef enum tnd_option {
     TND_OPT_GRAD_PATH = 0,
