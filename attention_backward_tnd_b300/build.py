@@ -36,10 +36,21 @@ def _stale(target, deps):
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every kernel source and link the shared library; returns its path."""
+    """Compile every kernel source and link the shared library; returns its path.
+    Processes that build at once (one per rank) take turns on a lock file, and
+    each one that follows finds the library current."""
     if not force and not _stale(LIB, _deps()):
         return LIB
     os.makedirs(OBJ_DIR, exist_ok=True)
+    import fcntl
+    with open(os.path.join(OBJ_DIR, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _stale(LIB, _deps()):
+            return LIB
+        return _build_locked(force, verbose, extra_flags)
+
+
+def _build_locked(force, verbose, extra_flags) -> str:
     headers = [d for d in _deps() if not d.endswith(".cu")]
     procs, objs = [], []
     for src in _sources():
