@@ -46,3 +46,17 @@ def test_dropout_mask_statistics_and_layout():
     frac = np.unpackbits(m, bitorder="little")[:1_000_003].mean()
     assert abs(frac - 0.9) < 0.002
     np.testing.assert_array_equal(m, workloads.dropout_mask(7, 1_000_003, 0.9, chunk_bits=4096))
+
+
+def test_value_head_dim_and_generated_pse_inputs():
+    """A value head dim below D shapes V and dY; a generated pse is fp32 slopes."""
+    wl = workloads.custom("dv", "bf16", [5, 9], [5, 9], 4, 2, 64, dv=24, sparse_mode=3,
+                          pse_kind="slopes", pse_batch=2, pse_type=2)
+    inp = workloads.make_inputs(wl)
+    assert wl.dv == 24 and inp.q.shape == (14, 4, 64) and inp.k.shape == (14, 2, 64)
+    assert inp.v.shape == (14, 2, 24) and inp.dy.shape == (14, 4, 24)
+    assert inp.pse.dtype == np.float32 and inp.pse.shape == (2, 4) and np.all(inp.pse > 0)
+    np.testing.assert_array_equal(inp.pse64, inp.pse.astype(np.float64))
+    shared = workloads.make_inputs(workloads.custom("dv1", "f16", [5], [5], 3, 1, 32, sparse_mode=2,
+                                                    pse_kind="slopes", pse_batch=1, pse_type=3))
+    assert shared.pse.shape == (3,) and shared.v.shape == (5, 1, 32)
