@@ -612,6 +612,39 @@ def test_grad_matches_central_differences(ora, ci):
             assert abs(fd - dsink[hh]) <= 1e-6 * max(1.0, abs(dsink[hh])), (hh, fd, dsink[hh])
 
 
+@pytest.mark.parametrize("variant", ["dv_below_d", "alibi_sqrt"])
+def test_new_paths_match_central_differences(ora, variant):
+    """Central differences of sum(dY * O) through the oracle's own forward, for
+    a value head dim below D (with dropout and a sink) and for the generated
+    sqrt alibi (pseType 3)."""
+    if variant == "dv_below_d":
+        (cu_q, cu_kv, nq, nkv, d, dv, scale, kw), (q, k, v, dy), _ = _dv_case(ora, 1)
+        p = _problem(ora, cu_q, cu_kv, nq, nkv, d, scale, dv=dv, **kw)
+    else:
+        seqs, nq, nkv, d = [23, 9], 2, 1, 8
+        rng0, cu_q, cu_kv, q, k, v, dy = random_problem(97, seqs, seqs, nq, nkv, d)
+        p = _problem(ora, cu_q, cu_kv, nq, nkv, d, 0.4, sparse_mode=3, pse=np.array([0.3, 0.05]), pse_type=3)
+    out, smax, ssum = ora.fwd(p, q, k, v)
+    dq, dk, dvv, _ = ora.grad(p, q, k, v, dy, out, smax, ssum)
+    h = 1e-6
+    rng = np.random.default_rng(5)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(ora.fwd(p, qq, kk, vv)[0] * dy))
+
+    for name, arr, g in (("q", q, dq), ("k", k, dk), ("v", v, dvv)):
+        for _ in range(10):
+            idx = tuple(rng.integers(0, n) for n in arr.shape)
+            a1, a2 = arr.copy(), arr.copy()
+            a1[idx] += h
+            a2[idx] -= h
+            args1 = {"q": q, "k": k, "v": v}
+            args2 = dict(args1)
+            args1[name], args2[name] = a1, a2
+            fd = (loss(args1["q"], args1["k"], args1["v"]) - loss(args2["q"], args2["k"], args2["v"])) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
 # --------------------------------------------------------------------------
 # closed forms and exact identities
 # --------------------------------------------------------------------------
